@@ -1,0 +1,702 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 DTensor-to-DTensor reshard (libreshard.so).
+
+Default workload: a DeepSeek-v3-shaped MoE refit slice -- one MoE layer of 256
+experts (gate/up [256, 2048, 7168], down [256, 7168, 2048], bf16, 22.5 GB)
+resharded from (PP1, EP16, TP2) to (DP2, TP8) with the read-once fan-out
+kernel, plus its attention/norm weights (~0.9 GB) on the gather-and-broadcast
+path (the hybrid refit split).  One step = one refit of that slice.  Inputs are
+seeded synthetic values N(0, 0.02) drawn on the device; they exceed the L2
+cache many times over, so no flush is needed between steps.
+
+Metric: effective GB/s = (global bytes read once + destination bytes written)
+per step / step time; the HBM roofline fraction divides by the measured copy
+bandwidth of the GPU.  One JSON line is printed (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --report FILE     # every workload: K1/K2/baseline latency table
+
+Multi-GPU (torchrun, one rank per GPU): every rank refits its own MoE layer
+(independent problems, no collective on the data path); the value is the sum
+of all ranks' bytes over the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "reshard effective GB/s and % HBM roofline; bytes moved vs gather-broadcast"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------------------ setup
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("moe_refit", "hybridflow", "ffn_up"),
+                    default="moe_refit")
+    ap.add_argument("--kernel", choices=("fanout", "boxcopy"), default="fanout")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    ap.add_argument("--report", default=None,
+                    help="write a per-workload table (JSON lines) to this file")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("kernels.cu", "internal.h"):
+        with open(os.path.join(ROOT, "dtensor_reshard_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_profile_traffic():
+    """Per-launch DRAM bytes of the fan-out kernel from the committed ncu summary
+    (profiles/traffic.json), or None if the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:  # noqa: BLE001
+        return None
+    return d if d.get("kernel_source_sha256_16") == kernel_source_hash() else None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+                power.append(float(row[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, row[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ workload
+class Job:
+    """One tensor of the workload: its plan and device buffers."""
+
+    def __init__(self, spec, plan, srcs, dsts, scratch=None):
+        self.spec, self.plan, self.srcs, self.dsts, self.scratch = spec, plan, srcs, dsts, scratch
+        self.stats = None
+
+    @property
+    def effective_bytes(self):
+        s = self.stats
+        return s["global_bytes"] + s["dst_bytes"]
+
+
+def build_jobs(workload, dev, with_gb=True):
+    """Plans and device buffers; source shards cut from a seeded global tensor with the
+    library's own layout (reshard_plan_local_shape)."""
+    import torch
+
+    import dtensor_reshard_gb300 as rs
+    from inputs import global_tensor
+
+    jobs = []
+    scratch_bytes = max([t.global_bytes for t in workload.tensors
+                         if t.path == "gather_broadcast"] or [0])
+    scratch = torch.empty(scratch_bytes, dtype=torch.uint8, device=dev) if (
+        with_gb and scratch_bytes) else None
+    for spec in workload.tensors:
+        if spec.path == "gather_broadcast" and not with_gb:
+            continue
+        plan = rs.reshard_plan_create(spec.global_shape, spec.dtype, spec.src_mesh,
+                                      spec.src_placements, spec.dst_mesh, spec.dst_placements)
+        glob = global_tensor(spec, device=dev)
+        srcs = []
+        for r in range(plan.n_src):
+            shp, off = rs.reshard_plan_local_shape(plan, 0, r)
+            sl = tuple(slice(o, o + s) for o, s in zip(off, shp))
+            srcs.append(glob[sl].contiguous() if math.prod(shp) else
+                        torch.empty(shp, dtype=glob.dtype, device=dev))
+        del glob
+        dsts = [torch.empty(rs.reshard_plan_local_shape(plan, 1, r)[0],
+                            dtype=srcs[0].dtype, device=dev) for r in range(plan.n_dst)]
+        rs.reshard_plan_upload(plan)
+        j = Job(spec, plan, srcs, dsts, scratch if spec.path == "gather_broadcast" else None)
+        j.stats = rs.reshard_plan_stats(plan)
+        jobs.append(j)
+    torch.cuda.synchronize()
+    return jobs
+
+
+def run_job(job, stream, kernel):
+    import dtensor_reshard_gb300 as rs
+    if job.spec.path == "gather_broadcast":
+        rs.gather_broadcast_execute(job.plan, job.srcs, job.dsts, job.scratch,
+                                    job.scratch.numel(), stream)
+    else:
+        rs.reshard_execute_ex(job.plan, job.srcs, job.dsts, kernel, stream)
+
+
+def launches_of(job, kernel):
+    t = job.stats["n_tiles"]
+    if job.spec.path == "gather_broadcast":
+        return int(t[2] > 0) + int(t[3] > 0)
+    return int(t[0 if kernel == 0 else 1] > 0)
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def oracle_sample(jobs, seconds):
+    """Time the CPU oracle on a bounded sample of the workload's reshard tensors.
+
+    Sample: for every reshard tensor, destination rank 0, its first k slices along
+    the outermost dim (k grown until about ``seconds`` of CPU time in total).
+    Returns (effective GB/s, sample description, cores used).
+    """
+    import numpy as np
+    import torch
+
+    import oracle as oracle_mod
+
+    o = oracle_mod.load()
+    rjobs = [j for j in jobs if j.spec.path == "reshard"]
+    if not rjobs:
+        return None
+
+    def sample(job, k):
+        spec = job.spec
+        doff, dshp = o.resolve(spec.global_shape, spec.dst_mesh, spec.dst_placements, 0)
+        k = min(k, dshp[0])
+        per = math.prod(dshp[1:])
+        # global box of the sample -> source shards it touches (host copies of those only)
+        lo = list(doff)
+        hi = [a + b for a, b in zip(doff, dshp)]
+        hi[0] = doff[0] + k
+        ptrs, keep = [], []
+        for s, (so, ss) in enumerate(o.boxes(spec.global_shape, spec.src_mesh,
+                                             spec.src_placements)):
+            touch = all(max(a, c) < min(b, c + d) for a, b, c, d in zip(lo, hi, so, ss))
+            if touch and math.prod(ss):
+                h = job.srcs[s].reshape(-1).view(torch.uint8).cpu().numpy()
+                keep.append(h)
+                ptrs.append(h.ctypes.data)
+            else:
+                ptrs.append(None)
+        out = np.empty(math.prod(dshp) * spec.elem_bytes if k == dshp[0] else
+                       k * per * spec.elem_bytes, dtype=np.uint8)
+        n = k * per
+        t0 = time.perf_counter()
+        o.reshard_elems(spec.global_shape, spec.elem_bytes, spec.src_mesh, spec.src_placements,
+                        spec.dst_mesh, spec.dst_placements, ptrs, out.ctypes.data, 0, 0, n)
+        dt = time.perf_counter() - t0
+        st = job.stats
+        eff = n * spec.elem_bytes * (1.0 + st["global_bytes"] / st["dst_bytes"])
+        return dt, eff, n, k
+
+    # calibrate on one slice of the first tensor, then size k per tensor
+    dt1, _, _, _ = sample(rjobs[0], 1)
+    per_tensor = seconds / len(rjobs)
+    k = max(1, int(per_tensor / max(dt1, 1e-4)))
+    tot_t, tot_b, desc = 0.0, 0.0, []
+    for j in rjobs:
+        dt, eff, n, kk = sample(j, k)
+        tot_t += dt
+        tot_b += eff
+        desc.append(f"{j.spec.name}: dst rank 0, first {kk} of dim 0 ({n} elements)")
+    return tot_b / tot_t / 1e9, "; ".join(desc), 1, tot_t
+
+
+# ------------------------------------------------------------------------------ timing
+def device_time(jobs, stream, steps, warmup, kernel, dist_ctx, gpu_uuid):
+    """Device-timed steps; returns (ms_per_step, dominant kernel avg ms, clocks)."""
+    import torch
+
+    for _ in range(warmup):
+        for j in jobs:
+            run_job(j, stream, kernel)
+    torch.cuda.synchronize()
+    dom = [j for j in jobs if j.spec.path == "reshard"]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps * len(dom))]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_uuid)
+    sampler.start()
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    e = 0
+    for _ in range(steps):
+        for j in jobs:
+            if j.spec.path == "reshard":
+                ev[e][0].record(stream)
+                run_job(j, stream, kernel)
+                ev[e][1].record(stream)
+                e += 1
+            else:
+                run_job(j, stream, kernel)
+    end.record(stream)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    dom_ms = [a.elapsed_time(b) for a, b in ev]
+    return total_ms / steps, dom_ms, clocks
+
+
+def e2e_time(jobs, stream, steps, warmup, kernel, dist_ctx):
+    """End to end through the public API with host buffers: every step copies the
+    sources in from pinned host memory, reshards, and reads every destination back."""
+    import torch
+
+    host_src = [[torch.empty(s.shape, dtype=s.dtype, pin_memory=True) for s in j.srcs]
+                for j in jobs]
+    host_dst = [[torch.empty(d.shape, dtype=d.dtype, pin_memory=True) for d in j.dsts]
+                for j in jobs]
+    for j, hs in zip(jobs, host_src):
+        for h, s in zip(hs, j.srcs):
+            h.copy_(s)
+    h2d = sum(s.numel() * s.element_size() for j in jobs for s in j.srcs)
+    d2h = sum(d.numel() * d.element_size() for j in jobs for d in j.dsts)
+
+    def one_step():
+        for j, hs, hd in zip(jobs, host_src, host_dst):
+            for s, h in zip(j.srcs, hs):
+                s.copy_(h, non_blocking=True)
+            run_job(j, stream, kernel)
+            for d, h in zip(j.dsts, hd):
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        one_step()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    t0 = time.perf_counter()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one_step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    dist_ctx.barrier()
+    return start.elapsed_time(end) / steps, wall / steps, h2d, d2h
+
+
+class DistCtx:
+    """Barrier and max/sum over ranks (no-ops for one process).  Reductions run on
+    the GPU under NCCL and on the CPU under gloo."""
+
+    def __init__(self, world):
+        self.world = world
+        self.device = "cpu"
+        if world > 1:
+            import torch.distributed as dist
+            self.dist = dist
+            self.device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def _reduce(self, x: float, op) -> float:
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=op)
+        return float(t.item())
+
+    def max(self, x: float) -> float:
+        return x if self.world == 1 else self._reduce(x, self.dist.ReduceOp.MAX)
+
+    def sum(self, x: float) -> float:
+        return x if self.world == 1 else self._reduce(x, self.dist.ReduceOp.SUM)
+
+
+def pick_workload(name):
+    from inputs import ffn_up, hybridflow, moe_refit
+    return {"moe_refit": moe_refit, "hybridflow": hybridflow, "ffn_up": ffn_up}[name]()
+
+
+# ------------------------------------------------------------------------------ arms
+def reference_arm(args, rank, world):
+    """The oracle on the host cores: the reference arm of this benchmark."""
+    if rank != 0:
+        return 0
+    import torch
+    dev = torch.device("cuda:0") if torch.cuda.is_available() else None
+    w = pick_workload(args.workload)
+    if dev is None:
+        print(json.dumps({"impl": "reference", "unavailable": "no CUDA device to build inputs"}))
+        return 0
+    torch.cuda.set_device(dev)
+    jobs = build_jobs(w, dev, with_gb=False)
+    per_step = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        v, desc, cores, _ = oracle_sample(jobs, per_step)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def ours_arm(args, rank, world, local):
+    import torch
+
+    import dtensor_reshard_gb300 as rs
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    dctx = DistCtx(world)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_uuid = str(getattr(props, "uuid", "")) or str(local)
+    if gpu_uuid and not gpu_uuid.startswith("GPU-") and len(gpu_uuid) > 8:
+        gpu_uuid = "GPU-" + gpu_uuid
+    kernel = rs.KERNEL_FANOUT if args.kernel == "fanout" else rs.KERNEL_BOXCOPY
+    w = pick_workload(args.workload)
+    t0 = time.perf_counter()
+    jobs = build_jobs(w, dev)
+    setup_s = time.perf_counter() - t0
+    stream = torch.cuda.current_stream(dev)
+
+    ms_step, dom_ms, clocks = device_time(jobs, stream, args.steps, args.warmup, kernel, dctx,
+                                          gpu_uuid)
+    ms_step_max = dctx.max(ms_step)
+    eff_bytes = sum(j.effective_bytes for j in jobs)
+    total_bytes = dctx.sum(eff_bytes)
+    value = total_bytes / (ms_step_max * 1e-3) / 1e9
+
+    peak, peak_kind = load_peaks()
+    dom_jobs = [j for j in jobs if j.spec.path == "reshard"]
+    dom_bytes = sum((j.stats["fanout_read_bytes"] + j.stats["fanout_write_bytes"])
+                    if kernel == rs.KERNEL_FANOUT else
+                    (j.stats["boxcopy_read_bytes"] + j.stats["boxcopy_write_bytes"])
+                    for j in dom_jobs)
+    dom_launch_ms = sum(dom_ms) / len(dom_ms)
+    dom_bytes_per_launch = dom_bytes / len(dom_jobs)
+    achieved = dom_bytes_per_launch / (dom_launch_ms * 1e-3) / 1e9
+    traffic = load_profile_traffic()
+    traffic_val = None
+    if traffic and traffic.get("workload") == w.name:
+        traffic_val = traffic.get("dram_bytes_per_launch")
+
+    # gather-and-broadcast comparison on the same tensors (reshard tensors only)
+    gb_ms = None
+    if args.workload == "moe_refit":
+        gb_ms = compare_gather_broadcast(dom_jobs, stream, max(3, args.steps // 4), dev)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(jobs, stream, args, kernel, dctx)
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline:
+        res = oracle_sample(jobs, args.cpu_seconds)
+        if res:
+            v, desc, cores, secs = res
+            cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                   "sample": desc, "seconds": round(secs, 2)}
+
+    launches = args.steps * sum(launches_of(j, kernel) for j in jobs)
+    st_tot = {k: sum(j.stats[k] for j in jobs) for k in (
+        "global_bytes", "dst_bytes", "src_bytes", "fanout_read_bytes", "fanout_write_bytes",
+        "boxcopy_read_bytes", "boxcopy_write_bytes", "gb_read_bytes", "gb_write_bytes")}
+    reshard_hbm = sum(j.stats["fanout_read_bytes"] + j.stats["fanout_write_bytes"]
+                      for j in dom_jobs)
+    gb_hbm = sum(j.stats["gb_read_bytes"] + j.stats["gb_write_bytes"] for j in dom_jobs)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "tensors": len(jobs),
+            "reshard_kernel": args.kernel,
+            "step": "3 expert tensors via reshard_execute + 9 attention/norm tensors via "
+                    "gather_broadcast_execute" if args.workload == "moe_refit" else "reshard",
+            "global_bytes_per_step": st_tot["global_bytes"],
+            "dst_bytes_per_step": st_tot["dst_bytes"],
+            "l2": "inputs larger than L2 (sources %.1f GB per step), no flush" % (
+                st_tot["src_bytes"] / 1e9),
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+        },
+        "hbm_roofline_frac": round(value / world / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic_val, "peak_kind": peak_kind,
+                     "kernel": "reshard_copy_kernel<16,false> (fan-out)",
+                     "algorithmic_bytes_per_launch": int(dom_bytes_per_launch),
+                     "avg_launch_ms": round(dom_launch_ms, 4)},
+        "bytes_vs_gather_broadcast": {
+            "reshard_hbm_bytes": reshard_hbm, "gather_broadcast_hbm_bytes": gb_hbm,
+            "hbm_ratio": round(reshard_hbm / gb_hbm, 4) if gb_hbm else None,
+            "reshard_payload_bytes": sum(j.stats["dst_bytes"] for j in dom_jobs),
+            "pages_logical_payload_2G": 2 * sum(j.stats["global_bytes"] for j in dom_jobs),
+            "reshard_ms": round(sum(dom_ms) / args.steps, 4),
+            "gather_broadcast_ms": round(gb_ms, 4) if gb_ms else None,
+            "speedup": round(gb_ms / (sum(dom_ms) / args.steps), 3) if gb_ms else None,
+        },
+        "planner_ms": round(sum(j.stats["planner_ns"] for j in jobs) / 1e6, 3),
+        "setup_s": round(setup_s, 2),
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def compare_gather_broadcast(dom_jobs, stream, reps, dev):
+    """Latency of the conventional path (materialise the full tensor, slice) on the
+    reshard tensors of the workload, for the bytes-moved comparison."""
+    import torch
+
+    import dtensor_reshard_gb300 as rs
+    gmax = max(j.stats["global_bytes"] for j in dom_jobs)
+    try:
+        scratch = torch.empty(gmax, dtype=torch.uint8, device=dev)
+    except RuntimeError:
+        return None
+    for j in dom_jobs:
+        rs.gather_broadcast_execute(j.plan, j.srcs, j.dsts, scratch, gmax, stream)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        for j in dom_jobs:
+            rs.gather_broadcast_execute(j.plan, j.srcs, j.dsts, scratch, gmax, stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    del scratch
+    return a.elapsed_time(b) / reps
+
+
+def run_e2e(jobs, stream, args, kernel, dctx):
+    """e2e at full size if the host has room for pinned copies of every buffer."""
+    need = sum(s.numel() * s.element_size() for j in jobs for s in j.srcs) + \
+        sum(d.numel() * d.element_size() for j in jobs for d in j.dsts)
+    avail = 0
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    sub = jobs
+    note = "all tensors"
+    if avail and need > 0.6 * avail:
+        # largest subset (in workload order) that fits comfortably
+        sub, acc = [], 0
+        for j in jobs:
+            b = sum(s.numel() * s.element_size() for s in j.srcs) + \
+                sum(d.numel() * d.element_size() for d in j.dsts)
+            if acc + b <= 0.6 * avail:
+                sub.append(j)
+                acc += b
+        note = f"subset: {', '.join(j.spec.name for j in sub)} (host memory)"
+        if not sub:
+            return None
+    steps = max(2, min(5, args.steps // 4))
+    dev_ms, wall_s, h2d, d2h = e2e_time(sub, stream, steps, 1, kernel, dctx)
+    ms = dctx.max(dev_ms)
+    eff = dctx.sum(sum(j.effective_bytes for j in sub))
+    return {"value": round(eff / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms, 3), "steps": steps, "tensors": note}
+
+
+# ------------------------------------------------------------------------------ report
+def report(args):
+    """Every workload at one GPU: latency of the fan-out (K2), box-copy (K1) and
+    gather-and-broadcast paths, effective GB/s, roofline fractions, bytes ratios,
+    planner time.  Writes JSON lines to args.report and a table to stderr."""
+    import torch
+
+    import dtensor_reshard_gb300 as rs
+    from inputs import workload
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    peak, _ = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    l2_flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    rows = []
+
+    def timed(fn, reps, flush):
+        ts = []
+        for i in range(reps + 3):
+            if flush:
+                l2_flush.fill_(i & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    for cfg in (1, 2, 3, 4, 5):
+        w = workload(cfg)
+        tensors = [t for t in w.tensors if t.path == "reshard"]
+        sub = type(w)(w.name, tuple(tensors), w.note)
+        jobs = build_jobs(sub, dev, with_gb=False)
+        G = sum(j.stats["global_bytes"] for j in jobs)
+        D = sum(j.stats["dst_bytes"] for j in jobs)
+        flush = G + D < 4 * (128 << 20)
+        gmax = max(j.stats["global_bytes"] for j in jobs)
+        scratch = torch.empty(max(gmax, 1), dtype=torch.uint8, device=dev)
+        reps = 20 if G < (1 << 30) else 5
+
+        def k2():
+            for j in jobs:
+                rs.reshard_execute_ex(j.plan, j.srcs, j.dsts, rs.KERNEL_FANOUT, stream)
+
+        def k1():
+            for j in jobs:
+                rs.reshard_execute_ex(j.plan, j.srcs, j.dsts, rs.KERNEL_BOXCOPY, stream)
+
+        def gb():
+            for j in jobs:
+                rs.gather_broadcast_execute(j.plan, j.srcs, j.dsts, scratch, gmax, stream)
+
+        t2, t1, tg = timed(k2, reps, flush), timed(k1, reps, flush), timed(gb, reps, flush)
+        b2 = sum(j.stats["fanout_read_bytes"] + j.stats["fanout_write_bytes"] for j in jobs)
+        b1 = sum(j.stats["boxcopy_read_bytes"] + j.stats["boxcopy_write_bytes"] for j in jobs)
+        bg = sum(j.stats["gb_read_bytes"] + j.stats["gb_write_bytes"] for j in jobs)
+        row = {
+            "workload": w.name, "tensors": len(jobs), "G": G, "D": D,
+            "l2_flush": flush,
+            "fanout_ms": round(t2, 4), "boxcopy_ms": round(t1, 4),
+            "gather_broadcast_ms": round(tg, 4),
+            "effective_GBps": round((G + D) / t2 / 1e6, 1),
+            "fanout_hbm_GBps": round(b2 / t2 / 1e6, 1),
+            "boxcopy_hbm_GBps": round(b1 / t1 / 1e6, 1),
+            "gb_hbm_GBps": round(bg / tg / 1e6, 1),
+            "fanout_roofline_frac": round(b2 / t2 / 1e6 / peak, 4),
+            "boxcopy_roofline_frac": round(b1 / t1 / 1e6 / peak, 4),
+            "min_bytes_roofline_frac": round((G + D) / t2 / 1e6 / peak, 4),
+            "hbm_bytes_fanout_vs_gb": round(b2 / bg, 4),
+            "payload_vs_pages_2G": round(D / (2 * G), 4),
+            "speedup_vs_gather_broadcast": round(tg / t2, 3),
+            "planner_ms": round(sum(j.stats["planner_ns"] for j in jobs) / 1e6, 3),
+        }
+        rows.append(row)
+        print(json.dumps(row), file=sys.stderr)
+        del jobs, scratch
+        torch.cuda.empty_cache()
+    with open(args.report, "w") as f:
+        for r in rows:
+            f.write(json.dumps(r) + "\n")
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    if args.report:
+        return report(args)
+    return ours_arm(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

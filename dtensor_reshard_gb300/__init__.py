@@ -1,0 +1,306 @@
+"""Python binding of libreshard.so: a GB300 (sm_103a) DTensor-to-DTensor reshard.
+
+The functions below carry the names of the C entry points declared in
+``include/reshard.h`` and only marshal arguments: every step of the reshard
+(layout resolution, intersection, planning, copying) runs inside the library.
+Device pointers may be passed as integers or as any object with a
+``data_ptr()`` method (e.g. a CUDA ``torch.Tensor``); streams as integers, as
+objects with a ``cuda_stream`` attribute, or None (legacy default stream).
+
+Placements are strings, ``"R"`` for Replicate and ``"S<d>"`` for Shard(d), or
+(kind, dim) tuples.  There is no CPU fallback: importing this package raises if
+the compiled library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Sequence
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libreshard.so")
+
+MAX_TENSOR_NDIM = 4
+MAX_MESH_NDIM = 4
+MAX_EXEC_BUFFERS = 1024
+
+DTYPES = {"u8": 0, "bf16": 1, "fp16": 2, "fp32": 3, "i32": 4, "fp64": 5, "i64": 6}
+ELEM_BYTES = {"u8": 1, "bf16": 2, "fp16": 2, "fp32": 4, "i32": 4, "fp64": 8, "i64": 8}
+
+OK = 0
+STATUS = {0: "RESHARD_OK", 1: "RESHARD_ERR_INVALID_ARG", 2: "RESHARD_ERR_UNSUPPORTED",
+          3: "RESHARD_ERR_SHAPE", 4: "RESHARD_ERR_CUDA", 5: "RESHARD_ERR_NO_MEMORY",
+          6: "RESHARD_ERR_BAD_HANDLE"}
+
+KERNEL_FANOUT = 0
+KERNEL_BOXCOPY = 1
+PROGRAM_FANOUT, PROGRAM_BOXCOPY, PROGRAM_GATHER, PROGRAM_SLICE = 0, 1, 2, 3
+
+
+class reshard_placement_t(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("dim", ctypes.c_int32)]
+
+
+class reshard_mesh_t(ctypes.Structure):
+    _fields_ = [("ndim", ctypes.c_int32), ("shape", ctypes.c_int64 * MAX_MESH_NDIM)]
+
+
+class reshard_stats_t(ctypes.Structure):
+    _fields_ = [("global_bytes", ctypes.c_int64), ("src_bytes", ctypes.c_int64),
+                ("dst_bytes", ctypes.c_int64), ("n_src_ranks", ctypes.c_int64),
+                ("n_dst_ranks", ctypes.c_int64), ("n_src_classes", ctypes.c_int64),
+                ("n_dst_classes", ctypes.c_int64), ("n_regions", ctypes.c_int64),
+                ("region_bytes", ctypes.c_int64), ("n_tiles", ctypes.c_int64 * 4),
+                ("fanout_read_bytes", ctypes.c_int64), ("fanout_write_bytes", ctypes.c_int64),
+                ("boxcopy_read_bytes", ctypes.c_int64), ("boxcopy_write_bytes", ctypes.c_int64),
+                ("gb_read_bytes", ctypes.c_int64), ("gb_write_bytes", ctypes.c_int64),
+                ("max_replica_read_bytes", ctypes.c_int64), ("max_fanout", ctypes.c_int64),
+                ("planner_ns", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        out = {}
+        for name, _ in self._fields_:
+            v = getattr(self, name)
+            out[name] = list(v) if name == "n_tiles" else int(v)
+        return out
+
+
+class reshard_tile_t(ctypes.Structure):
+    _fields_ = [("src_off", ctypes.c_int64), ("dst_off", ctypes.c_int64),
+                ("src_row_stride", ctypes.c_int64), ("dst_row_stride", ctypes.c_int64),
+                ("src_plane_stride", ctypes.c_int64), ("dst_plane_stride", ctypes.c_int64),
+                ("row_bytes", ctypes.c_uint32), ("nrows", ctypes.c_uint32),
+                ("nplanes", ctypes.c_uint32), ("src_buf", ctypes.c_uint16),
+                ("dst_group", ctypes.c_uint16)]
+
+
+assert ctypes.sizeof(reshard_tile_t) == 64
+
+
+class ReshardError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` "
+                          "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    sig = {
+        "reshard_plan_create": ([i64p, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.POINTER(reshard_mesh_t),
+                                 ctypes.POINTER(reshard_placement_t),
+                                 ctypes.POINTER(reshard_mesh_t),
+                                 ctypes.POINTER(reshard_placement_t), vpp], ctypes.c_int),
+        "reshard_plan_upload": ([vp], ctypes.c_int),
+        "reshard_execute": ([vp, vpp, vpp, vp], ctypes.c_int),
+        "reshard_execute_ex": ([vp, vpp, vpp, ctypes.c_int32, vp], ctypes.c_int),
+        "gather_broadcast_execute": ([vp, vpp, vpp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "reshard_plan_local_shape": ([vp, ctypes.c_int32, ctypes.c_int64, i64p, i64p],
+                                     ctypes.c_int),
+        "reshard_plan_stats": ([vp, ctypes.POINTER(reshard_stats_t)], ctypes.c_int),
+        "reshard_plan_program": ([vp, ctypes.c_int32,
+                                  ctypes.POINTER(ctypes.POINTER(reshard_tile_t)), i64p,
+                                  ctypes.POINTER(i64p),
+                                  ctypes.POINTER(ctypes.POINTER(ctypes.c_uint32)),
+                                  ctypes.POINTER(ctypes.POINTER(ctypes.c_uint16)), i64p],
+                                 ctypes.c_int),
+        "reshard_tile_units": ([ctypes.POINTER(reshard_tile_t)], ctypes.c_int64),
+        "reshard_plan_destroy": ([vp], ctypes.c_int),
+        "reshard_last_error": ([], ctypes.c_char_p),
+        "reshard_version": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def reshard_last_error() -> str:
+    return _lib.reshard_last_error().decode()
+
+
+def reshard_version() -> str:
+    return _lib.reshard_version().decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise ReshardError(status, where, reshard_last_error())
+
+
+# ------------------------------------------------------------------------ marshalling
+def placement(p) -> tuple:
+    """(kind, dim) of a placement given as "R", "S<d>" or a (kind, dim) tuple."""
+    if isinstance(p, str):
+        if p == "R":
+            return (0, 0)
+        if p.startswith("S"):
+            return (1, int(p[1:]))
+        raise ValueError(f"unknown placement {p!r}")
+    kind, dim = p
+    return (int(kind), int(dim))
+
+
+def _mesh(mesh: Sequence[int]) -> reshard_mesh_t:
+    m = reshard_mesh_t()
+    m.ndim = len(mesh)
+    for i, s in enumerate(list(mesh)[:MAX_MESH_NDIM]):
+        m.shape[i] = int(s)
+    return m
+
+
+def _placements(pls) -> ctypes.Array:
+    arr = (reshard_placement_t * max(1, len(pls)))()
+    for i, p in enumerate(pls):
+        arr[i].kind, arr[i].dim = placement(p)
+    return arr
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr()) or None
+    return int(x) or None
+
+
+def _ptr_array(xs) -> ctypes.Array:
+    return (ctypes.c_void_p * max(1, len(xs)))(*[_ptr(x) for x in xs])
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s or None
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream) or None
+    return int(s) or None
+
+
+class Plan:
+    """Owning wrapper of a reshard_plan_t handle."""
+
+    def __init__(self, handle: int, global_shape, dtype, src_mesh, src_placements, dst_mesh,
+                 dst_placements):
+        self.handle = handle
+        self.global_shape = tuple(int(s) for s in global_shape)
+        self.dtype = dtype
+        self.src_mesh, self.src_placements = tuple(src_mesh), tuple(src_placements)
+        self.dst_mesh, self.dst_placements = tuple(dst_mesh), tuple(dst_placements)
+        self.n_src = math.prod(self.src_mesh)
+        self.n_dst = math.prod(self.dst_mesh)
+
+    @property
+    def _as_parameter_(self):
+        if not self.handle:
+            raise ReshardError(6, "plan", "plan already destroyed")
+        return ctypes.c_void_p(self.handle)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            try:
+                _lib.reshard_plan_destroy(ctypes.c_void_p(h))
+            except Exception:  # noqa: BLE001 - interpreter shutdown
+                pass
+            self.handle = None
+
+
+# ------------------------------------------------------------------------ entry points
+def reshard_plan_create(global_shape, dtype, src_mesh, src_placements, dst_mesh,
+                        dst_placements) -> Plan:
+    shape = (ctypes.c_int64 * max(1, len(global_shape)))(*[int(s) for s in global_shape])
+    h = ctypes.c_void_p()
+    dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    st = _lib.reshard_plan_create(shape, len(global_shape), dt, ctypes.byref(_mesh(src_mesh)),
+                                  _placements(src_placements), ctypes.byref(_mesh(dst_mesh)),
+                                  _placements(dst_placements), ctypes.byref(h))
+    _check(st, "reshard_plan_create")
+    return Plan(h.value, global_shape, dtype, src_mesh, src_placements, dst_mesh, dst_placements)
+
+
+def reshard_plan_upload(plan: Plan):
+    _check(_lib.reshard_plan_upload(plan), "reshard_plan_upload")
+
+
+def reshard_execute(plan: Plan, src_ptrs, dst_ptrs, stream=None):
+    _check(_lib.reshard_execute(plan, _ptr_array(src_ptrs), _ptr_array(dst_ptrs),
+                                _stream(stream)), "reshard_execute")
+
+
+def reshard_execute_ex(plan: Plan, src_ptrs, dst_ptrs, kernel: int, stream=None):
+    _check(_lib.reshard_execute_ex(plan, _ptr_array(src_ptrs), _ptr_array(dst_ptrs),
+                                   int(kernel), _stream(stream)), "reshard_execute_ex")
+
+
+def gather_broadcast_execute(plan: Plan, src_ptrs, dst_ptrs, full_scratch, scratch_bytes: int,
+                             stream=None):
+    _check(_lib.gather_broadcast_execute(plan, _ptr_array(src_ptrs), _ptr_array(dst_ptrs),
+                                         _ptr(full_scratch), int(scratch_bytes), _stream(stream)),
+           "gather_broadcast_execute")
+
+
+def reshard_plan_local_shape(plan: Plan, side: int, rank: int):
+    """(shape, offset) tuples of one rank's local shard (side 0 = source, 1 = destination)."""
+    nd = len(plan.global_shape)
+    shp = (ctypes.c_int64 * nd)()
+    off = (ctypes.c_int64 * nd)()
+    _check(_lib.reshard_plan_local_shape(plan, int(side), int(rank), shp, off),
+           "reshard_plan_local_shape")
+    return tuple(shp), tuple(off)
+
+
+def reshard_plan_stats(plan: Plan) -> dict:
+    s = reshard_stats_t()
+    _check(_lib.reshard_plan_stats(plan, ctypes.byref(s)), "reshard_plan_stats")
+    return s.as_dict()
+
+
+def reshard_plan_program(plan: Plan, program: int):
+    """(tiles, unit_prefix, group_offsets, group_buffers) of one program, copied to Python."""
+    tp = ctypes.POINTER(reshard_tile_t)()
+    nt = ctypes.c_int64()
+    pp = ctypes.POINTER(ctypes.c_int64)()
+    go = ctypes.POINTER(ctypes.c_uint32)()
+    gb = ctypes.POINTER(ctypes.c_uint16)()
+    ng = ctypes.c_int64()
+    _check(_lib.reshard_plan_program(plan, int(program), ctypes.byref(tp), ctypes.byref(nt),
+                                     ctypes.byref(pp), ctypes.byref(go), ctypes.byref(gb),
+                                     ctypes.byref(ng)), "reshard_plan_program")
+    n, g = nt.value, ng.value
+    tiles = [{f: getattr(tp[i], f) for f, _ in reshard_tile_t._fields_} for i in range(n)]
+    prefix = [pp[i] for i in range(n + 1)]
+    goff = [go[i] for i in range(g + 1)]
+    gbuf = [gb[i] for i in range(goff[-1])] if g >= 0 and goff else []
+    return tiles, prefix, goff, gbuf
+
+
+def reshard_tile_units(tile: dict) -> int:
+    t = reshard_tile_t(**tile)
+    return int(_lib.reshard_tile_units(ctypes.byref(t)))
+
+
+def reshard_plan_destroy(plan: Plan):
+    if not plan.handle:
+        raise ReshardError(6, "reshard_plan_destroy", "plan already destroyed")
+    st = _lib.reshard_plan_destroy(plan)
+    plan.handle = None
+    _check(st, "reshard_plan_destroy")

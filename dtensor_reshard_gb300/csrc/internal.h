@@ -1,0 +1,92 @@
+// internal.h -- shared between the host planner (planner.cpp) and the CUDA
+// kernels (kernels.cu) of libreshard.so.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "reshard.h"
+
+namespace rs {
+
+// A multi-row tile whose rows are longer than this is split into one
+// single-row ("run") tile per row, so that work units stay small.
+constexpr int64_t kRunSplitBytes = 64 * 1024;
+// Work-unit size of a single-row tile, and the row budget of a multi-row unit.
+constexpr int64_t kUnitBytes = 4096;
+// Largest single-row tile (longer runs are cut into several tiles).
+constexpr int64_t kMaxRunBytes = int64_t(1) << 30;
+// Largest destination group one tile fans out to (larger groups are split).
+constexpr int kMaxGroup = 256;
+
+// Work units of a tile (must match the kernels' reading of a tile).
+inline int64_t tile_units(const reshard_tile_t& t) {
+  if (t.nrows == 1 && t.nplanes == 1) return (int64_t(t.row_bytes) + kUnitBytes - 1) / kUnitBytes;
+  int64_t rows = int64_t(t.nrows) * int64_t(t.nplanes);
+  int64_t upr = t.row_bytes >= kUnitBytes ? 1 : kUnitBytes / t.row_bytes;
+  return (rows + upr - 1) / upr;
+}
+
+struct Box {
+  int64_t off[RESHARD_MAX_TENSOR_NDIM];
+  int64_t shp[RESHARD_MAX_TENSOR_NDIM];
+};
+
+struct Layout {
+  int32_t mesh_ndim = 0;
+  int64_t mesh[RESHARD_MAX_MESH_NDIM] = {};
+  reshard_placement_t pl[RESHARD_MAX_MESH_NDIM] = {};
+  int64_t nranks = 0;
+  std::vector<Box> box;  // per flat rank
+};
+
+// One copy program: tiles in execution order, the units prefix, and the
+// destination groups (lists of buffer indices).
+struct Program {
+  std::vector<reshard_tile_t> tiles;
+  std::vector<int64_t> prefix;     // ntiles + 1
+  std::vector<uint32_t> goff;      // ngroups + 1
+  std::vector<uint16_t> gbuf;      // buffer indices
+  // device copies (inside the plan's single device allocation)
+  const reshard_tile_t* d_tiles = nullptr;
+  const int64_t* d_prefix = nullptr;
+  const uint32_t* d_goff = nullptr;
+  const uint16_t* d_gbuf = nullptr;
+  // OR of every tile's offsets, strides and row length (alignment class)
+  uint64_t align_bits = 0;
+  bool has_planes = false;  // some tile has nplanes > 1
+  int64_t total_units() const { return prefix.empty() ? 0 : prefix.back(); }
+};
+
+}  // namespace rs
+
+struct reshard_plan_s {
+  uint64_t magic = 0;
+  int32_t ndim = 0;
+  int64_t gshape[RESHARD_MAX_TENSOR_NDIM] = {};
+  int32_t elem_bytes = 0;
+  rs::Layout src, dst;
+  rs::Program prog[4];
+  reshard_stats_t stats = {};
+  // device binding
+  int device = -1;
+  void* d_mem = nullptr;
+  int num_sms = 0;
+  int blocks_per_sm = 0;
+};
+
+namespace rs {
+
+// Error reporting (thread-local message).
+reshard_status_t fail(reshard_status_t st, const std::string& msg);
+
+// Kernel side (kernels.cu).  Launches one program over the buffer table
+// bufs[nbufs] on `stream`.  Returns OK when there is nothing to do.
+reshard_status_t launch_program(const reshard_plan_s* plan, const Program& p,
+                                unsigned char* const* bufs, int nbufs, void* stream);
+// Occupancy of the copy kernel on the current device (blocks per SM).
+reshard_status_t copy_kernel_occupancy(int* blocks_per_sm);
+
+}  // namespace rs

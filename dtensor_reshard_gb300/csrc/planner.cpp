@@ -1,0 +1,737 @@
+// planner.cpp -- host planner and C ABI of libreshard.so.
+//
+// The planner turns two DTensor layouts of one global tensor into copy
+// programs for the CUDA kernels:
+//   1. resolve every rank's box (global offset + local shape);
+//   2. group ranks holding identical boxes into classes (replicas);
+//   3. intersect every destination class with every source class;
+//   4. pick one source replica per region, largest region first, onto the
+//      replica with the fewest bytes read so far (ties: lowest rank);
+//   5. express each region in both local layouts, collapse dims that are
+//      contiguous in both, and cut it into tiles;
+//   6. attach the destination replicas of the region's class as one fan-out
+//      group and sort the tiles by destination.
+// Steps 3-4 follow the Reshard collective write-ups (news.bpdata.com, section
+// "A Reshard kollektiv kommunikacio": exact source/destination intersections
+// first, each contribution sent once, replicas assemble locally; techfeed.io,
+// section on NVIDIA's implementation: incoming data spread as evenly as
+// possible across replicas).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+
+#include "internal.h"
+
+namespace rs {
+namespace {
+
+constexpr uint64_t kPlanMagic = 0x5245534841524431ull;  // "RESHARD1"
+
+thread_local std::string g_last_error;
+
+std::mutex g_registry_mu;
+std::unordered_set<const reshard_plan_s*>& registry() {
+  static std::unordered_set<const reshard_plan_s*> r;
+  return r;
+}
+
+bool live(const reshard_plan_s* p) {
+  if (!p) return false;
+  std::lock_guard<std::mutex> lk(g_registry_mu);
+  return registry().count(p) != 0;
+}
+
+int elem_size(int32_t dtype) {
+  switch (dtype) {
+    case RESHARD_U8: return 1;
+    case RESHARD_BF16:
+    case RESHARD_FP16: return 2;
+    case RESHARD_FP32:
+    case RESHARD_I32: return 4;
+    case RESHARD_FP64:
+    case RESHARD_I64: return 8;
+    default: return 0;
+  }
+}
+
+// ---------------------------------------------------------------- step 1: resolve
+// Shard(d) on a mesh dim of size k splits the current local extent n of dim d
+// into torch.chunk pieces of ceil(n/k); mesh dims apply in order.
+void resolve_rank(int32_t nd, const int64_t* gshape, const Layout& L, int64_t rank, Box* b) {
+  int64_t coord[RESHARD_MAX_MESH_NDIM];
+  int64_t rest = rank;
+  for (int m = L.mesh_ndim - 1; m >= 0; --m) {
+    coord[m] = rest % L.mesh[m];
+    rest /= L.mesh[m];
+  }
+  bool sharded[RESHARD_MAX_TENSOR_NDIM] = {};
+  for (int d = 0; d < nd; ++d) {
+    b->off[d] = 0;
+    b->shp[d] = gshape[d];
+  }
+  for (int m = 0; m < L.mesh_ndim; ++m) {
+    if (L.pl[m].kind != RESHARD_SHARD) continue;
+    const int d = L.pl[m].dim;
+    const int64_t n = b->shp[d];
+    const int64_t piece = (n + L.mesh[m] - 1) / L.mesh[m];
+    const int64_t lo = std::min(coord[m] * piece, n);
+    const int64_t hi = std::min(lo + piece, n);
+    b->off[d] += lo;
+    b->shp[d] = hi - lo;
+    sharded[d] = true;
+  }
+  for (int d = 0; d < nd; ++d)
+    if (sharded[d] && b->shp[d] == 0) b->off[d] = gshape[d];
+}
+
+int64_t box_volume(int32_t nd, const Box& b) {
+  int64_t v = 1;
+  for (int d = 0; d < nd; ++d) v *= b.shp[d];
+  return v;
+}
+
+struct Class {
+  Box box;
+  std::vector<int64_t> ranks;  // ascending
+  int64_t volume = 0;
+};
+
+// ---------------------------------------------------------------- step 2: classes
+std::vector<Class> classes_of(int32_t nd, const Layout& L) {
+  std::vector<Class> out;
+  std::map<std::vector<int64_t>, size_t> index;
+  for (int64_t r = 0; r < L.nranks; ++r) {
+    const Box& b = L.box[r];
+    const int64_t vol = box_volume(nd, b);
+    if (vol == 0) continue;
+    std::vector<int64_t> key(b.off, b.off + nd);
+    key.insert(key.end(), b.shp, b.shp + nd);
+    auto it = index.find(key);
+    if (it == index.end()) {
+      index.emplace(key, out.size());
+      Class c;
+      c.box = b;
+      c.volume = vol;
+      c.ranks.push_back(r);
+      out.push_back(c);
+    } else {
+      out[it->second].ranks.push_back(r);
+    }
+  }
+  return out;
+}
+
+// ---------------------------------------------------------------- step 5: tiles
+struct Dim {
+  int64_t e, ss, ds;  // extent, source stride, destination stride (elements)
+};
+
+void row_major_strides(int32_t nd, const int64_t* shp, int64_t* st) {
+  int64_t s = 1;
+  for (int d = nd - 1; d >= 0; --d) {
+    st[d] = s;
+    s *= shp[d];
+  }
+}
+
+// Emit the tiles copying a box of extents e[nd] (elements) that starts at
+// element src_base / dst_base of buffers with strides sst / dst (elements).
+void emit_box(Program& P, uint16_t src_buf, uint16_t group, int32_t nd, const int64_t* e,
+              int64_t src_base, const int64_t* sst, int64_t dst_base, const int64_t* dstr,
+              int64_t eb) {
+  std::vector<Dim> dims;
+  for (int d = 0; d < nd; ++d) {
+    if (e[d] == 0) return;
+    if (e[d] > 1) dims.push_back({e[d], sst[d], dstr[d]});
+  }
+  // merge neighbours that are contiguous in both layouts
+  std::vector<Dim> m;
+  for (const Dim& d : dims) {
+    if (!m.empty() && m.back().ss == d.e * d.ss && m.back().ds == d.e * d.ds) {
+      m.back() = {m.back().e * d.e, d.ss, d.ds};
+    } else {
+      m.push_back(d);
+    }
+  }
+  int64_t row_elems = 1;
+  if (!m.empty() && m.back().ss == 1 && m.back().ds == 1) {
+    row_elems = m.back().e;
+    m.pop_back();
+  }
+  const int64_t row_bytes = row_elems * eb;
+  // A single row, or rows longer than kRunSplitBytes, become run tiles (one
+  // per row, cut into pieces of at most kMaxRunBytes).
+  auto emit_run = [&](int64_t sbyte, int64_t dbyte) {
+    for (int64_t o = 0; o < row_bytes; o += kMaxRunBytes) {
+      reshard_tile_t t = {};
+      t.src_off = sbyte + o;
+      t.dst_off = dbyte + o;
+      t.row_bytes = uint32_t(std::min(kMaxRunBytes, row_bytes - o));
+      t.nrows = t.nplanes = 1;
+      t.src_buf = src_buf;
+      t.dst_group = group;
+      P.tiles.push_back(t);
+    }
+  };
+  auto emit_rows = [&](int64_t sb, int64_t db, int64_t nplanes, int64_t sps, int64_t dps,
+                       int64_t nrows, int64_t srs, int64_t drs) {
+    if (nplanes * nrows == 1 || row_bytes > kRunSplitBytes) {
+      for (int64_t p = 0; p < nplanes; ++p)
+        for (int64_t r = 0; r < nrows; ++r)
+          emit_run((sb + p * sps + r * srs) * eb, (db + p * dps + r * drs) * eb);
+      return;
+    }
+    // keep nrows * nplanes of one tile below 2^30: slice planes, then rows
+    const int64_t kMaxRows = int64_t(1) << 30;
+    const int64_t pstep = std::max<int64_t>(1, kMaxRows / nrows);
+    for (int64_t p0 = 0; p0 < nplanes; p0 += pstep) {
+      const int64_t np = std::min(nplanes - p0, pstep);
+      for (int64_t r0 = 0; r0 < nrows; r0 += kMaxRows) {
+        const int64_t nr = std::min(nrows - r0, kMaxRows);
+        reshard_tile_t t = {};
+        t.src_off = (sb + p0 * sps + r0 * srs) * eb;
+        t.dst_off = (db + p0 * dps + r0 * drs) * eb;
+        t.row_bytes = uint32_t(row_bytes);
+        t.nrows = uint32_t(nr);
+        t.nplanes = uint32_t(np);
+        if (t.nrows > 1) {
+          t.src_row_stride = srs * eb;
+          t.dst_row_stride = drs * eb;
+        }
+        if (t.nplanes > 1) {
+          t.src_plane_stride = sps * eb;
+          t.dst_plane_stride = dps * eb;
+        }
+        t.src_buf = src_buf;
+        t.dst_group = group;
+        P.tiles.push_back(t);
+      }
+    }
+  };
+  const size_t k = m.size();
+  if (k == 0) {
+    emit_rows(src_base, dst_base, 1, 0, 0, 1, 0, 0);
+  } else if (k == 1) {
+    emit_rows(src_base, dst_base, 1, 0, 0, m[0].e, m[0].ss, m[0].ds);
+  } else {
+    // outer dims beyond two become a loop of 2-level tiles
+    const Dim& pl = m[k - 2];
+    const Dim& rw = m[k - 1];
+    std::vector<int64_t> idx(k - 2, 0);
+    while (true) {
+      int64_t sb = src_base, db = dst_base;
+      for (size_t i = 0; i + 2 < k; ++i) {
+        sb += idx[i] * m[i].ss;
+        db += idx[i] * m[i].ds;
+      }
+      emit_rows(sb, db, pl.e, pl.ss, pl.ds, rw.e, rw.ss, rw.ds);
+      int64_t i = int64_t(k) - 3;
+      for (; i >= 0; --i) {
+        if (++idx[i] < m[i].e) break;
+        idx[i] = 0;
+      }
+      if (i < 0) break;
+    }
+  }
+}
+
+void finish_program(Program& P) {
+  // sort by destination (first buffer of the group, then offset)
+  std::stable_sort(P.tiles.begin(), P.tiles.end(),
+                   [&](const reshard_tile_t& a, const reshard_tile_t& b) {
+                     const uint16_t ba = P.gbuf[P.goff[a.dst_group]];
+                     const uint16_t bb = P.gbuf[P.goff[b.dst_group]];
+                     if (ba != bb) return ba < bb;
+                     if (a.dst_off != b.dst_off) return a.dst_off < b.dst_off;
+                     return a.dst_group < b.dst_group;
+                   });
+  P.prefix.assign(P.tiles.size() + 1, 0);
+  for (size_t i = 0; i < P.tiles.size(); ++i) {
+    const reshard_tile_t& t = P.tiles[i];
+    P.prefix[i + 1] = P.prefix[i] + tile_units(t);
+    P.align_bits |= uint64_t(t.src_off) | uint64_t(t.dst_off) | t.row_bytes |
+                    uint64_t(t.src_row_stride) | uint64_t(t.dst_row_stride) |
+                    uint64_t(t.src_plane_stride) | uint64_t(t.dst_plane_stride);
+    if (t.nplanes > 1) P.has_planes = true;
+  }
+}
+
+int64_t tile_bytes(const reshard_tile_t& t) {
+  return int64_t(t.row_bytes) * t.nrows * t.nplanes;
+}
+
+// ---------------------------------------------------------------- validation
+reshard_status_t read_layout(const char* side, int32_t nd, const reshard_mesh_t* mesh,
+                             const reshard_placement_t* pl, Layout* L) {
+  if (!mesh || !pl) return fail(RESHARD_ERR_INVALID_ARG, std::string(side) + ": null mesh or placements");
+  if (mesh->ndim < 1 || mesh->ndim > RESHARD_MAX_MESH_NDIM)
+    return fail(RESHARD_ERR_UNSUPPORTED, std::string(side) + ": mesh ndim must be 1..4");
+  L->mesh_ndim = mesh->ndim;
+  L->nranks = 1;
+  for (int m = 0; m < mesh->ndim; ++m) {
+    if (mesh->shape[m] < 1)
+      return fail(RESHARD_ERR_INVALID_ARG, std::string(side) + ": mesh sizes must be >= 1");
+    if (mesh->shape[m] > RESHARD_MAX_RANKS || L->nranks * mesh->shape[m] > RESHARD_MAX_RANKS)
+      return fail(RESHARD_ERR_UNSUPPORTED, std::string(side) + ": too many ranks");
+    L->mesh[m] = mesh->shape[m];
+    L->nranks *= mesh->shape[m];
+    if (pl[m].kind == RESHARD_SHARD) {
+      if (pl[m].dim < 0 || pl[m].dim >= nd)
+        return fail(RESHARD_ERR_INVALID_ARG, std::string(side) + ": Shard dim out of range");
+    } else if (pl[m].kind != RESHARD_REPLICATE) {
+      return fail(RESHARD_ERR_UNSUPPORTED,
+                  std::string(side) + ": only Shard and Replicate placements are supported");
+    }
+    L->pl[m] = pl[m];
+    if (L->pl[m].kind == RESHARD_REPLICATE) L->pl[m].dim = 0;
+  }
+  return RESHARD_OK;
+}
+
+reshard_status_t build_plan(reshard_plan_s* P) {
+  const int32_t nd = P->ndim;
+  const int64_t eb = P->elem_bytes;
+  const int64_t M = P->src.nranks, N = P->dst.nranks;
+  P->src.box.resize(M);
+  P->dst.box.resize(N);
+  for (int64_t r = 0; r < M; ++r) resolve_rank(nd, P->gshape, P->src, r, &P->src.box[r]);
+  for (int64_t r = 0; r < N; ++r) resolve_rank(nd, P->gshape, P->dst, r, &P->dst.box[r]);
+
+  reshard_stats_t& S = P->stats;
+  S.global_bytes = eb;
+  for (int d = 0; d < nd; ++d) S.global_bytes *= P->gshape[d];
+  S.n_src_ranks = M;
+  S.n_dst_ranks = N;
+  for (int64_t r = 0; r < M; ++r) S.src_bytes += box_volume(nd, P->src.box[r]) * eb;
+  for (int64_t r = 0; r < N; ++r) S.dst_bytes += box_volume(nd, P->dst.box[r]) * eb;
+
+  const std::vector<Class> sc = classes_of(nd, P->src);
+  const std::vector<Class> dc = classes_of(nd, P->dst);
+  S.n_src_classes = int64_t(sc.size());
+  S.n_dst_classes = int64_t(dc.size());
+
+  // ---- step 3: intersections
+  struct Region {
+    size_t d, s;
+    int64_t lo[RESHARD_MAX_TENSOR_NDIM], ext[RESHARD_MAX_TENSOR_NDIM];
+    int64_t bytes;
+    int64_t replica = -1;
+  };
+  std::vector<Region> regions;
+  for (size_t di = 0; di < dc.size(); ++di) {
+    for (size_t si = 0; si < sc.size(); ++si) {
+      Region g;
+      g.d = di;
+      g.s = si;
+      int64_t vol = 1;
+      for (int d = 0; d < nd; ++d) {
+        const int64_t lo = std::max(dc[di].box.off[d], sc[si].box.off[d]);
+        const int64_t hi = std::min(dc[di].box.off[d] + dc[di].box.shp[d],
+                                    sc[si].box.off[d] + sc[si].box.shp[d]);
+        if (hi <= lo) {
+          vol = 0;
+          break;
+        }
+        g.lo[d] = lo;
+        g.ext[d] = hi - lo;
+        vol *= hi - lo;
+      }
+      if (vol == 0) continue;
+      g.bytes = vol * eb;
+      regions.push_back(g);
+    }
+  }
+  S.n_regions = int64_t(regions.size());
+  for (const Region& g : regions) S.region_bytes += g.bytes;
+
+  // ---- step 4: replica pick, largest region first onto the least-loaded replica
+  {
+    std::vector<size_t> order(regions.size());
+    for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](size_t a, size_t b) { return regions[a].bytes > regions[b].bytes; });
+    std::vector<int64_t> load(size_t(M), 0);
+    for (size_t i : order) {
+      Region& g = regions[i];
+      int64_t best = -1;
+      for (int64_t r : sc[g.s].ranks)
+        if (best < 0 || load[size_t(r)] < load[size_t(best)]) best = r;
+      g.replica = best;
+      load[size_t(best)] += g.bytes;
+    }
+    for (int64_t r = 0; r < M; ++r) S.max_replica_read_bytes = std::max(S.max_replica_read_bytes, load[size_t(r)]);
+  }
+
+  // ---- step 6 (groups first): destination groups
+  const uint16_t scratch_buf = uint16_t(M + N);
+  std::vector<std::vector<uint16_t>> fan_groups_of(dc.size());  // FANOUT program
+  Program& PF = P->prog[RESHARD_PROGRAM_FANOUT];
+  Program& PB = P->prog[RESHARD_PROGRAM_BOXCOPY];
+  Program& PG = P->prog[RESHARD_PROGRAM_GATHER];
+  Program& PS = P->prog[RESHARD_PROGRAM_SLICE];
+  for (Program* p : {&PF, &PB, &PG, &PS}) p->goff.push_back(0);
+  for (size_t di = 0; di < dc.size(); ++di) {
+    const auto& rk = dc[di].ranks;
+    S.max_fanout = std::max<int64_t>(S.max_fanout, int64_t(rk.size()));
+    for (size_t a = 0; a < rk.size(); a += kMaxGroup) {
+      fan_groups_of[di].push_back(uint16_t(PF.goff.size() - 1));
+      for (size_t b = a; b < std::min(rk.size(), a + size_t(kMaxGroup)); ++b)
+        PF.gbuf.push_back(uint16_t(M + rk[b]));
+      PF.goff.push_back(uint32_t(PF.gbuf.size()));
+    }
+  }
+  // one group per destination rank (BOXCOPY and SLICE)
+  for (Program* p : {&PB, &PS}) {
+    for (int64_t r = 0; r < N; ++r) {
+      p->gbuf.push_back(uint16_t(M + r));
+      p->goff.push_back(uint32_t(p->gbuf.size()));
+    }
+  }
+  PG.gbuf.push_back(scratch_buf);
+  PG.goff.push_back(1);
+
+  // ---- step 5: tiles
+  int64_t gst[RESHARD_MAX_TENSOR_NDIM];
+  row_major_strides(nd, P->gshape, gst);
+  for (const Region& g : regions) {
+    const Box& sb = P->src.box[size_t(g.replica)];
+    const Box& db = dc[g.d].box;
+    int64_t sst[RESHARD_MAX_TENSOR_NDIM], dst[RESHARD_MAX_TENSOR_NDIM];
+    row_major_strides(nd, sb.shp, sst);
+    row_major_strides(nd, db.shp, dst);
+    int64_t s0 = 0, d0 = 0;
+    for (int d = 0; d < nd; ++d) {
+      s0 += (g.lo[d] - sb.off[d]) * sst[d];
+      d0 += (g.lo[d] - db.off[d]) * dst[d];
+    }
+    for (uint16_t grp : fan_groups_of[g.d])
+      emit_box(PF, uint16_t(g.replica), grp, nd, g.ext, s0, sst, d0, dst, eb);
+    for (int64_t r : dc[g.d].ranks)
+      emit_box(PB, uint16_t(g.replica), uint16_t(r), nd, g.ext, s0, sst, d0, dst, eb);
+  }
+  // gather: one replica of every source class into the full tensor
+  {
+    std::vector<size_t> order(sc.size());
+    for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](size_t a, size_t b) { return sc[a].volume > sc[b].volume; });
+    std::vector<int64_t> load(size_t(M), 0);
+    for (size_t ci : order) {
+      int64_t best = -1;
+      for (int64_t r : sc[ci].ranks)
+        if (best < 0 || load[size_t(r)] < load[size_t(best)]) best = r;
+      load[size_t(best)] += sc[ci].volume;
+      const Box& b = sc[ci].box;
+      int64_t sst[RESHARD_MAX_TENSOR_NDIM];
+      row_major_strides(nd, b.shp, sst);
+      int64_t d0 = 0;
+      for (int d = 0; d < nd; ++d) d0 += b.off[d] * gst[d];
+      emit_box(PG, uint16_t(best), 0, nd, b.shp, 0, sst, d0, gst, eb);
+    }
+  }
+  // slice: every destination rank copies its box out of the full tensor
+  for (int64_t r = 0; r < N; ++r) {
+    const Box& b = P->dst.box[size_t(r)];
+    if (box_volume(nd, b) == 0) continue;
+    int64_t dst[RESHARD_MAX_TENSOR_NDIM];
+    row_major_strides(nd, b.shp, dst);
+    int64_t s0 = 0;
+    for (int d = 0; d < nd; ++d) s0 += b.off[d] * gst[d];
+    emit_box(PS, scratch_buf, uint16_t(r), nd, b.shp, s0, gst, 0, dst, eb);
+  }
+  for (Program* p : {&PF, &PB, &PG, &PS}) finish_program(*p);
+  for (int k = 0; k < 4; ++k) S.n_tiles[k] = int64_t(P->prog[k].tiles.size());
+
+  // ---- traffic accounting
+  for (const reshard_tile_t& t : PF.tiles) {
+    const int64_t R = P->prog[0].goff[t.dst_group + 1] - P->prog[0].goff[t.dst_group];
+    S.fanout_read_bytes += tile_bytes(t);
+    S.fanout_write_bytes += R * tile_bytes(t);
+  }
+  for (const reshard_tile_t& t : PB.tiles) {
+    S.boxcopy_read_bytes += tile_bytes(t);
+    S.boxcopy_write_bytes += tile_bytes(t);
+  }
+  for (const Program* p : {&PG, &PS})
+    for (const reshard_tile_t& t : p->tiles) {
+      S.gb_read_bytes += tile_bytes(t);
+      S.gb_write_bytes += tile_bytes(t);
+    }
+  return RESHARD_OK;
+}
+
+}  // namespace
+
+reshard_status_t fail(reshard_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+}  // namespace rs
+
+using rs::fail;
+
+extern "C" {
+
+reshard_status_t reshard_plan_create(const int64_t* global_shape, int32_t tensor_ndim,
+                                     reshard_dtype_t dtype, const reshard_mesh_t* src_mesh,
+                                     const reshard_placement_t* src_placements,
+                                     const reshard_mesh_t* dst_mesh,
+                                     const reshard_placement_t* dst_placements,
+                                     reshard_plan_t* out_plan) {
+  const auto t0 = std::chrono::steady_clock::now();
+  if (!out_plan) return fail(RESHARD_ERR_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  if (tensor_ndim < 1 || tensor_ndim > RESHARD_MAX_TENSOR_NDIM)
+    return fail(RESHARD_ERR_UNSUPPORTED, "tensor ndim must be 1..4");
+  if (!global_shape) return fail(RESHARD_ERR_INVALID_ARG, "global_shape is NULL");
+  const int eb = rs::elem_size(dtype);
+  if (!eb) return fail(RESHARD_ERR_INVALID_ARG, "unknown dtype");
+  int64_t numel = 1;
+  for (int d = 0; d < tensor_ndim; ++d) {
+    if (global_shape[d] < 0) return fail(RESHARD_ERR_INVALID_ARG, "negative global extent");
+    if (global_shape[d] > 0 && numel > (int64_t(1) << 56) / global_shape[d])
+      return fail(RESHARD_ERR_UNSUPPORTED, "tensor too large");
+    numel *= global_shape[d];
+  }
+  reshard_plan_s* P = new (std::nothrow) reshard_plan_s();
+  if (!P) return fail(RESHARD_ERR_NO_MEMORY, "host allocation failed");
+  P->ndim = tensor_ndim;
+  P->elem_bytes = eb;
+  for (int d = 0; d < tensor_ndim; ++d) P->gshape[d] = global_shape[d];
+  reshard_status_t st = rs::read_layout("source", tensor_ndim, src_mesh, src_placements, &P->src);
+  if (st == RESHARD_OK)
+    st = rs::read_layout("destination", tensor_ndim, dst_mesh, dst_placements, &P->dst);
+  if (st == RESHARD_OK && P->src.nranks + P->dst.nranks + 1 > 65535)
+    st = fail(RESHARD_ERR_UNSUPPORTED, "M + N + 1 must fit in 16 bits");
+  if (st == RESHARD_OK) {
+    try {
+      st = rs::build_plan(P);
+    } catch (const std::bad_alloc&) {
+      st = fail(RESHARD_ERR_NO_MEMORY, "host allocation failed while planning");
+    }
+  }
+  if (st != RESHARD_OK) {
+    delete P;
+    return st;
+  }
+  P->magic = rs::kPlanMagic;
+  P->stats.planner_ns = std::chrono::duration_cast<std::chrono::nanoseconds>(
+                            std::chrono::steady_clock::now() - t0).count();
+  {
+    std::lock_guard<std::mutex> lk(rs::g_registry_mu);
+    rs::registry().insert(P);
+  }
+  *out_plan = P;
+  return RESHARD_OK;
+}
+
+reshard_status_t reshard_plan_destroy(reshard_plan_t plan) {
+  {
+    std::lock_guard<std::mutex> lk(rs::g_registry_mu);
+    if (!plan || !rs::registry().erase(plan))
+      return fail(RESHARD_ERR_BAD_HANDLE, "plan is NULL or already destroyed");
+  }
+  if (plan->d_mem) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != plan->device) cudaSetDevice(plan->device);
+    cudaFree(plan->d_mem);
+    if (cur >= 0 && cur != plan->device) cudaSetDevice(cur);
+  }
+  plan->magic = 0;
+  delete plan;
+  return RESHARD_OK;
+}
+
+reshard_status_t reshard_plan_upload(reshard_plan_t plan) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
+  if (plan->device >= 0) {
+    if (plan->device != dev)
+      return fail(RESHARD_ERR_INVALID_ARG, "plan is bound to another device");
+    return RESHARD_OK;
+  }
+  int sms = 0;
+  ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return fail(RESHARD_ERR_CUDA, std::string("device query: ") + cudaGetErrorString(ce));
+  int bps = 0;
+  reshard_status_t st = rs::copy_kernel_occupancy(&bps);
+  if (st != RESHARD_OK) return st;
+
+  // one allocation: per program tiles | prefix | goff | gbuf, each 256-byte aligned
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t total = 0;
+  size_t offs[4][4];
+  for (int k = 0; k < 4; ++k) {
+    const rs::Program& p = plan->prog[k];
+    const size_t sz[4] = {p.tiles.size() * sizeof(reshard_tile_t), p.prefix.size() * sizeof(int64_t),
+                          p.goff.size() * sizeof(uint32_t), p.gbuf.size() * sizeof(uint16_t)};
+    for (int j = 0; j < 4; ++j) {
+      offs[k][j] = total;
+      total += up(sz[j]);
+    }
+  }
+  std::vector<unsigned char> host;
+  try {
+    host.assign(total, 0);
+  } catch (const std::bad_alloc&) {
+    return fail(RESHARD_ERR_NO_MEMORY, "host staging allocation failed");
+  }
+  for (int k = 0; k < 4; ++k) {
+    const rs::Program& p = plan->prog[k];
+    if (!p.tiles.empty()) std::memcpy(&host[offs[k][0]], p.tiles.data(), p.tiles.size() * sizeof(reshard_tile_t));
+    if (!p.prefix.empty()) std::memcpy(&host[offs[k][1]], p.prefix.data(), p.prefix.size() * sizeof(int64_t));
+    if (!p.goff.empty()) std::memcpy(&host[offs[k][2]], p.goff.data(), p.goff.size() * sizeof(uint32_t));
+    if (!p.gbuf.empty()) std::memcpy(&host[offs[k][3]], p.gbuf.data(), p.gbuf.size() * sizeof(uint16_t));
+  }
+  void* d = nullptr;
+  ce = cudaMalloc(&d, std::max<size_t>(total, 256));
+  if (ce != cudaSuccess) return fail(RESHARD_ERR_NO_MEMORY, std::string("cudaMalloc: ") + cudaGetErrorString(ce));
+  ce = cudaMemcpy(d, host.data(), total, cudaMemcpyHostToDevice);
+  if (ce != cudaSuccess) {
+    cudaFree(d);
+    return fail(RESHARD_ERR_CUDA, std::string("cudaMemcpy: ") + cudaGetErrorString(ce));
+  }
+  unsigned char* base = static_cast<unsigned char*>(d);
+  for (int k = 0; k < 4; ++k) {
+    rs::Program& p = plan->prog[k];
+    p.d_tiles = reinterpret_cast<const reshard_tile_t*>(base + offs[k][0]);
+    p.d_prefix = reinterpret_cast<const int64_t*>(base + offs[k][1]);
+    p.d_goff = reinterpret_cast<const uint32_t*>(base + offs[k][2]);
+    p.d_gbuf = reinterpret_cast<const uint16_t*>(base + offs[k][3]);
+  }
+  plan->d_mem = d;
+  plan->device = dev;
+  plan->num_sms = sms;
+  plan->blocks_per_sm = bps;
+  return RESHARD_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Build the buffer table [src..., dst..., scratch] and check null pointers.
+reshard_status_t buffer_table(reshard_plan_t plan, const void* const* src_ptrs,
+                              void* const* dst_ptrs, void* scratch, std::vector<unsigned char*>* bufs) {
+  const int64_t M = plan->src.nranks, N = plan->dst.nranks;
+  if (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS)
+    return fail(RESHARD_ERR_UNSUPPORTED, "M + N + 1 exceeds RESHARD_MAX_EXEC_BUFFERS");
+  if (!src_ptrs || !dst_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "null pointer array");
+  bufs->resize(size_t(M + N + 1));
+  for (int64_t r = 0; r < M; ++r) {
+    if (!src_ptrs[r] && rs::box_volume(plan->ndim, plan->src.box[size_t(r)]) > 0)
+      return fail(RESHARD_ERR_INVALID_ARG, "NULL source pointer for a non-empty shard (rank " +
+                                               std::to_string(r) + ")");
+    (*bufs)[size_t(r)] = static_cast<unsigned char*>(const_cast<void*>(src_ptrs[r]));
+  }
+  for (int64_t r = 0; r < N; ++r) {
+    if (!dst_ptrs[r] && rs::box_volume(plan->ndim, plan->dst.box[size_t(r)]) > 0)
+      return fail(RESHARD_ERR_INVALID_ARG, "NULL destination pointer for a non-empty shard (rank " +
+                                               std::to_string(r) + ")");
+    (*bufs)[size_t(M + r)] = static_cast<unsigned char*>(dst_ptrs[r]);
+  }
+  (*bufs)[size_t(M + N)] = static_cast<unsigned char*>(scratch);
+  return RESHARD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+reshard_status_t reshard_execute_ex(reshard_plan_t plan, const void* const* src_ptrs,
+                                    void* const* dst_ptrs, int32_t kernel, void* stream) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (kernel != RESHARD_KERNEL_FANOUT && kernel != RESHARD_KERNEL_BOXCOPY)
+    return fail(RESHARD_ERR_INVALID_ARG, "unknown kernel");
+  std::vector<unsigned char*> bufs;
+  reshard_status_t st = buffer_table(plan, src_ptrs, dst_ptrs, nullptr, &bufs);
+  if (st != RESHARD_OK) return st;
+  st = reshard_plan_upload(plan);
+  if (st != RESHARD_OK) return st;
+  const rs::Program& p =
+      plan->prog[kernel == RESHARD_KERNEL_FANOUT ? RESHARD_PROGRAM_FANOUT : RESHARD_PROGRAM_BOXCOPY];
+  return rs::launch_program(plan, p, bufs.data(), int(bufs.size()), stream);
+}
+
+reshard_status_t reshard_execute(reshard_plan_t plan, const void* const* src_ptrs,
+                                 void* const* dst_ptrs, void* stream) {
+  return reshard_execute_ex(plan, src_ptrs, dst_ptrs, RESHARD_KERNEL_FANOUT, stream);
+}
+
+reshard_status_t gather_broadcast_execute(reshard_plan_t plan, const void* const* src_ptrs,
+                                          void* const* dst_ptrs, void* full_scratch,
+                                          size_t scratch_bytes, void* stream) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (plan->stats.global_bytes > 0) {
+    if (!full_scratch) return fail(RESHARD_ERR_INVALID_ARG, "full_scratch is NULL");
+    if (scratch_bytes < size_t(plan->stats.global_bytes))
+      return fail(RESHARD_ERR_INVALID_ARG, "full_scratch is smaller than the global tensor");
+  }
+  std::vector<unsigned char*> bufs;
+  reshard_status_t st = buffer_table(plan, src_ptrs, dst_ptrs, full_scratch, &bufs);
+  if (st != RESHARD_OK) return st;
+  st = reshard_plan_upload(plan);
+  if (st != RESHARD_OK) return st;
+  st = rs::launch_program(plan, plan->prog[RESHARD_PROGRAM_GATHER], bufs.data(), int(bufs.size()), stream);
+  if (st != RESHARD_OK) return st;
+  return rs::launch_program(plan, plan->prog[RESHARD_PROGRAM_SLICE], bufs.data(), int(bufs.size()), stream);
+}
+
+reshard_status_t reshard_plan_local_shape(reshard_plan_t plan, int32_t side, int64_t rank,
+                                          int64_t* shape, int64_t* offset) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (side != 0 && side != 1) return fail(RESHARD_ERR_INVALID_ARG, "side must be 0 or 1");
+  const rs::Layout& L = side == 0 ? plan->src : plan->dst;
+  if (rank < 0 || rank >= L.nranks) return fail(RESHARD_ERR_INVALID_ARG, "rank out of range");
+  if (!shape && !offset) return fail(RESHARD_ERR_INVALID_ARG, "both outputs are NULL");
+  for (int d = 0; d < plan->ndim; ++d) {
+    if (shape) shape[d] = L.box[size_t(rank)].shp[d];
+    if (offset) offset[d] = L.box[size_t(rank)].off[d];
+  }
+  return RESHARD_OK;
+}
+
+reshard_status_t reshard_plan_stats(reshard_plan_t plan, reshard_stats_t* out) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (!out) return fail(RESHARD_ERR_INVALID_ARG, "out is NULL");
+  *out = plan->stats;
+  return RESHARD_OK;
+}
+
+reshard_status_t reshard_plan_program(reshard_plan_t plan, int32_t program,
+                                      const reshard_tile_t** tiles, int64_t* ntiles,
+                                      const int64_t** unit_prefix, const uint32_t** group_offsets,
+                                      const uint16_t** group_buffers, int64_t* ngroups) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (program < 0 || program > 3) return fail(RESHARD_ERR_INVALID_ARG, "unknown program");
+  const rs::Program& p = plan->prog[program];
+  if (tiles) *tiles = p.tiles.data();
+  if (ntiles) *ntiles = int64_t(p.tiles.size());
+  if (unit_prefix) *unit_prefix = p.prefix.data();
+  if (group_offsets) *group_offsets = p.goff.data();
+  if (group_buffers) *group_buffers = p.gbuf.data();
+  if (ngroups) *ngroups = int64_t(p.goff.size()) - 1;
+  return RESHARD_OK;
+}
+
+int64_t reshard_tile_units(const reshard_tile_t* tile) {
+  return tile ? rs::tile_units(*tile) : 0;
+}
+
+const char* reshard_last_error(void) { return rs::g_last_error.c_str(); }
+
+const char* reshard_version(void) { return "libreshard 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,279 @@
+/*
+ * reshard.h -- C ABI of libreshard.so, a single-GPU DTensor-to-DTensor reshard.
+ *
+ * A global tensor laid out as M source shards (a device mesh plus one
+ * Shard(dim) / Replicate placement per mesh dim) is rewritten into N
+ * destination shards of another layout.  Only the intersections of source and
+ * destination shard boxes are moved; the full tensor is never materialised on
+ * the reshard path.  All shard buffers live in the memory of the current CUDA
+ * device: every source or destination "rank" is simply its own device buffer.
+ *
+ * Defining passages ("Accelerating Reinforcement Learning Weight Refit with the
+ * Reshard Collective", as summarised by the pages cited below):
+ *  - news.bpdata.com, section "A megkozelites: refit mint DTensor-to-DTensor
+ *    reshard": a DTensor is a global shape, a device mesh and placements
+ *    (sharded or replicated); a destination shard can be built from parts of
+ *    several source shards, and a replicated weight is available at several
+ *    sources.
+ *  - news.bpdata.com, section "A Reshard kollektiv kommunikacio": one call is
+ *    given the source and destination DTensor descriptions; the library first
+ *    determines the exact intersections of source and destination shards, then
+ *    maps the transfers, sending each contribution once and letting replicas
+ *    assemble their shard locally.
+ *  - techfeed.io, section "Reshard Collective: DTensor-to-DTensor": the call is
+ *    made once from the application, like all-reduce or all-gather, and the
+ *    library derives the transfer pattern.
+ *
+ * Conventions shared by every entry point
+ *  - Ranks are flat, row-major coordinates on their mesh.  Source and
+ *    destination ranks are distinct buffers even when the meshes are equal.
+ *  - A local shard is a contiguous row-major array of its local shape.
+ *  - Uneven splits follow torch.chunk: Shard(d) on a mesh dim of size k splits
+ *    the current local extent n of tensor dim d into chunks of ceil(n/k);
+ *    trailing ranks get short or EMPTY shards.  Several mesh dims sharding the
+ *    same tensor dim nest in mesh-dim order (mesh dim 0 outermost).
+ *  - The reshard is a bit copy: the element size comes from the dtype, no
+ *    value is converted, NaN payloads and -0 survive.
+ *  - Every call returns a reshard_status_t; none aborts, traps or prints.  On
+ *    failure reshard_last_error() describes the cause.
+ *  - The caller owns every device buffer and stream.  Execution entry points
+ *    enqueue work on `stream` (a cudaStream_t, NULL = legacy default stream)
+ *    and return without synchronising; buffers must stay alive until that
+ *    work has completed.  Pointer arrays are read during the call only.
+ *  - Source replicas must hold identical bytes (they are replicas); which
+ *    replica supplies a region is the planner's choice.
+ */
+#ifndef RESHARD_H_
+#define RESHARD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RESHARD_MAX_TENSOR_NDIM 4
+#define RESHARD_MAX_MESH_NDIM 4
+/* Largest M + N (+1 for the scratch buffer) one execution call accepts. */
+#define RESHARD_MAX_EXEC_BUFFERS 1024
+/* Largest M or N plan creation accepts (planner-only use may exceed the above). */
+#define RESHARD_MAX_RANKS 65000
+
+typedef enum reshard_status {
+  RESHARD_OK = 0,
+  RESHARD_ERR_INVALID_ARG = 1, /* null pointer, bad enum, negative size, ... */
+  RESHARD_ERR_UNSUPPORTED = 2, /* valid request outside what this library does */
+  RESHARD_ERR_SHAPE = 3,       /* layout inconsistent with the tensor shape */
+  RESHARD_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  RESHARD_ERR_NO_MEMORY = 5,   /* host or device allocation failed */
+  RESHARD_ERR_BAD_HANDLE = 6   /* plan is NULL, destroyed or never created */
+} reshard_status_t;
+
+/* Element types.  Only the element size matters (bit copy). */
+typedef enum reshard_dtype {
+  RESHARD_U8 = 0,   /* 1 byte  */
+  RESHARD_BF16 = 1, /* 2 bytes */
+  RESHARD_FP16 = 2, /* 2 bytes */
+  RESHARD_FP32 = 3, /* 4 bytes */
+  RESHARD_I32 = 4,  /* 4 bytes */
+  RESHARD_FP64 = 5, /* 8 bytes */
+  RESHARD_I64 = 6   /* 8 bytes */
+} reshard_dtype_t;
+
+/* Placement of a tensor on one mesh dim (DTensor's Replicate / Shard(dim)).
+ * Partial (pending-reduction) placements are not part of the method. */
+typedef enum reshard_placement_kind {
+  RESHARD_REPLICATE = 0,
+  RESHARD_SHARD = 1
+} reshard_placement_kind_t;
+
+typedef struct reshard_placement {
+  int32_t kind; /* reshard_placement_kind_t */
+  int32_t dim;  /* tensor dim for RESHARD_SHARD, ignored for RESHARD_REPLICATE */
+} reshard_placement_t;
+
+typedef struct reshard_mesh {
+  int32_t ndim;                           /* 1..RESHARD_MAX_MESH_NDIM */
+  int64_t shape[RESHARD_MAX_MESH_NDIM];   /* sizes >= 1; ranks = product */
+} reshard_mesh_t;
+
+typedef struct reshard_plan_s* reshard_plan_t;
+
+/* Which copy kernel an execution uses. */
+typedef enum reshard_kernel {
+  /* Read-once fan-out (default): each region is read once from one source
+   * replica and written to every destination replica that needs it.  HBM
+   * traffic = global bytes G (read) + destination bytes D (write). */
+  RESHARD_KERNEL_FANOUT = 0,
+  /* Plain box copy: one copy per (region, destination replica); the source
+   * is re-read for every replica.  HBM traffic = D (read) + D (write). */
+  RESHARD_KERNEL_BOXCOPY = 1
+} reshard_kernel_t;
+
+/* Copy programs a plan holds (for inspection and for the CPU test executor). */
+typedef enum reshard_program {
+  RESHARD_PROGRAM_FANOUT = 0,  /* reshard, read-once fan-out */
+  RESHARD_PROGRAM_BOXCOPY = 1, /* reshard, one copy per destination replica */
+  RESHARD_PROGRAM_GATHER = 2,  /* gather-and-broadcast step 1: shards -> full */
+  RESHARD_PROGRAM_SLICE = 3    /* gather-and-broadcast step 2: full -> shards */
+} reshard_program_t;
+
+/* Planner and traffic statistics of one plan (all byte counts exact). */
+typedef struct reshard_stats {
+  int64_t global_bytes;        /* G: bytes of the global tensor */
+  int64_t src_bytes;           /* sum of all source shard bytes (replicas included) */
+  int64_t dst_bytes;           /* D: sum of all destination shard bytes (replicas included) */
+  int64_t n_src_ranks, n_dst_ranks;
+  int64_t n_src_classes;       /* distinct non-empty source boxes */
+  int64_t n_dst_classes;       /* distinct non-empty destination boxes (fan-out groups) */
+  int64_t n_regions;           /* source-class x destination-class intersections moved */
+  int64_t region_bytes;        /* sum of region bytes (= G for a complete layout) */
+  int64_t n_tiles[4];          /* tiles per reshard_program_t */
+  int64_t fanout_read_bytes, fanout_write_bytes;    /* HBM bytes of RESHARD_KERNEL_FANOUT */
+  int64_t boxcopy_read_bytes, boxcopy_write_bytes;  /* HBM bytes of RESHARD_KERNEL_BOXCOPY */
+  int64_t gb_read_bytes, gb_write_bytes;            /* HBM bytes of gather_broadcast_execute */
+  int64_t max_replica_read_bytes;  /* busiest source replica's bytes read (fan-out plan) */
+  int64_t max_fanout;          /* largest number of destination replicas of one box */
+  int64_t planner_ns;          /* wall time of reshard_plan_create */
+} reshard_stats_t;
+
+/*
+ * One copy descriptor ("tile") as the kernels execute it, exposed read-only
+ * for inspection and tests.  A tile copies nplanes x nrows rows of row_bytes
+ * from its source buffer to the same local place in every buffer of its
+ * destination group.  Byte offsets and strides are relative to the start of
+ * the buffers.  Buffer indices: [0, M) source ranks, [M, M+N) destination
+ * ranks, M+N the gather-and-broadcast scratch.
+ */
+typedef struct reshard_tile {
+  int64_t src_off, dst_off;                   /* bytes, first row of plane 0 */
+  int64_t src_row_stride, dst_row_stride;     /* bytes between rows */
+  int64_t src_plane_stride, dst_plane_stride; /* bytes between planes */
+  uint32_t row_bytes;                         /* contiguous bytes per row */
+  uint32_t nrows;                             /* rows per plane */
+  uint32_t nplanes;
+  uint16_t src_buf;                           /* buffer index of the source */
+  uint16_t dst_group;                         /* destination group index */
+} reshard_tile_t;
+
+/*
+ * Plan a reshard of one tensor (steps: resolve both layouts, intersect every
+ * source box with every destination box, pick one source replica per region
+ * balancing bytes read across replicas, collapse contiguous dims into copy
+ * descriptors, group destination replicas for fan-out, sort by destination).
+ * Host only: needs no GPU and touches no device memory.
+ *
+ * global_shape  [tensor_ndim] extents >= 0 (1 <= tensor_ndim <= 4)
+ * dtype         element type (sets the element size)
+ * src_mesh, src_placements[src_mesh->ndim]: source layout
+ * dst_mesh, dst_placements[dst_mesh->ndim]: destination layout
+ * out_plan      receives the plan; release it with reshard_plan_destroy().
+ * Errors: INVALID_ARG (null/ranges/enums), UNSUPPORTED (ndim or ranks beyond
+ * the limits above), NO_MEMORY.
+ */
+reshard_status_t reshard_plan_create(const int64_t* global_shape, int32_t tensor_ndim,
+                                     reshard_dtype_t dtype, const reshard_mesh_t* src_mesh,
+                                     const reshard_placement_t* src_placements,
+                                     const reshard_mesh_t* dst_mesh,
+                                     const reshard_placement_t* dst_placements,
+                                     reshard_plan_t* out_plan);
+
+/*
+ * Copy the plan's descriptor tables to the CURRENT device (one cudaMalloc and
+ * one synchronous cudaMemcpy) and bind the plan to it.  Executions call this
+ * themselves on first use; call it explicitly to keep allocation out of the
+ * first execution, and always before capturing an execution in a CUDA graph.
+ * Errors: BAD_HANDLE, CUDA (no device, copy failed), NO_MEMORY,
+ * INVALID_ARG (plan already bound to a different device).
+ */
+reshard_status_t reshard_plan_upload(reshard_plan_t plan);
+
+/*
+ * The reshard itself (news.bpdata.com, section "A Reshard kollektiv
+ * kommunikacio"): every destination shard receives exactly the intersections
+ * of its box with the source boxes, each region read once and fanned out to
+ * all destination replicas.  Equivalent to
+ * reshard_execute_ex(plan, src_ptrs, dst_ptrs, RESHARD_KERNEL_FANOUT, stream).
+ *
+ * src_ptrs[M]  device pointers of the source shards (NULL allowed only for an
+ *              empty shard).  dst_ptrs[N] likewise for the destinations.
+ * Destination buffers must not overlap each other or any source buffer.
+ * Errors: BAD_HANDLE, INVALID_ARG (null pointer for a non-empty shard),
+ * UNSUPPORTED (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS), CUDA (launch failed).
+ */
+reshard_status_t reshard_execute(reshard_plan_t plan, const void* const* src_ptrs,
+                                 void* const* dst_ptrs, void* stream);
+
+/* reshard_execute with an explicit choice of copy kernel (reshard_kernel_t). */
+reshard_status_t reshard_execute_ex(reshard_plan_t plan, const void* const* src_ptrs,
+                                    void* const* dst_ptrs, int32_t kernel, void* stream);
+
+/*
+ * The conventional refit path, kept as the baseline (news.bpdata.com, section
+ * "Miert problema a sulyrefit az RL post-training soran?"; techfeed.io, section
+ * on the payload being twice the model size): all-gather the full parameter,
+ * broadcast it, and let every destination keep its slice.  On one GPU the
+ * broadcast is free, so this is: (1) every source region is written into
+ * `full_scratch` (the global tensor, row-major), then (2) every destination
+ * rank copies its own box out of it.  Same destination bytes as
+ * reshard_execute.  HBM traffic = 2G + 2D.
+ *
+ * full_scratch  device buffer of at least G bytes, owned by the caller; its
+ *               contents on return are the global tensor.
+ * scratch_bytes its size in bytes.
+ * Errors: as reshard_execute, plus INVALID_ARG when scratch_bytes < G or
+ * full_scratch is NULL for a non-empty tensor.
+ */
+reshard_status_t gather_broadcast_execute(reshard_plan_t plan, const void* const* src_ptrs,
+                                          void* const* dst_ptrs, void* full_scratch,
+                                          size_t scratch_bytes, void* stream);
+
+/*
+ * Local box of one rank (news.bpdata.com, section "A megkozelites": the DTensor
+ * description fixes each rank's shard).  side 0 = source, 1 = destination.
+ * shape[tensor_ndim], offset[tensor_ndim] receive the local shape and the
+ * global offset; an empty dim reports offset = global extent (DTensor's
+ * convention).  Errors: BAD_HANDLE, INVALID_ARG.
+ */
+reshard_status_t reshard_plan_local_shape(reshard_plan_t plan, int32_t side, int64_t rank,
+                                          int64_t* shape, int64_t* offset);
+
+/* Planner and traffic statistics.  Errors: BAD_HANDLE, INVALID_ARG. */
+reshard_status_t reshard_plan_stats(reshard_plan_t plan, reshard_stats_t* out);
+
+/*
+ * Read-only view of one copy program (reshard_program_t) of the plan, valid
+ * until the plan is destroyed: tiles[ntiles], unit_prefix[ntiles + 1] (the
+ * kernels' work units; see reshard_tile_units), group_offsets[ngroups + 1]
+ * and group_buffers[group_offsets[ngroups]] (destination buffer indices of
+ * each group).  Any output pointer may be NULL.  Errors: BAD_HANDLE,
+ * INVALID_ARG.
+ */
+reshard_status_t reshard_plan_program(reshard_plan_t plan, int32_t program,
+                                      const reshard_tile_t** tiles, int64_t* ntiles,
+                                      const int64_t** unit_prefix,
+                                      const uint32_t** group_offsets,
+                                      const uint16_t** group_buffers, int64_t* ngroups);
+
+/*
+ * Work units of a tile: a single-row tile is split into 4096-byte units, a
+ * multi-row tile into units of max(1, 4096 / row_bytes) rows.  Each CTA of a
+ * copy kernel takes an equal share of a program's units.  Returns 0 for NULL.
+ */
+int64_t reshard_tile_units(const reshard_tile_t* tile);
+
+/* Release a plan and its device tables.  Errors: BAD_HANDLE. */
+reshard_status_t reshard_plan_destroy(reshard_plan_t plan);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* reshard_last_error(void);
+
+/* Library version string. */
+const char* reshard_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RESHARD_H_ */

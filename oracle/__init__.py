@@ -99,6 +99,12 @@ class Oracle:
                                            ctypes.c_int32, _I64P, _I32P,
                                            ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p]
         lib.oracle_gather_full.restype = ctypes.c_int
+        lib.oracle_reshard_elems.argtypes = [ctypes.c_int32, _I64P, ctypes.c_int64,
+                                             ctypes.c_int32, _I64P, _I32P,
+                                             ctypes.c_int32, _I64P, _I32P,
+                                             ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p,
+                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+        lib.oracle_reshard_elems.restype = ctypes.c_int
         self.lib = lib
 
     # -- layout --------------------------------------------------------------------------
@@ -142,6 +148,23 @@ class Oracle:
                 raise OracleError(f"oracle_reshard failed ({rc}) for dst rank {r}")
             outs.append(out)
         return outs
+
+    def reshard_elems(self, gshape, elem_bytes, src_mesh, src_pl, dst_mesh, dst_pl, src_ptrs,
+                      dst_ptr, dst_rank, e_begin, e_end):
+        """Elements [e_begin, e_end) of one destination rank, on raw host pointers.
+
+        ``src_ptrs`` are host addresses of the source shards (ints or None),
+        ``dst_ptr`` the host address of the rank's whole local shard.
+        """
+        sp = (ctypes.c_void_p * max(1, len(src_ptrs)))(*src_ptrs)
+        rc = self.lib.oracle_reshard_elems(len(gshape), _arr64(gshape), int(elem_bytes),
+                                           len(src_mesh), _arr64(src_mesh),
+                                           _arr32(shard_dims(src_pl)),
+                                           len(dst_mesh), _arr64(dst_mesh),
+                                           _arr32(shard_dims(dst_pl)),
+                                           sp, dst_ptr, int(dst_rank), int(e_begin), int(e_end))
+        if rc:
+            raise OracleError(f"oracle_reshard_elems failed ({rc})")
 
     def source_of(self, gshape, src_mesh, src_pl, dst_mesh, dst_pl, dst_rank, dst_linear):
         """(src rank, src linear element index) that supplies one dst element."""

@@ -202,6 +202,45 @@ static int64_t owner_of(const src_boxes* sb, const int64_t* g) {
 }
 
 /*
+ * Elements [e_begin, e_end) (row-major linear indices) of destination rank r,
+ * written to out (which holds the whole local shard of r).
+ */
+static int fill_rank(const src_boxes* sb, int32_t ndim, const int64_t* gshape, int64_t elem_bytes,
+                     int32_t dst_mesh_ndim, const int64_t* dst_mesh, const int32_t* dst_shard_dim,
+                     const void* const* src_bufs, int64_t r, int64_t e_begin, int64_t e_end,
+                     unsigned char* out) {
+  int64_t doff[ORACLE_MAX_NDIM], dshp[ORACLE_MAX_NDIM];
+  oracle_resolve(ndim, gshape, dst_mesh_ndim, dst_mesh, dst_shard_dim, r, doff, dshp);
+  int64_t n = volume(ndim, dshp);
+  if (e_begin < 0 || e_end > n || e_begin > e_end) return -1;
+  int64_t i[ORACLE_MAX_NDIM], g[ORACLE_MAX_NDIM], j[ORACLE_MAX_NDIM];
+  /* local multi-index of element e_begin */
+  int64_t rest = e_begin;
+  for (int32_t d = ndim - 1; d >= 0; --d) {
+    i[d] = dshp[d] ? rest % dshp[d] : 0;
+    rest = dshp[d] ? rest / dshp[d] : 0;
+  }
+  for (int64_t e = e_begin; e < e_end; ++e) {
+    /* e is the row-major linear index of local multi-index i */
+    for (int32_t d = 0; d < ndim; ++d) g[d] = doff[d] + i[d];
+    int64_t s = owner_of(sb, g);
+    if (s < 0) return -2;
+    const int64_t* soff = sb->off + s * ndim;
+    const int64_t* sshp = sb->shp + s * ndim;
+    for (int32_t d = 0; d < ndim; ++d) j[d] = g[d] - soff[d];
+    const unsigned char* in = (const unsigned char*)src_bufs[s];
+    memcpy(out + linear(ndim, i, dshp) * elem_bytes, in + linear(ndim, j, sshp) * elem_bytes,
+           (size_t)elem_bytes);
+    /* advance the local multi-index (odometer, last dim fastest) */
+    for (int32_t d = ndim - 1; d >= 0; --d) {
+      if (++i[d] < dshp[d]) break;
+      i[d] = 0;
+    }
+  }
+  return 0;
+}
+
+/*
  * Fill destination ranks [dst_begin, dst_end) of the destination layout from
  * the source shards.  src_bufs[s] is source rank s's local buffer (may be NULL
  * for an empty shard), dst_bufs[r - dst_begin] is destination rank r's.
@@ -219,37 +258,37 @@ int oracle_reshard(int32_t ndim, const int64_t* gshape, int64_t elem_bytes,
   src_boxes sb;
   int rc = load_src_boxes(&sb, ndim, gshape, src_mesh_ndim, src_mesh, src_shard_dim);
   if (rc) return rc;
-
-  for (int64_t r = dst_begin; r < dst_end; ++r) {
+  for (int64_t r = dst_begin; r < dst_end && rc == 0; ++r) {
     int64_t doff[ORACLE_MAX_NDIM], dshp[ORACLE_MAX_NDIM];
     oracle_resolve(ndim, gshape, dst_mesh_ndim, dst_mesh, dst_shard_dim, r, doff, dshp);
-    int64_t n = volume(ndim, dshp);
-    unsigned char* out = (unsigned char*)dst_bufs[r - dst_begin];
-    int64_t i[ORACLE_MAX_NDIM], g[ORACLE_MAX_NDIM], j[ORACLE_MAX_NDIM];
-    for (int32_t d = 0; d < ndim; ++d) i[d] = 0;
-    for (int64_t e = 0; e < n; ++e) {
-      /* e is the row-major linear index of local multi-index i */
-      for (int32_t d = 0; d < ndim; ++d) g[d] = doff[d] + i[d];
-      int64_t s = owner_of(&sb, g);
-      if (s < 0) {
-        free_src_boxes(&sb);
-        return -2;
-      }
-      const int64_t* soff = sb.off + s * ndim;
-      const int64_t* sshp = sb.shp + s * ndim;
-      for (int32_t d = 0; d < ndim; ++d) j[d] = g[d] - soff[d];
-      const unsigned char* in = (const unsigned char*)src_bufs[s];
-      memcpy(out + linear(ndim, i, dshp) * elem_bytes, in + linear(ndim, j, sshp) * elem_bytes,
-             (size_t)elem_bytes);
-      /* advance the local multi-index (odometer, last dim fastest) */
-      for (int32_t d = ndim - 1; d >= 0; --d) {
-        if (++i[d] < dshp[d]) break;
-        i[d] = 0;
-      }
-    }
+    rc = fill_rank(&sb, ndim, gshape, elem_bytes, dst_mesh_ndim, dst_mesh, dst_shard_dim,
+                   src_bufs, r, 0, volume(ndim, dshp), (unsigned char*)dst_bufs[r - dst_begin]);
   }
   free_src_boxes(&sb);
-  return 0;
+  return rc;
+}
+
+/*
+ * The same definition restricted to elements [e_begin, e_end) of one
+ * destination rank (dst_buf holds that rank's whole local shard).  Used to
+ * time the oracle on a bounded part of a large workload.
+ */
+int oracle_reshard_elems(int32_t ndim, const int64_t* gshape, int64_t elem_bytes,
+                         int32_t src_mesh_ndim, const int64_t* src_mesh,
+                         const int32_t* src_shard_dim, int32_t dst_mesh_ndim,
+                         const int64_t* dst_mesh, const int32_t* dst_shard_dim,
+                         const void* const* src_bufs, void* dst_buf, int64_t dst_rank,
+                         int64_t e_begin, int64_t e_end) {
+  if (elem_bytes < 1) return -1;
+  if (check_layout(ndim, gshape, dst_mesh_ndim, dst_mesh, dst_shard_dim)) return -1;
+  if (dst_rank < 0 || dst_rank >= mesh_ranks(dst_mesh_ndim, dst_mesh)) return -1;
+  src_boxes sb;
+  int rc = load_src_boxes(&sb, ndim, gshape, src_mesh_ndim, src_mesh, src_shard_dim);
+  if (rc) return rc;
+  rc = fill_rank(&sb, ndim, gshape, elem_bytes, dst_mesh_ndim, dst_mesh, dst_shard_dim, src_bufs,
+                 dst_rank, e_begin, e_end, (unsigned char*)dst_buf);
+  free_src_boxes(&sb);
+  return rc;
 }
 
 /*

@@ -1,0 +1,75 @@
+"""Test helpers: scattering with the oracle's layout, a CPU executor of plan tiles.
+
+The CPU tile executor is test code that runs the library's copy programs on
+host byte buffers, so planner mistakes show up without a GPU.  It is never used
+by the library or the benchmark.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import dtensor_reshard_gb300 as rs
+
+
+def oracle_boxes(o, gshape, mesh, placements):
+    return o.boxes(gshape, mesh, placements)
+
+
+def slice_box(t: torch.Tensor, off, shp) -> torch.Tensor:
+    """Contiguous local shard of a global tensor for a box (offset, shape)."""
+    if math.prod(shp) == 0:
+        return t.new_empty(tuple(shp))
+    sl = tuple(slice(a, a + b) for a, b in zip(off, shp))
+    return t[sl].contiguous()
+
+
+def to_bytes(t: torch.Tensor) -> np.ndarray:
+    t = t.contiguous().cpu()
+    if t.numel() == 0:
+        return np.zeros(0, dtype=np.uint8)
+    return t.view(torch.uint8).reshape(-1).numpy().copy()
+
+
+def scatter_with_oracle(o, glob: torch.Tensor, mesh, placements):
+    """Source shards (contiguous tensors) of ``glob`` under a layout, by the oracle's boxes."""
+    gshape = tuple(glob.shape)
+    return [slice_box(glob, off, shp) for off, shp in oracle_boxes(o, gshape, mesh, placements)]
+
+
+def expected_dst(o, spec, src_bytes):
+    """Oracle's destination byte buffers for a TensorSpec-like object."""
+    return o.reshard(spec.global_shape, spec.elem_bytes, spec.src_mesh, spec.src_placements,
+                     spec.dst_mesh, spec.dst_placements, src_bytes)
+
+
+def run_program_cpu(plan, program, bufs):
+    """Execute one copy program of ``plan`` on host buffers (list of uint8 arrays).
+
+    ``bufs`` is the buffer table [sources..., destinations..., scratch].  Returns,
+    per buffer, a count array of how many times each byte was written.
+    """
+    tiles, prefix, goff, gbuf = rs.reshard_plan_program(plan, program)
+    writes = [np.zeros(b.size, dtype=np.int32) for b in bufs]
+    for t in tiles:
+        src = bufs[t["src_buf"]]
+        for g in range(goff[t["dst_group"]], goff[t["dst_group"] + 1]):
+            di = gbuf[g]
+            dst = bufs[di]
+            for p in range(t["nplanes"]):
+                for r in range(t["nrows"]):
+                    so = t["src_off"] + p * t["src_plane_stride"] + r * t["src_row_stride"]
+                    do = t["dst_off"] + p * t["dst_plane_stride"] + r * t["dst_row_stride"]
+                    n = t["row_bytes"]
+                    assert 0 <= so and so + n <= src.size, ("source out of bounds", t)
+                    assert 0 <= do and do + n <= dst.size, ("destination out of bounds", t)
+                    dst[do:do + n] = src[so:so + n]
+                    writes[di][do:do + n] += 1
+    return writes
+
+
+def spec_plan(spec):
+    return rs.reshard_plan_create(spec.global_shape, spec.dtype, spec.src_mesh,
+                                  spec.src_placements, spec.dst_mesh, spec.dst_placements)

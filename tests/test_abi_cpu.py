@@ -1,0 +1,145 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol, and its
+host-side entry points (planning, queries, argument checks, handle checks) behave."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import dtensor_reshard_gb300 as rs
+from inputs import workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "reshard.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\([^;{]*\)\s*;", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("reshard_plan_create", "reshard_execute", "gather_broadcast_execute",
+                     "reshard_plan_local_shape", "reshard_plan_stats", "reshard_plan_destroy",
+                     "reshard_last_error"):
+        assert required in names, required
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(rs.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_struct_layouts_match_header():
+    assert ctypes.sizeof(rs.reshard_tile_t) == 64
+    assert ctypes.sizeof(rs.reshard_mesh_t) == 40
+    assert ctypes.sizeof(rs.reshard_placement_t) == 8
+
+
+def _create(gshape, dtype, sm, sp, dm, dp):
+    shape = (ctypes.c_int64 * max(1, len(gshape)))(*gshape)
+    h = ctypes.c_void_p()
+    st = rs._lib.reshard_plan_create(shape, len(gshape), dtype, ctypes.byref(rs._mesh(sm)),
+                                     rs._placements(sp), ctypes.byref(rs._mesh(dm)),
+                                     rs._placements(dp), ctypes.byref(h))
+    return st, h
+
+
+@pytest.mark.parametrize("args,status", [
+    (((8, 8), 1, (2,), ("S0",), (4,), ("S2",)), 1),           # shard dim out of range
+    (((8, 8), 99, (2,), ("S0",), (4,), ("S1",)), 1),          # unknown dtype
+    (((8, 8), 1, (0,), ("S0",), (4,), ("S1",)), 1),           # mesh size 0
+    (((8, -1), 1, (2,), ("S0",), (4,), ("S1",)), 1),          # negative extent
+    (((1, 2, 3, 4, 5), 1, (2,), ("S0",), (4,), ("S1",)), 2),  # tensor ndim 5
+    (((8, 8), 1, (1, 1, 1, 1, 1), ("R",) * 5, (4,), ("S1",)), 2),  # mesh ndim 5
+    (((8, 8), 1, (2,), ((7, 0),), (4,), ("S1",)), 2),         # Partial-like placement kind
+])
+def test_plan_create_rejects_bad_arguments(args, status):
+    st, h = _create(*args)
+    assert st == status, rs.reshard_last_error()
+    assert not h.value
+    assert rs.reshard_last_error()
+
+
+def test_null_out_plan_and_null_shape():
+    assert rs._lib.reshard_plan_create(None, 2, 1, None, None, None, None, None) == 1
+    h = ctypes.c_void_p()
+    assert rs._lib.reshard_plan_create(None, 2, 1, None, None, None, None, ctypes.byref(h)) == 1
+
+
+def test_handle_checks_after_destroy():
+    st, h = _create((8, 8), 1, (2,), ("S0",), (4,), ("S1",))
+    assert st == 0
+    assert rs._lib.reshard_plan_destroy(h) == 0
+    assert rs._lib.reshard_plan_destroy(h) == 6
+    s = rs.reshard_stats_t()
+    assert rs._lib.reshard_plan_stats(h, ctypes.byref(s)) == 6
+    assert rs._lib.reshard_execute(h, None, None, None) == 6
+    assert rs._lib.reshard_plan_stats(None, ctypes.byref(s)) == 6
+    # a pointer that was never a plan
+    bogus = ctypes.c_void_p(ctypes.addressof(s))
+    assert rs._lib.reshard_plan_stats(bogus, ctypes.byref(s)) == 6
+
+
+def test_execute_argument_checks_before_any_device_work():
+    p = rs.reshard_plan_create((8, 8), "bf16", (2,), ("S0",), (4,), ("S1",))
+    srcs = (ctypes.c_void_p * 2)(None, 0x1000)   # NULL for a non-empty source shard
+    dsts = (ctypes.c_void_p * 4)(0x2000, 0x3000, 0x4000, 0x5000)
+    assert rs._lib.reshard_execute(p, srcs, dsts, None) == 1
+    assert "source" in rs.reshard_last_error()
+    assert rs._lib.reshard_execute(p, None, dsts, None) == 1
+    assert rs._lib.reshard_execute_ex(p, srcs, dsts, 7, None) == 1
+    full = 0x9000
+    assert rs._lib.gather_broadcast_execute(p, srcs, dsts, full, 64, None) == 1  # scratch < G
+    assert rs._lib.gather_broadcast_execute(p, srcs, dsts, None, 1 << 20, None) == 1
+
+
+def test_too_many_ranks_for_execution_is_unsupported():
+    p = rs.reshard_plan_create((4096,), "fp32", (1024,), ("S0",), (4,), ("S0",))
+    srcs = (ctypes.c_void_p * 1024)(*([0x1000] * 1024))
+    dsts = (ctypes.c_void_p * 4)(*([0x2000] * 4))
+    assert rs._lib.reshard_execute(p, srcs, dsts, None) == 2
+
+
+def test_local_shape_matches_oracle(oracle):
+    for cfg in (1, 2, 3, 5):
+        for spec in workload(cfg).tensors[:4]:
+            p = rs.reshard_plan_create(spec.global_shape, spec.dtype, spec.src_mesh,
+                                       spec.src_placements, spec.dst_mesh, spec.dst_placements)
+            for side, mesh, pl in ((0, spec.src_mesh, spec.src_placements),
+                                   (1, spec.dst_mesh, spec.dst_placements)):
+                for r in range(math.prod(mesh)):
+                    shp, off = rs.reshard_plan_local_shape(p, side, r)
+                    assert (off, shp) == oracle.resolve(spec.global_shape, mesh, pl, r)
+            with pytest.raises(rs.ReshardError):
+                rs.reshard_plan_local_shape(p, 2, 0)
+            with pytest.raises(rs.ReshardError):
+                rs.reshard_plan_local_shape(p, 0, spec.n_src)
+
+
+def test_stats_of_the_large_workloads():
+    """Byte accounting at the full sizes (planning only, no device memory)."""
+    w = workload(3)
+    G = sum(t.global_bytes for t in w.tensors)
+    D = 0
+    for spec in w.tensors:
+        s = rs.reshard_plan_stats(rs.reshard_plan_create(
+            spec.global_shape, spec.dtype, spec.src_mesh, spec.src_placements, spec.dst_mesh,
+            spec.dst_placements))
+        assert s["region_bytes"] == s["global_bytes"] == spec.global_bytes
+        assert s["fanout_read_bytes"] == spec.global_bytes
+        assert s["fanout_write_bytes"] == s["dst_bytes"] == 4 * spec.global_bytes
+        assert s["boxcopy_read_bytes"] == s["boxcopy_write_bytes"] == s["dst_bytes"]
+        assert s["gb_read_bytes"] == s["gb_write_bytes"] == s["global_bytes"] + s["dst_bytes"]
+        assert s["max_fanout"] == 4 and s["n_regions"] == 8
+        D += s["dst_bytes"]
+    assert G == 11_274_289_152 and D == 4 * G  # 24 x 28672 x 8192 x 2 bytes
+
+
+def test_version_string():
+    assert "sm_103a" in rs.reshard_version()

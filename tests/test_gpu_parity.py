@@ -1,0 +1,284 @@
+"""GPU parity: the CUDA path against the CPU oracle, bit for bit (needs a GB300).
+
+Every call goes through the C ABI (via the ctypes binding).  Destination
+buffers sit between guard bands that must come back untouched.  Sizes the
+oracle finishes in seconds are compared in full; the full-size workloads are
+compared on oracle-sampled elements and, in full, against the slices of the
+global tensor given by the oracle's boxes.
+"""
+import math
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import dtensor_reshard_gb300 as rs
+from inputs import TensorSpec, global_tensor, workload
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 512
+GUARD_BYTE = 0x5C
+FILL_BYTE = 0xA5
+
+
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    return torch.device("cuda:0")
+
+
+class Guarded:
+    """A device byte buffer with guard bands; ``ptr`` is the payload's address."""
+
+    def __init__(self, nbytes, misalign=0, fill=FILL_BYTE):
+        self.n = int(nbytes)
+        self.lead = GUARD + misalign
+        self.buf = torch.full((self.lead + self.n + GUARD,), GUARD_BYTE, dtype=torch.uint8,
+                              device="cuda")
+        if self.n:
+            self.buf[self.lead:self.lead + self.n].fill_(fill)
+        self.ptr = self.buf.data_ptr() + self.lead if self.n else None
+
+    def payload(self):
+        return self.buf[self.lead:self.lead + self.n]
+
+    def guards_intact(self):
+        head = self.buf[:self.lead]
+        tail = self.buf[self.lead + self.n:]
+        return bool((head == GUARD_BYTE).all()) and bool((tail == GUARD_BYTE).all())
+
+
+def _upload(arrs, misalign=0):
+    out = []
+    for a in arrs:
+        g = Guarded(a.size, misalign)
+        if a.size:
+            g.payload().copy_(torch.from_numpy(a).cuda())
+        out.append(g)
+    return out
+
+
+def run_and_compare(oracle, spec, kernel=rs.KERNEL_FANOUT, misalign=0, stream=None,
+                    path="reshard"):
+    _cuda()
+    glob = global_tensor(spec)
+    srcs = [helpers.to_bytes(s) for s in helpers.scatter_with_oracle(
+        oracle, glob, spec.src_mesh, spec.src_placements)]
+    want = helpers.expected_dst(oracle, spec, srcs)
+    dsrc = _upload(srcs, misalign)
+    ddst = [Guarded(w.size, misalign) for w in want]
+    plan = helpers.spec_plan(spec)
+    sptr = [g.ptr for g in dsrc]
+    dptr = [g.ptr for g in ddst]
+    scratch = None
+    if path == "reshard":
+        rs.reshard_execute_ex(plan, sptr, dptr, kernel, stream)
+    else:
+        scratch = Guarded(spec.global_bytes, misalign)
+        rs.gather_broadcast_execute(plan, sptr, dptr, scratch.ptr, spec.global_bytes, stream)
+    torch.cuda.synchronize()
+    for r, (g, w) in enumerate(zip(ddst, want)):
+        got = g.payload().cpu().numpy()
+        if not np.array_equal(got, w):
+            bad = np.flatnonzero(got != w)
+            raise AssertionError(f"{spec.name} dst rank {r}: {bad.size} bytes differ, "
+                                 f"first at {bad[0]} (kernel {kernel}, path {path})")
+        assert g.guards_intact(), f"guard band overwritten at dst rank {r}"
+    for r, g in enumerate(dsrc):
+        assert g.payload().cpu().numpy().tobytes() == srcs[r].tobytes(), "source modified"
+        assert g.guards_intact()
+    if scratch is not None:
+        assert np.array_equal(scratch.payload().cpu().numpy(), helpers.to_bytes(glob))
+        assert scratch.guards_intact()
+
+
+# ---------------------------------------------------------------------- reduced workloads
+@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+@pytest.mark.parametrize("kernel", [rs.KERNEL_FANOUT, rs.KERNEL_BOXCOPY])
+def test_reduced_workloads(oracle, cfg, kernel):
+    for spec in workload(cfg, reduced=True).tensors:
+        run_and_compare(oracle, spec, kernel=kernel)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+def test_reduced_workloads_gather_broadcast(oracle, cfg):
+    for spec in workload(cfg, reduced=True).tensors:
+        run_and_compare(oracle, spec, path="gather_broadcast")
+
+
+def test_uneven_stress_reduced(oracle):
+    for spec in workload(4, reduced=True).tensors:
+        run_and_compare(oracle, spec)
+        run_and_compare(oracle, spec, kernel=rs.KERNEL_BOXCOPY)
+
+
+def test_worked_example_blocks(oracle):
+    """Each destination of the 8x8 example holds rows 0-3 of source 0 and rows 4-7 of
+    source 1 at columns 2j..2j+1 (two 4x2 blocks)."""
+    spec = workload(1).tensors[0]
+    run_and_compare(oracle, spec)
+    glob = global_tensor(spec).cuda()
+    srcs = [glob[:4].contiguous(), glob[4:].contiguous()]
+    dsts = [torch.empty(8, 2, dtype=glob.dtype, device="cuda") for _ in range(4)]
+    plan = helpers.spec_plan(spec)
+    rs.reshard_execute(plan, srcs, dsts)
+    torch.cuda.synchronize()
+    for j in range(4):
+        assert torch.equal(dsts[j][:4], srcs[0][:, 2 * j:2 * j + 2])
+        assert torch.equal(dsts[j][4:], srcs[1][:, 2 * j:2 * j + 2])
+
+
+# ---------------------------------------------------------------------- edge cases
+def _spec(gshape, dtype, sm, sp, dm, dp, seed=0):
+    return TensorSpec("edge", tuple(gshape), dtype, tuple(sm), tuple(sp), tuple(dm), tuple(dp),
+                      init=("bits",), seed=seed)
+
+
+EDGE = [
+    _spec((0, 7), "bf16", (2,), ("S0",), (3,), ("S1",)),              # empty tensor
+    _spec((3,), "fp32", (8,), ("S0",), (5,), ("S0",)),                # more ranks than elements
+    _spec((1,), "u8", (1,), ("R",), (4,), ("R",)),                    # one byte, fan-out 4
+    _spec((5, 3), "bf16", (4,), ("S0",), (2, 2), ("S1", "S0")),       # ragged + empty shards
+    _spec((1000, 37), "bf16", (3,), ("S1",), (7,), ("S0",)),          # odd bf16 rows
+    _spec((4097, 3), "u8", (5,), ("S0",), (2,), ("S1",)),             # 1-byte rows
+    _spec((37, 11, 13), "fp16", (2, 3), ("S2", "S1"), (3, 2), ("S1", "S2")),  # 3-D planes
+    _spec((3, 5, 7, 9), "fp64", (2,), ("S3",), (2, 2), ("S1", "S3")),  # 4-D
+    _spec((64, 4096), "bf16", (2,), ("S0",), (64,), ("R",)),          # fan-out 64
+    _spec((300, 1000), "bf16", (1,), ("R",), (300,), ("R",)),         # fan-out 300 > group max
+    _spec((512,), "fp32", (510,), ("S0",), (513,), ("S0",)),          # M + N + 1 = 1024
+    _spec((2, 70000), "bf16", (2,), ("S1",), (2,), ("S0",)),          # 70 KB runs inside rows
+    _spec((16, 3, 100000), "fp32", (2, 2), ("S0", "S2"), (4,), ("S2",)),  # long rows, planes
+]
+
+
+@pytest.mark.parametrize("i", range(len(EDGE)))
+def test_edge_cases(oracle, i):
+    spec = EDGE[i]
+    run_and_compare(oracle, spec)
+    run_and_compare(oracle, spec, kernel=rs.KERNEL_BOXCOPY)
+    if spec.global_bytes:
+        run_and_compare(oracle, spec, path="gather_broadcast")
+
+
+@pytest.mark.parametrize("misalign", [1, 2, 4, 8])
+def test_misaligned_buffers(oracle, misalign):
+    """Base pointers off the 16-byte grid take the narrower vector paths."""
+    for spec in (workload(2, reduced=True).tensors[0], EDGE[4], EDGE[6]):
+        run_and_compare(oracle, spec, misalign=misalign)
+
+
+def test_nan_payloads_and_negative_zero_survive(oracle):
+    spec = _spec((257, 129), "fp32", (2, 2), ("S0", "R"), (3,), ("S1",), seed=77)
+    run_and_compare(oracle, spec)
+
+
+def test_runs_on_a_side_stream(oracle):
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run_and_compare(oracle, workload(2, reduced=True).tensors[0], stream=s)
+
+
+def test_repeated_execution_is_stable(oracle):
+    spec = workload(3, reduced=True).tensors[0]
+    for _ in range(3):
+        run_and_compare(oracle, spec)
+
+
+def test_execute_after_destroy_is_rejected():
+    _cuda()
+    plan = rs.reshard_plan_create((8, 8), "bf16", (2,), ("S0",), (4,), ("S1",))
+    h = plan.handle
+    rs.reshard_plan_destroy(plan)
+    import ctypes
+    assert rs._lib.reshard_execute(ctypes.c_void_p(h), None, None, None) == 6
+
+
+def test_replan_after_rank_removal(oracle):
+    """Membership change = destroy + re-create with the shrunken mesh (planned on the host)."""
+    spec = workload(2, reduced=True).tensors[0]
+    run_and_compare(oracle, spec)
+    shrunk = TensorSpec(spec.name, spec.global_shape, spec.dtype, spec.src_mesh,
+                        spec.src_placements, (3, 2), spec.dst_placements, init=spec.init,
+                        seed=spec.seed)
+    run_and_compare(oracle, shrunk)
+
+
+# ---------------------------------------------------------------------- full sizes
+def _full_size_check(oracle, spec, samples=4000, kernel=rs.KERNEL_FANOUT, seed=0):
+    """Full-size run: every destination shard equals the global tensor cut by the oracle's
+    box, and oracle_source_of agrees on sampled elements."""
+    dev = _cuda()
+    glob = global_tensor(spec, device=dev)
+    src_boxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+    dst_boxes = oracle.boxes(spec.global_shape, spec.dst_mesh, spec.dst_placements)
+    srcs = [helpers.slice_box(glob, o, s) for o, s in src_boxes]
+    dsts = [torch.empty(s, dtype=glob.dtype, device=dev) for _, s in dst_boxes]
+    for d in dsts:
+        if d.numel():
+            d.view(-1).view(torch.uint8).fill_(FILL_BYTE)
+    plan = helpers.spec_plan(spec)
+    rs.reshard_execute_ex(plan, srcs, dsts, kernel)
+    torch.cuda.synchronize()
+    for r, (o, s) in enumerate(dst_boxes):
+        if math.prod(s):
+            want = helpers.slice_box(glob, o, s)
+            assert torch.equal(dsts[r].reshape(-1).view(torch.uint8),
+                               want.reshape(-1).view(torch.uint8)), (spec.name, r)
+    del glob
+    rng = random.Random(seed)
+    nonempty = [r for r, (_, s) in enumerate(dst_boxes) if math.prod(s)]
+    ivt = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}[spec.elem_bytes]
+    by_rank = {}
+    for _ in range(samples if nonempty else 0):
+        r = rng.choice(nonempty)
+        e = rng.randrange(math.prod(dst_boxes[r][1]))
+        s, j = oracle.source_of(spec.global_shape, spec.src_mesh, spec.src_placements,
+                                spec.dst_mesh, spec.dst_placements, r, e)
+        by_rank.setdefault((r, s), []).append((e, j))
+    for (r, s), pairs in by_rank.items():
+        e = torch.tensor([p[0] for p in pairs], device=dev)
+        j = torch.tensor([p[1] for p in pairs], device=dev)
+        got = dsts[r].reshape(-1).view(ivt)[e]
+        want = srcs[s].reshape(-1).view(ivt)[j]
+        assert torch.equal(got, want), (spec.name, r, s)
+
+
+def test_full_ffn_up_against_full_oracle(oracle):
+    """Dense FFN up-projection at its full size, compared byte for byte with the oracle."""
+    spec = workload(2).tensors[0]
+    run_and_compare(oracle, spec)
+
+
+@pytest.mark.parametrize("idx", [0, 2])
+def test_full_hybridflow_layer(oracle, idx):
+    _full_size_check(oracle, workload(3).tensors[idx])
+
+
+@pytest.mark.parametrize("idx", [0, 2, 3, 4])
+def test_full_moe_refit(oracle, idx):
+    spec = workload(5).tensors[idx]
+    if spec.path == "gather_broadcast":
+        dev = _cuda()
+        glob = global_tensor(spec, device=dev)
+        src_boxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+        dst_boxes = oracle.boxes(spec.global_shape, spec.dst_mesh, spec.dst_placements)
+        srcs = [helpers.slice_box(glob, o, s) for o, s in src_boxes]
+        dsts = [torch.empty(s, dtype=glob.dtype, device=dev) for _, s in dst_boxes]
+        scratch = torch.empty(spec.global_bytes, dtype=torch.uint8, device=dev)
+        plan = helpers.spec_plan(spec)
+        rs.gather_broadcast_execute(plan, srcs, dsts, scratch, spec.global_bytes)
+        torch.cuda.synchronize()
+        assert torch.equal(scratch, glob.reshape(-1).view(torch.uint8))
+        for r, (o, s) in enumerate(dst_boxes):
+            assert torch.equal(dsts[r].reshape(-1).view(torch.uint8),
+                               helpers.slice_box(glob, o, s).reshape(-1).view(torch.uint8))
+    else:
+        _full_size_check(oracle, spec)
+
+
+def test_full_uneven_stress_sampled(oracle):
+    for spec in workload(4).tensors:
+        _full_size_check(oracle, spec, samples=300)

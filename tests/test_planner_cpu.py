@@ -1,0 +1,192 @@
+"""The planner's copy programs, executed on the CPU by a test-only tile executor and
+compared with the oracle; invariants of the tiles and of the replica choice."""
+import math
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import dtensor_reshard_gb300 as rs
+from inputs import TensorSpec, global_tensor, workload
+from tests import helpers
+from tests import torch_chunk_layout as tcl
+
+
+def _case(gshape, dtype, sm, sp, dm, dp, seed):
+    return TensorSpec("case", tuple(gshape), dtype, tuple(sm), tuple(sp), tuple(dm), tuple(dp),
+                      init=("bits",), seed=seed)
+
+
+def _check_spec(oracle, spec, programs=(0, 1)):
+    glob = global_tensor(spec)
+    srcs = [helpers.to_bytes(s) for s in helpers.scatter_with_oracle(
+        oracle, glob, spec.src_mesh, spec.src_placements)]
+    want = helpers.expected_dst(oracle, spec, srcs)
+    plan = helpers.spec_plan(spec)
+    for program in programs:
+        dsts = [np.full(w.size, 0xA5, dtype=np.uint8) for w in want]
+        bufs = [s.copy() for s in srcs] + dsts + [np.zeros(0, dtype=np.uint8)]
+        writes = helpers.run_program_cpu(plan, program, bufs)
+        M = spec.n_src
+        for r, w in enumerate(want):
+            assert np.array_equal(bufs[M + r], w), (spec, program, r)
+            assert (writes[M + r] == 1).all(), ("each dst byte written exactly once", spec, r)
+        for s in range(M):
+            assert not writes[s].any(), "sources must not be written"
+    # gather-and-broadcast: gather covers the full tensor once, slice fills every dst
+    G = spec.global_bytes
+    dsts = [np.full(w.size, 0x5A, dtype=np.uint8) for w in want]
+    bufs = [s.copy() for s in srcs] + dsts + [np.zeros(G, dtype=np.uint8)]
+    wg = helpers.run_program_cpu(plan, rs.PROGRAM_GATHER, bufs)
+    assert (wg[-1] == 1).all()
+    assert np.array_equal(bufs[-1], helpers.to_bytes(glob))
+    ws = helpers.run_program_cpu(plan, rs.PROGRAM_SLICE, bufs)
+    for r, w in enumerate(want):
+        assert np.array_equal(bufs[spec.n_src + r], w)
+        assert (ws[spec.n_src + r] == 1).all()
+    return plan
+
+
+def test_worked_example_programs(oracle):
+    _check_spec(oracle, workload(1).tensors[0])
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 5])
+def test_reduced_workloads(oracle, cfg):
+    w = workload(cfg, reduced=True)
+    for spec in w.tensors[:4]:
+        _check_spec(oracle, spec)
+
+
+def test_uneven_stress_reduced(oracle):
+    for spec in workload(4, reduced=True).tensors:
+        _check_spec(oracle, spec)
+
+
+def test_bruteforce_small_layouts(oracle):
+    rng = random.Random(17)
+    layouts = {nd: [(m, p) for m in tcl.all_meshes(4) for p in tcl.all_placements(len(m), nd)]
+               for nd in (1, 2, 3)}
+    for i in range(400):
+        nd = rng.choice((1, 2, 3))
+        gshape = tuple(rng.randint(0 if rng.random() < 0.05 else 1, 7) for _ in range(nd))
+        (sm, sp), (dm, dp) = rng.choice(layouts[nd]), rng.choice(layouts[nd])
+        dtype = rng.choice(("u8", "bf16", "fp32", "fp64"))
+        _check_spec(oracle, _case(gshape, dtype, sm, sp, dm, dp, seed=i))
+
+
+def test_four_dim_tensors(oracle):
+    rng = random.Random(5)
+    for i in range(40):
+        gshape = tuple(rng.randint(1, 5) for _ in range(4))
+        sm = tuple(rng.randint(1, 3) for _ in range(rng.randint(1, 3)))
+        dm = tuple(rng.randint(1, 3) for _ in range(rng.randint(1, 3)))
+        sp = tuple(rng.choice(["R", "S0", "S1", "S2", "S3"]) for _ in sm)
+        dp = tuple(rng.choice(["R", "S0", "S1", "S2", "S3"]) for _ in dm)
+        _check_spec(oracle, _case(gshape, "fp16", sm, sp, dm, dp, seed=100 + i))
+
+
+def test_unit_prefix_matches_tile_units():
+    spec = workload(5, reduced=True).tensors[2]
+    plan = helpers.spec_plan(spec)
+    for program in range(4):
+        tiles, prefix, _, _ = rs.reshard_plan_program(plan, program)
+        assert prefix[0] == 0
+        for i, t in enumerate(tiles):
+            assert prefix[i + 1] - prefix[i] == rs.reshard_tile_units(t) > 0
+
+
+def test_tiles_sorted_by_destination():
+    spec = workload(5, reduced=True).tensors[0]
+    plan = helpers.spec_plan(spec)
+    tiles, _, goff, gbuf = rs.reshard_plan_program(plan, rs.PROGRAM_FANOUT)
+    keys = [(gbuf[goff[t["dst_group"]]], t["dst_off"]) for t in tiles]
+    assert keys == sorted(keys)
+
+
+def test_replica_load_balance():
+    """Greedy largest-first: within a source class, replica loads differ by at most one region."""
+    rng = random.Random(9)
+    checked = 0
+    for i in range(300):
+        nd = rng.choice((1, 2))
+        gshape = tuple(rng.randint(1, 40) for _ in range(nd))
+        sm = (rng.randint(2, 4), rng.randint(1, 4))
+        sp = ("R", f"S{rng.randrange(nd)}")
+        dm = (rng.randint(1, 8),)
+        dp = (f"S{rng.randrange(nd)}",)
+        plan = rs.reshard_plan_create(gshape, "bf16", sm, sp, dm, dp)
+        tiles, _, goff, _ = rs.reshard_plan_program(plan, rs.PROGRAM_FANOUT)
+        load = {}
+        for t in tiles:
+            b = t["row_bytes"] * t["nrows"] * t["nplanes"]
+            load[t["src_buf"]] = load.get(t["src_buf"], 0) + b
+        # group source ranks by their box (replicas)
+        classes = {}
+        for r in range(math.prod(sm)):
+            shp, off = rs.reshard_plan_local_shape(plan, 0, r)
+            classes.setdefault((shp, off), []).append(r)
+        # largest region = largest source box x destination box intersection
+        biggest = 0
+        for r in range(math.prod(dm)):
+            dshp, doff = rs.reshard_plan_local_shape(plan, 1, r)
+            for (sshp, soff) in classes:
+                v = 2
+                for a, b, c, d in zip(soff, sshp, doff, dshp):
+                    v *= max(0, min(a + b, c + d) - max(a, c))
+                biggest = max(biggest, v)
+        for ranks in classes.values():
+            if len(ranks) < 2:
+                continue
+            loads = [load.get(r, 0) for r in ranks]
+            assert max(loads) - min(loads) <= biggest, (gshape, sm, sp, dm, dp, loads)
+            checked += 1
+    assert checked > 100
+
+
+def test_fanout_groups_hybridflow():
+    """Training TP8 -> (TP2, DP4): each region is one fan-out record to 4 replicas."""
+    spec = workload(3).tensors[0]
+    plan = helpers.spec_plan(spec)
+    tiles, _, goff, gbuf = rs.reshard_plan_program(plan, rs.PROGRAM_FANOUT)
+    sizes = {goff[g + 1] - goff[g] for g in range(len(goff) - 1)}
+    assert sizes == {4}
+    st = rs.reshard_plan_stats(plan)
+    assert st["fanout_read_bytes"] == spec.global_bytes
+    assert st["fanout_write_bytes"] == 4 * spec.global_bytes
+    # every region is one contiguous 58.7 MB run, cut into run tiles
+    assert all(t["nrows"] == 1 and t["nplanes"] == 1 for t in tiles)
+    assert sum(t["row_bytes"] for t in tiles) == spec.global_bytes
+
+
+def test_moe_down_is_strided_rows():
+    """Down projection [E, 7168, 2048] Shard(ffn): 512-byte rows at a 2 KiB source stride."""
+    spec = workload(5).tensors[2]
+    plan = helpers.spec_plan(spec)
+    tiles, _, goff, _ = rs.reshard_plan_program(plan, rs.PROGRAM_FANOUT)
+    assert all(t["row_bytes"] == 512 and t["src_row_stride"] == 2048
+               and t["dst_row_stride"] == 512 for t in tiles)
+    assert {goff[g + 1] - goff[g] for g in range(len(goff) - 1)} == {2}
+
+
+def test_planner_scale_pages_layout():
+    """The pages' TP4 x PP8 x EP16 -> TP8 x DP16 layout (512 -> 128 ranks), planning only."""
+    gshape = (128, 2048, 7168)
+    plan = rs.reshard_plan_create(gshape, "bf16", (4, 8, 16), ("S1", "R", "S0"), (8, 16),
+                                  ("S1", "R"))
+    st = rs.reshard_plan_stats(plan)
+    G = math.prod(gshape) * 2
+    assert st["region_bytes"] == G
+    assert st["dst_bytes"] == 16 * G
+    assert st["n_src_ranks"] == 512 and st["n_dst_ranks"] == 128
+    assert st["planner_ns"] < 2e9
+
+
+def test_empty_and_degenerate_layouts(oracle):
+    # zero-size tensor, more ranks than elements, size-1 meshes
+    for spec in (_case((0, 5), "bf16", (2,), ("S0",), (3,), ("S1",), 1),
+                 _case((3,), "fp32", (8,), ("S0",), (5,), ("S0",), 2),
+                 _case((5, 1), "bf16", (1, 1), ("R", "S1"), (1,), ("R",), 3),
+                 _case((1, 1, 1), "u8", (2, 2), ("S0", "S2"), (3,), ("S1",), 4)):
+        _check_spec(oracle, spec)
