@@ -51,6 +51,10 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=("moe_refit", "hybridflow", "ffn_up"),
                     default="moe_refit")
     ap.add_argument("--kernel", choices=("fanout", "boxcopy"), default="fanout")
+    ap.add_argument("--reshard-only", action="store_true",
+                    help="leave out the gather-and-broadcast tensors (profiling captures)")
+    ap.add_argument("--experts", type=int, default=256,
+                    help="experts of the MoE workload (smaller for profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -217,12 +221,17 @@ def launches_of(job, kernel):
 
 
 # ------------------------------------------------------------------------------ CPU oracle
+_HOST_SRC = {}
+
+
 def oracle_sample(jobs, seconds):
     """Time the CPU oracle on a bounded sample of the workload's reshard tensors.
 
-    Sample: for every reshard tensor, destination rank 0, its first k slices along
-    the outermost dim (k grown until about ``seconds`` of CPU time in total).
-    Returns (effective GB/s, sample description, cores used).
+    Sample: for every reshard tensor, destination rank 0, consecutive slices of its
+    outermost dim from the start, processed a few slices at a time until the tensor's
+    share of ``seconds`` of CPU time is spent.  Only the source shards a chunk touches
+    are copied to the host (outside the timed calls).
+    Returns (effective GB/s, sample description, cores used, CPU seconds).
     """
     import numpy as np
     import torch
@@ -233,47 +242,47 @@ def oracle_sample(jobs, seconds):
     rjobs = [j for j in jobs if j.spec.path == "reshard"]
     if not rjobs:
         return None
-
-    def sample(job, k):
-        spec = job.spec
-        doff, dshp = o.resolve(spec.global_shape, spec.dst_mesh, spec.dst_placements, 0)
-        k = min(k, dshp[0])
-        per = math.prod(dshp[1:])
-        # global box of the sample -> source shards it touches (host copies of those only)
-        lo = list(doff)
-        hi = [a + b for a, b in zip(doff, dshp)]
-        hi[0] = doff[0] + k
-        ptrs, keep = [], []
-        for s, (so, ss) in enumerate(o.boxes(spec.global_shape, spec.src_mesh,
-                                             spec.src_placements)):
-            touch = all(max(a, c) < min(b, c + d) for a, b, c, d in zip(lo, hi, so, ss))
-            if touch and math.prod(ss):
-                h = job.srcs[s].reshape(-1).view(torch.uint8).cpu().numpy()
-                keep.append(h)
-                ptrs.append(h.ctypes.data)
-            else:
-                ptrs.append(None)
-        out = np.empty(math.prod(dshp) * spec.elem_bytes if k == dshp[0] else
-                       k * per * spec.elem_bytes, dtype=np.uint8)
-        n = k * per
-        t0 = time.perf_counter()
-        o.reshard_elems(spec.global_shape, spec.elem_bytes, spec.src_mesh, spec.src_placements,
-                        spec.dst_mesh, spec.dst_placements, ptrs, out.ctypes.data, 0, 0, n)
-        dt = time.perf_counter() - t0
-        st = job.stats
-        eff = n * spec.elem_bytes * (1.0 + st["global_bytes"] / st["dst_bytes"])
-        return dt, eff, n, k
-
-    # calibrate on one slice of the first tensor, then size k per tensor
-    dt1, _, _, _ = sample(rjobs[0], 1)
-    per_tensor = seconds / len(rjobs)
-    k = max(1, int(per_tensor / max(dt1, 1e-4)))
+    budget = seconds / len(rjobs)
     tot_t, tot_b, desc = 0.0, 0.0, []
     for j in rjobs:
-        dt, eff, n, kk = sample(j, k)
-        tot_t += dt
-        tot_b += eff
-        desc.append(f"{j.spec.name}: dst rank 0, first {kk} of dim 0 ({n} elements)")
+        spec = j.spec
+        doff, dshp = o.resolve(spec.global_shape, spec.dst_mesh, spec.dst_placements, 0)
+        if math.prod(dshp) == 0:
+            continue
+        per = math.prod(dshp[1:])
+        chunk = max(1, (4 << 20) // max(1, per))
+        sboxes = o.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+        out = np.empty(math.prod(dshp) * spec.elem_bytes, dtype=np.uint8)
+        t_spent, done, n = 0.0, 0, 0
+        while t_spent < budget and done < dshp[0]:
+            k = min(chunk, dshp[0] - done)
+            lo = list(doff)
+            hi = [a + b for a, b in zip(doff, dshp)]
+            lo[0], hi[0] = doff[0] + done, doff[0] + done + k
+            ptrs = []
+            for s, (so, ss) in enumerate(sboxes):
+                touch = math.prod(ss) and all(
+                    max(a, c) < min(b, c + d) for a, b, c, d in zip(lo, hi, so, ss))
+                if touch:
+                    key = (id(j), s)
+                    if key not in _HOST_SRC:
+                        _HOST_SRC[key] = j.srcs[s].reshape(-1).view(torch.uint8).cpu().numpy()
+                    ptrs.append(_HOST_SRC[key].ctypes.data)
+                else:
+                    ptrs.append(None)
+            t0 = time.perf_counter()
+            o.reshard_elems(spec.global_shape, spec.elem_bytes, spec.src_mesh,
+                            spec.src_placements, spec.dst_mesh, spec.dst_placements, ptrs,
+                            out.ctypes.data, 0, done * per, (done + k) * per)
+            t_spent += time.perf_counter() - t0
+            n += k * per
+            done += k
+        st = j.stats
+        tot_t += t_spent
+        tot_b += n * spec.elem_bytes * (1.0 + st["global_bytes"] / st["dst_bytes"])
+        desc.append(f"{spec.name}: dst rank 0, first {done} of dim 0 ({n} elements)")
+    if tot_t == 0:
+        return None
     return tot_b / tot_t / 1e9, "; ".join(desc), 1, tot_t
 
 
@@ -384,9 +393,11 @@ class DistCtx:
         return x if self.world == 1 else self._reduce(x, self.dist.ReduceOp.SUM)
 
 
-def pick_workload(name):
+def pick_workload(name, experts=256):
     from inputs import ffn_up, hybridflow, moe_refit
-    return {"moe_refit": moe_refit, "hybridflow": hybridflow, "ffn_up": ffn_up}[name]()
+    if name == "moe_refit":
+        return moe_refit(experts=experts)
+    return {"hybridflow": hybridflow, "ffn_up": ffn_up}[name]()
 
 
 # ------------------------------------------------------------------------------ arms
@@ -396,7 +407,7 @@ def reference_arm(args, rank, world):
         return 0
     import torch
     dev = torch.device("cuda:0") if torch.cuda.is_available() else None
-    w = pick_workload(args.workload)
+    w = pick_workload(args.workload, args.experts)
     if dev is None:
         print(json.dumps({"impl": "reference", "unavailable": "no CUDA device to build inputs"}))
         return 0
@@ -441,9 +452,9 @@ def ours_arm(args, rank, world, local):
     if gpu_uuid and not gpu_uuid.startswith("GPU-") and len(gpu_uuid) > 8:
         gpu_uuid = "GPU-" + gpu_uuid
     kernel = rs.KERNEL_FANOUT if args.kernel == "fanout" else rs.KERNEL_BOXCOPY
-    w = pick_workload(args.workload)
+    w = pick_workload(args.workload, args.experts)
     t0 = time.perf_counter()
-    jobs = build_jobs(w, dev)
+    jobs = build_jobs(w, dev, with_gb=not args.reshard_only)
     setup_s = time.perf_counter() - t0
     stream = torch.cuda.current_stream(dev)
 
@@ -500,8 +511,8 @@ def ours_arm(args, rank, world, local):
         "config": {
             "workload": w.name, "tensors": len(jobs),
             "reshard_kernel": args.kernel,
-            "step": "3 expert tensors via reshard_execute + 9 attention/norm tensors via "
-                    "gather_broadcast_execute" if args.workload == "moe_refit" else "reshard",
+            "step": "%d tensors via reshard_execute + %d via gather_broadcast_execute" % (
+                len(dom_jobs), len(jobs) - len(dom_jobs)),
             "global_bytes_per_step": st_tot["global_bytes"],
             "dst_bytes_per_step": st_tot["dst_bytes"],
             "l2": "inputs larger than L2 (sources %.1f GB per step), no flush" % (
