@@ -102,6 +102,7 @@ def _load():
         "reshard_execute": ([vp, vpp, vpp, vp], ctypes.c_int),
         "reshard_execute_ex": ([vp, vpp, vpp, ctypes.c_int32, vp], ctypes.c_int),
         "gather_broadcast_execute": ([vp, vpp, vpp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "gather_broadcast_execute_static": ([vp, vpp, vpp, vp], ctypes.c_int),
         "reshard_plan_local_shape": ([vp, ctypes.c_int32, ctypes.c_int64, i64p, i64p],
                                      ctypes.c_int),
         "reshard_plan_stats": ([vp, ctypes.POINTER(reshard_stats_t)], ctypes.c_int),
@@ -256,6 +257,18 @@ def gather_broadcast_execute(plan: Plan, src_ptrs, dst_ptrs, full_scratch, scrat
     _check(_lib.gather_broadcast_execute(plan, _ptr_array(src_ptrs), _ptr_array(dst_ptrs),
                                          _ptr(full_scratch), int(scratch_bytes), _stream(stream)),
            "gather_broadcast_execute")
+
+
+def gather_broadcast_execute_static(plan: Plan, src_ptrs, dst_ptrs, stream=None):
+    """gather_broadcast_execute with the library's static device scratch (no allocation;
+    see include/reshard.h for the size limits and the sharing rules)."""
+    _check(_lib.gather_broadcast_execute_static(plan, _ptr_array(src_ptrs), _ptr_array(dst_ptrs),
+                                                _stream(stream)),
+           "gather_broadcast_execute_static")
+
+
+STATIC_SCRATCH_BYTES = 64 << 20
+STATIC_TABLE_BYTES = 1 << 20
 
 
 def reshard_plan_local_shape(plan: Plan, side: int, rank: int):

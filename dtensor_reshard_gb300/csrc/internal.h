@@ -86,6 +86,11 @@ reshard_status_t fail(reshard_status_t st, const std::string& msg);
 // bufs[nbufs] on `stream`.  Returns OK when there is nothing to do.
 reshard_status_t launch_program(const reshard_plan_s* plan, const Program& p,
                                 unsigned char* const* bufs, int nbufs, void* stream);
+// Same, with the program's tables at explicit device addresses (no uploaded plan).
+reshard_status_t launch_program_tables(const Program& p, const reshard_tile_t* d_tiles,
+                                       const int64_t* d_prefix, const uint32_t* d_goff,
+                                       const uint16_t* d_gbuf, int num_sms,
+                                       unsigned char* const* bufs, int nbufs, void* stream);
 // Occupancy of the copy kernel on the current device (blocks per SM).
 reshard_status_t copy_kernel_occupancy(int* blocks_per_sm);
 

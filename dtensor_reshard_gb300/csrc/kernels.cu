@@ -297,4 +297,49 @@ reshard_status_t launch_program(const reshard_plan_s* plan, const Program& prog,
   return RESHARD_OK;
 }
 
+
+// Launch one program whose tables live at caller-given device addresses (the
+// allocation-free entry point keeps them in a static device array).  Same kernel
+// and grid rule as launch_program; needs no uploaded plan.
+reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t* d_tiles,
+                                       const int64_t* d_prefix, const uint32_t* d_goff,
+                                       const uint16_t* d_gbuf, int num_sms,
+                                       unsigned char* const* bufs, int nbufs, void* stream) {
+  const int64_t total = prog.total_units();
+  if (total == 0) return RESHARD_OK;
+  if (nbufs > RESHARD_MAX_EXEC_BUFFERS) return fail(RESHARD_ERR_UNSUPPORTED, "too many buffers");
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess)
+    return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
+  uint64_t align = prog.align_bits;
+  for (int i = 0; i < nbufs; ++i) align |= reinterpret_cast<uint64_t>(bufs[i]);
+  int w_log2 = 4;
+  while (w_log2 > 0 && (align & ((uint64_t(1) << w_log2) - 1)) != 0) --w_log2;
+  const int planes = prog.has_planes ? 1 : 0;
+  int bps = 1;
+  reshard_status_t st = occupancy(dev, w_log2, planes, &bps);
+  if (st != RESHARD_OK) return st;
+
+  KernelParams kp;
+  kp.tiles = d_tiles;
+  kp.prefix = d_prefix;
+  kp.goff = d_goff;
+  kp.gbuf = d_gbuf;
+  kp.total_units = total;
+  kp.ntiles = int32_t(prog.tiles.size());
+  kp.nbufs = nbufs;
+  for (int i = 0; i < nbufs; ++i) kp.bufs[i] = bufs[i];
+  for (int i = nbufs; i < RESHARD_MAX_EXEC_BUFFERS; ++i) kp.bufs[i] = nullptr;
+
+  const int64_t max_grid = int64_t(num_sms) * bps;
+  const unsigned grid = unsigned(total < max_grid ? total : max_grid);
+  void* args[] = {&kp};
+  ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[w_log2][planes]), dim3(grid),
+                        dim3(kThreads), args, 0, static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess)
+    return fail(RESHARD_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(ce));
+  return RESHARD_OK;
+}
+
 }  // namespace rs

@@ -229,6 +229,50 @@ reshard_status_t gather_broadcast_execute(reshard_plan_t plan, const void* const
                                           void* const* dst_ptrs, void* full_scratch,
                                           size_t scratch_bytes, void* stream);
 
+/* Sizes of the static device arrays used by gather_broadcast_execute_static. */
+#define RESHARD_STATIC_SCRATCH_BYTES (64ull << 20) /* largest global tensor: 64 MiB */
+#define RESHARD_STATIC_TABLE_BYTES (1ull << 20)    /* gather + slice descriptor tables */
+
+/*
+ * gather_broadcast_execute without any allocation.  The write-ups have no
+ * counterpart of this entry point; it exists for callers that cannot call
+ * cudaMalloc: an inference engine whose memory pool has already claimed the
+ * device memory it may use, a caller in a latency-critical path that must not
+ * incur the implicit device synchronisation cudaMalloc/cudaFree can cause, or
+ * code that owns no allocator at all (a plugin handed only its input and output
+ * buffers).  Such callers cannot provide the full-tensor scratch nor the
+ * plan's device tables that the other entry points allocate.
+ *
+ * Instead, the scratch (RESHARD_STATIC_SCRATCH_BYTES) and the descriptor tables
+ * (RESHARD_STATIC_TABLE_BYTES) live in file-scope static device arrays of the
+ * library: every GPU on which the library's device code is loaded holds those
+ * 65 MiB until the process exits.  The caller passes only the source and
+ * destination pointers (as for gather_broadcast_execute) and the stream; the
+ * result is the same.  The plan need not be uploaded.
+ *
+ * The first call on a device looks up the arrays' device addresses
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Each call copies the plan's tables from host memory into
+ * the static array with cudaMemcpyAsync on `stream` (pageable source, so the
+ * call waits until earlier work on `stream` has finished) and then launches the
+ * gather and slice kernels on `stream`.  No part of the arrays needs to start at
+ * zero: the gather writes every byte of the global tensor before the slice reads
+ * it, and the tables are rewritten by every call.
+ *
+ * All calls share the arrays and each call overwrites the previous contents:
+ * calls that can overlap on the GPU (different streams without ordering between
+ * them, or several host threads) race and produce wrong results.  Calls on one
+ * stream are ordered and safe.  No cudaMalloc, cudaFree or other allocating
+ * library routine is called.
+ *
+ * Errors: as gather_broadcast_execute, plus UNSUPPORTED when the global tensor
+ * exceeds RESHARD_STATIC_SCRATCH_BYTES or the gather + slice tables exceed
+ * RESHARD_STATIC_TABLE_BYTES (use gather_broadcast_execute with a caller-owned
+ * scratch then), CUDA when the symbol lookup or the table copy fails.
+ */
+reshard_status_t gather_broadcast_execute_static(reshard_plan_t plan, const void* const* src_ptrs,
+                                                 void* const* dst_ptrs, void* stream);
+
 /*
  * Local box of one rank (news.bpdata.com, section "A megkozelites": the DTensor
  * description fixes each rank's shard).  side 0 = source, 1 = destination.
