@@ -523,7 +523,7 @@ def ours_arm(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic_val, "peak_kind": peak_kind,
-                     "kernel": "reshard_copy_kernel<16,false> (fan-out)",
+                     "kernel": "fanout_staged_kernel (TMA bulk copies, fan-out)",
                      "algorithmic_bytes_per_launch": int(dom_bytes_per_launch),
                      "avg_launch_ms": round(dom_launch_ms, 4)},
         "bytes_vs_gather_broadcast": {

@@ -103,6 +103,8 @@ def _load():
         "reshard_execute_ex": ([vp, vpp, vpp, ctypes.c_int32, vp], ctypes.c_int),
         "gather_broadcast_execute": ([vp, vpp, vpp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "gather_broadcast_execute_static": ([vp, vpp, vpp, vp], ctypes.c_int),
+        "reshard_device_status": ([ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+        "reshard_selftest_wait_timeout": ([ctypes.c_uint32, vp], ctypes.c_int),
         "reshard_plan_local_shape": ([vp, ctypes.c_int32, ctypes.c_int64, i64p, i64p],
                                      ctypes.c_int),
         "reshard_plan_stats": ([vp, ctypes.POINTER(reshard_stats_t)], ctypes.c_int),
@@ -265,6 +267,18 @@ def gather_broadcast_execute_static(plan: Plan, src_ptrs, dst_ptrs, stream=None)
     _check(_lib.gather_broadcast_execute_static(plan, _ptr_array(src_ptrs), _ptr_array(dst_ptrs),
                                                 _stream(stream)),
            "gather_broadcast_execute_static")
+
+
+def reshard_device_status(clear: bool = False) -> int:
+    """Status word of the current device's copy kernels (0 = no wait ever ran out)."""
+    v = ctypes.c_uint32()
+    _check(_lib.reshard_device_status(1 if clear else 0, ctypes.byref(v)), "reshard_device_status")
+    return int(v.value)
+
+
+def reshard_selftest_wait_timeout(polls: int = 4096, stream=None):
+    _check(_lib.reshard_selftest_wait_timeout(int(polls), _stream(stream)),
+           "reshard_selftest_wait_timeout")
 
 
 STATIC_SCRATCH_BYTES = 64 << 20

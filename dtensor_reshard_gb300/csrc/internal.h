@@ -29,6 +29,19 @@ inline int64_t tile_units(const reshard_tile_t& t) {
   return (rows + upr - 1) / upr;
 }
 
+// Parameter block of the copy kernels: the program's device tables and the
+// per-call buffer table (sources, destinations, scratch), passed by value.
+struct KernelParams {
+  const reshard_tile_t* tiles;
+  const int64_t* prefix;
+  const uint32_t* goff;
+  const uint16_t* gbuf;
+  int64_t total_units;
+  int32_t ntiles;
+  int32_t nbufs;
+  unsigned char* bufs[RESHARD_MAX_EXEC_BUFFERS];
+};
+
 struct Box {
   int64_t off[RESHARD_MAX_TENSOR_NDIM];
   int64_t shp[RESHARD_MAX_TENSOR_NDIM];
@@ -57,6 +70,7 @@ struct Program {
   // OR of every tile's offsets, strides and row length (alignment class)
   uint64_t align_bits = 0;
   bool has_planes = false;  // some tile has nplanes > 1
+  bool staged = false;      // eligible for the TMA-staged fan-out kernel when 16-byte aligned
   int64_t total_units() const { return prefix.empty() ? 0 : prefix.back(); }
 };
 
@@ -91,6 +105,9 @@ reshard_status_t launch_program_tables(const Program& p, const reshard_tile_t* d
                                        const int64_t* d_prefix, const uint32_t* d_goff,
                                        const uint16_t* d_gbuf, int num_sms,
                                        unsigned char* const* bufs, int nbufs, void* stream);
+// TMA-staged fan-out (bulk_fanout.cu) for a 16-byte-aligned program.
+reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelParams& kp,
+                                      void* stream);
 // Occupancy of the copy kernel on the current device (blocks per SM).
 reshard_status_t copy_kernel_occupancy(int* blocks_per_sm);
 

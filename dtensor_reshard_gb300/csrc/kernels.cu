@@ -1,8 +1,10 @@
-// kernels.cu -- the copy kernel of libreshard.so (sm_103a).
+// kernels.cu -- the vector copy kernel of libreshard.so (sm_103a).
 //
 // One persistent kernel executes every copy program of a plan: the read-once
 // fan-out reshard, the per-replica box copy, and both steps of the
-// gather-and-broadcast baseline.  The work of a program is a list of tiles
+// gather-and-broadcast baseline.  (A fan-out whose tiles and buffers are all
+// 16-byte aligned is handed to the TMA-staged kernel of bulk_fanout.cu, which
+// uses the same work partition.)  The work of a program is a list of tiles
 // (see reshard_tile_t), each split into equal work units; CTA b of a grid of
 // G takes units [b*U/G, (b+1)*U/G) of the program's U units, so every CTA
 // moves the same number of bytes regardless of how unequal the tiles are, and
@@ -32,17 +34,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
-
-struct KernelParams {
-  const reshard_tile_t* tiles;
-  const int64_t* prefix;
-  const uint32_t* goff;
-  const uint16_t* gbuf;
-  int64_t total_units;
-  int32_t ntiles;
-  int32_t nbufs;
-  unsigned char* bufs[RESHARD_MAX_EXEC_BUFFERS];
-};
 
 // Unsigned 32-bit division by a runtime-invariant divisor through a multiply
 // and a shift (Granlund and Montgomery, "Division by Invariant Integers using
@@ -270,11 +261,6 @@ reshard_status_t launch_program(const reshard_plan_s* plan, const Program& prog,
   for (int i = 0; i < nbufs; ++i) align |= reinterpret_cast<uint64_t>(bufs[i]);
   int w_log2 = 4;
   while (w_log2 > 0 && (align & ((uint64_t(1) << w_log2) - 1)) != 0) --w_log2;
-  const int planes = prog.has_planes ? 1 : 0;
-  int bps = 1;
-  reshard_status_t st = occupancy(dev, w_log2, planes, &bps);
-  if (st != RESHARD_OK) return st;
-
   KernelParams kp;
   kp.tiles = prog.d_tiles;
   kp.prefix = prog.d_prefix;
@@ -286,6 +272,13 @@ reshard_status_t launch_program(const reshard_plan_s* plan, const Program& prog,
   for (int i = 0; i < nbufs; ++i) kp.bufs[i] = bufs[i];
   for (int i = nbufs; i < RESHARD_MAX_EXEC_BUFFERS; ++i) kp.bufs[i] = nullptr;
 
+  // A fully 16-byte-aligned fan-out goes through the TMA-staged pipeline.
+  if (prog.staged && w_log2 == 4) return launch_fanout_staged(plan, kp, stream);
+
+  const int planes = prog.has_planes ? 1 : 0;
+  int bps = 1;
+  reshard_status_t st = occupancy(dev, w_log2, planes, &bps);
+  if (st != RESHARD_OK) return st;
   const int64_t max_grid = int64_t(plan->num_sms) * bps;
   const unsigned grid = unsigned(total < max_grid ? total : max_grid);
   void* args[] = {&kp};

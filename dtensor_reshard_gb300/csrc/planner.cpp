@@ -448,6 +448,7 @@ reshard_status_t build_plan(reshard_plan_s* P) {
     emit_box(PS, scratch_buf, uint16_t(r), nd, b.shp, s0, gst, 0, dst, eb);
   }
   for (Program* p : {&PF, &PB, &PG, &PS}) finish_program(*p);
+  PF.staged = true;
   for (int k = 0; k < 4; ++k) S.n_tiles[k] = int64_t(P->prog[k].tiles.size());
 
   // ---- traffic accounting

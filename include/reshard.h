@@ -229,6 +229,26 @@ reshard_status_t gather_broadcast_execute(reshard_plan_t plan, const void* const
                                           void* const* dst_ptrs, void* full_scratch,
                                           size_t scratch_bytes, void* stream);
 
+/*
+ * Status word of the current device's copy kernels (no counterpart on the pages:
+ * failure detection of this library).  The TMA-staged fan-out kernel bounds
+ * every wait on its shared-memory barriers; a wait that runs out (which a
+ * correct run never does) records a nonzero code here instead of hanging or
+ * trapping, and the kernel returns.  Codes: 0 none, 1 producer wait, 2 consumer
+ * wait, 3 self-test.  Synchronous (reads device memory with cudaMemcpy);
+ * `clear` != 0 resets the word to 0 after reading.  Errors: INVALID_ARG, CUDA.
+ */
+reshard_status_t reshard_device_status(int32_t clear, uint32_t* status);
+
+/*
+ * Launch, on `stream`, one CTA that waits on a shared-memory barrier nobody
+ * will ever arrive at, with the same bounded wait as the copy kernels but a
+ * limit of `polls` polls (1..2^20).  After the stream completes,
+ * reshard_device_status() reports code 3 and the device remains usable.  For
+ * tests of the failure path.  Errors: INVALID_ARG, CUDA.
+ */
+reshard_status_t reshard_selftest_wait_timeout(uint32_t polls, void* stream);
+
 /* Sizes of the static device arrays used by gather_broadcast_execute_static. */
 #define RESHARD_STATIC_SCRATCH_BYTES (64ull << 20) /* largest global tensor: 64 MiB */
 #define RESHARD_STATIC_TABLE_BYTES (1ull << 20)    /* gather + slice descriptor tables */

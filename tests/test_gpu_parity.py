@@ -93,6 +93,7 @@ def run_and_compare(oracle, spec, kernel=rs.KERNEL_FANOUT, misalign=0, stream=No
     if scratch is not None:
         assert np.array_equal(scratch.payload().cpu().numpy(), helpers.to_bytes(glob))
         assert scratch.guards_intact()
+    assert rs.reshard_device_status() == 0, "a bounded wait ran out in a copy kernel"
 
 
 # ---------------------------------------------------------------------- reduced workloads
