@@ -39,8 +39,11 @@ struct KernelParams {
   int64_t total_units;
   int32_t ntiles;
   int32_t nbufs;
+  uint32_t flags;  // kFlagDstCongruent: every destination buffer has the same address mod 16
+  uint32_t pad;
   unsigned char* bufs[RESHARD_MAX_EXEC_BUFFERS];
 };
+constexpr uint32_t kFlagDstCongruent = 1u;
 
 struct Box {
   int64_t off[RESHARD_MAX_TENSOR_NDIM];
@@ -71,6 +74,9 @@ struct Program {
   uint64_t align_bits = 0;
   bool has_planes = false;  // some tile has nplanes > 1
   bool staged = false;      // eligible for the TMA-staged fan-out kernel when 16-byte aligned
+  int max_fanout = 0;       // largest destination group
+  int64_t tile_bytes = 0;   // source bytes of all tiles
+  int64_t long_row_bytes = 0;  // ... of those in rows of at least 512 bytes (runs included)
   int64_t total_units() const { return prefix.empty() ? 0 : prefix.back(); }
 };
 

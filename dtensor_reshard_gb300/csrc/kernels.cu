@@ -204,16 +204,224 @@ __global__ void __launch_bounds__(kThreads, PLANES ? 2 : 4)
 }
 
 
+// ---------------------------------------------------------------- realigning path
+// For programs whose offsets, strides or rows are not all 16-byte aligned.  A
+// destination range is written with aligned 16-byte stores; each output
+// vector is assembled from the two aligned 16-byte source vectors that hold
+// its bytes (byte permute), so source and destination may differ in alignment
+// by any number of bytes.  Bytes before the first and after the last aligned
+// destination vector are copied one by one.  Source reads may touch bytes
+// outside the range only inside the aligned 16-byte granules that also hold
+// bytes of the range.
+
+__device__ __forceinline__ uint4 load16_cached(const unsigned char* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Bytes [o, o + 16) of the 32 bytes A:B, with q = o / 4 and
+// sel = 0x3210 + 0x1111 * (o % 4) (byte-permute selector).
+__device__ __forceinline__ uint4 funnel16(const uint4& A, const uint4& B, uint32_t q,
+                                          uint32_t sel) {
+  const uint32_t x0 = q == 0 ? A.x : q == 1 ? A.y : q == 2 ? A.z : A.w;
+  const uint32_t x1 = q == 0 ? A.y : q == 1 ? A.z : q == 2 ? A.w : B.x;
+  const uint32_t x2 = q == 0 ? A.z : q == 1 ? A.w : q == 2 ? B.x : B.y;
+  const uint32_t x3 = q == 0 ? A.w : q == 1 ? B.x : q == 2 ? B.y : B.z;
+  const uint32_t x4 = q == 0 ? B.x : q == 1 ? B.y : q == 2 ? B.z : B.w;
+  return make_uint4(__byte_perm(x0, x1, sel), __byte_perm(x1, x2, sel), __byte_perm(x2, x3, sel),
+                    __byte_perm(x3, x4, sel));
+}
+
+constexpr int kRealignUnroll = 4;
+
+// m aligned destination vectors: vector k comes from source bytes at base + o + 16k.
+__device__ __forceinline__ void realigned_body(const unsigned char* base, uint32_t o,
+                                               unsigned char* const* sdst, int R, int64_t doff,
+                                               uint32_t m, int tid, int nthr) {
+  const uint32_t q = o >> 2;
+  const uint32_t sel = 0x3210u + 0x1111u * (o & 3u);
+  const bool two = o != 0;
+#pragma unroll 1
+  for (uint32_t k0 = tid; k0 < m; k0 += uint32_t(kRealignUnroll) * nthr) {
+    uint4 out[kRealignUnroll];
+#pragma unroll
+    for (int j = 0; j < kRealignUnroll; ++j) {
+      const uint32_t k = k0 + j * nthr;
+      if (k < m) {
+        const uint4 A = load16_cached(base + size_t(k) * 16);
+        const uint4 B = two ? load16_cached(base + size_t(k) * 16 + 16) : A;
+        out[j] = funnel16(A, B, q, sel);
+      }
+    }
+#pragma unroll 1
+    for (int r = 0; r < R; ++r) {
+      unsigned char* d = sdst[r] + doff;
+#pragma unroll
+      for (int j = 0; j < kRealignUnroll; ++j) {
+        const uint32_t k = k0 + j * nthr;
+        if (k < m) store_stream<uint4>(d + size_t(k) * 16, out[j]);
+      }
+    }
+  }
+}
+
+// n bytes from s to sdst[r] + doff for r < R, by threads tid of nthr.  All
+// sdst[r] + doff must have the same address mod 16.
+__device__ __forceinline__ void realigned_copy(const unsigned char* s, unsigned char* const* sdst,
+                                               int R, int64_t doff, uint64_t n, int tid,
+                                               int nthr) {
+  const uint32_t dmis = uint32_t(reinterpret_cast<uintptr_t>(sdst[0] + doff) & 15u);
+  const uint64_t h = min(uint64_t((16u - dmis) & 15u), n);
+  for (uint64_t i = tid; i < h; i += nthr) {
+    const unsigned char v = s[i];
+    for (int r = 0; r < R; ++r) sdst[r][doff + i] = v;
+  }
+  const uint32_t m = uint32_t((n - h) >> 4);
+  const unsigned char* s0 = s + h;
+  const uint32_t o = uint32_t(reinterpret_cast<uintptr_t>(s0) & 15u);
+  const unsigned char* base = s0 - o;
+  realigned_body(base, o, sdst, R, doff + int64_t(h), m, tid, nthr);
+  for (uint64_t i = h + uint64_t(m) * 16 + tid; i < n; i += nthr) {
+    const unsigned char v = s[i];
+    for (int r = 0; r < R; ++r) sdst[r][doff + i] = v;
+  }
+}
+
+// A short row (< 64 bytes) by one thread, in the widest unit both ends allow.
+__device__ __forceinline__ void short_row_copy(const unsigned char* s, unsigned char* d,
+                                               uint32_t n) {
+  const uint32_t a = uint32_t(reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d)) | n;
+  if ((a & 7u) == 0) {
+    for (uint32_t i = 0; i < n; i += 8)
+      *reinterpret_cast<uint2*>(d + i) = *reinterpret_cast<const uint2*>(s + i);
+  } else if ((a & 3u) == 0) {
+    for (uint32_t i = 0; i < n; i += 4)
+      *reinterpret_cast<uint32_t*>(d + i) = *reinterpret_cast<const uint32_t*>(s + i);
+  } else if ((a & 1u) == 0) {
+    for (uint32_t i = 0; i < n; i += 2)
+      *reinterpret_cast<uint16_t*>(d + i) = *reinterpret_cast<const uint16_t*>(s + i);
+  } else {
+    for (uint32_t i = 0; i < n; ++i) d[i] = s[i];
+  }
+}
+
+constexpr uint32_t kShortRow = 64;
+
+template <bool PLANES>
+__global__ void __launch_bounds__(kThreads, PLANES ? 2 : 3)
+    reshard_realign_kernel(const __grid_constant__ KernelParams p) {
+  __shared__ unsigned char* s_dst[kMaxGroup];
+  const bool congruent = (p.flags & kFlagDstCongruent) != 0;
+  const int64_t total = p.total_units;
+  int64_t u0 = total * int64_t(blockIdx.x) / int64_t(gridDim.x);
+  const int64_t u1 = total * int64_t(blockIdx.x + 1) / int64_t(gridDim.x);
+  if (u0 >= u1) return;
+  int lo = 0, hi = p.ntiles - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.prefix[mid] <= u0) lo = mid;
+    else hi = mid - 1;
+  }
+  int ti = lo;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  while (u0 < u1) {
+    const reshard_tile_t t = p.tiles[ti];
+    const int64_t tb = p.prefix[ti];
+    const int64_t te = p.prefix[ti + 1];
+    const int64_t a = u0 - tb;
+    const int64_t b = (u1 < te ? u1 : te) - tb;
+    const uint32_t g0 = p.goff[t.dst_group];
+    const int R = int(p.goff[t.dst_group + 1] - g0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < R; i += kThreads) s_dst[i] = p.bufs[p.gbuf[g0 + i]];
+    __syncthreads();
+    const unsigned char* src = p.bufs[t.src_buf];
+    const bool run = t.nrows == 1 && t.nplanes == 1;
+    const uint32_t upr = t.row_bytes >= kUnitBytes ? 1u : uint32_t(kUnitBytes) / t.row_bytes;
+    const uint64_t rows = uint64_t(t.nrows) * t.nplanes;
+    const uint32_t r_begin = run ? 0u : uint32_t(a * upr);
+    const uint32_t r_end = run ? 1u : uint32_t(min(uint64_t(b) * upr, rows));
+    const FastDiv by_rows(PLANES ? t.nrows : 1u);
+    auto row_offsets = [&](uint32_t r, int64_t* so, int64_t* dof) {
+      uint32_t pl = 0, q = r;
+      if (PLANES) {
+        pl = by_rows.div(r);
+        q = r - pl * t.nrows;
+      }
+      *so = t.src_off + int64_t(pl) * t.src_plane_stride + int64_t(q) * t.src_row_stride;
+      *dof = t.dst_off + int64_t(pl) * t.dst_plane_stride + int64_t(q) * t.dst_row_stride;
+    };
+    if (run || t.row_bytes >= kShortRow) {
+      // a run: the whole CTA on its byte range; long rows: one warp per row
+      const uint32_t njobs = r_end - r_begin;
+      const uint32_t first = run ? 0u : uint32_t(warp);
+      const uint32_t stride = run ? 1u : uint32_t(kThreads / 32);
+      const int tid = run ? int(threadIdx.x) : lane;
+      const int nthr = run ? kThreads : 32;
+      for (uint32_t j = first; j < njobs; j += stride) {
+        int64_t so, dof;
+        uint64_t n;
+        if (run) {
+          const int64_t b0 = a * kUnitBytes;
+          so = t.src_off + b0;
+          dof = t.dst_off + b0;
+          n = uint64_t(min(b * kUnitBytes, int64_t(t.row_bytes)) - b0);
+        } else {
+          row_offsets(r_begin + j, &so, &dof);
+          n = t.row_bytes;
+        }
+        const int passes = congruent ? 1 : R;
+        for (int q = 0; q < passes; ++q)
+          realigned_copy(src + so, s_dst + q, congruent ? R : 1, dof, n, tid, nthr);
+      }
+    } else {
+      // short rows: one thread per row
+      for (uint32_t r = r_begin + threadIdx.x; r < r_end; r += kThreads) {
+        int64_t so, dof;
+        row_offsets(r, &so, &dof);
+        for (int j = 0; j < R; ++j) short_row_copy(src + so, s_dst[j] + dof, t.row_bytes);
+      }
+    }
+    u0 = tb + b;
+    ++ti;
+  }
+}
+
 using KernelFn = void (*)(KernelParams);
 
 // Instantiations indexed by [log2 W][planes].
-const KernelFn kKernels[5][2] = {
-    {reshard_copy_kernel<1, false>, reshard_copy_kernel<1, true>},
+// [0]: realigning kernel (any alignment); [k], k = 1..4: 2^k-byte vector kernel;
+// [5]: byte kernel.
+const KernelFn kKernels[6][2] = {
+    {reshard_realign_kernel<false>, reshard_realign_kernel<true>},
     {reshard_copy_kernel<2, false>, reshard_copy_kernel<2, true>},
     {reshard_copy_kernel<4, false>, reshard_copy_kernel<4, true>},
     {reshard_copy_kernel<8, false>, reshard_copy_kernel<8, true>},
     {reshard_copy_kernel<16, false>, reshard_copy_kernel<16, true>},
+    {reshard_copy_kernel<1, false>, reshard_copy_kernel<1, true>},
 };
+
+// Kernel for a program whose widest common access is 2^w_log2 bytes: the
+// 16-byte vector kernel when everything is aligned; otherwise the realigning
+// kernel when the program fans out to several replicas over mostly long rows
+// (16-byte stores then pay for the byte permutes), else the element-width
+// kernel (measured on the uneven-stress tensors).
+int choose_kernel(const Program& prog, int w_log2) {
+  if (w_log2 == 4) return 4;
+  if (prog.max_fanout >= 2 && 2 * prog.long_row_bytes >= prog.tile_bytes) return 0;
+  return w_log2 == 0 ? 5 : w_log2;
+}
+
+// Every destination buffer of the program at the same address mod 16?
+bool destinations_congruent(const Program& prog, unsigned char* const* bufs) {
+  int64_t first = -1;
+  for (uint16_t bi : prog.gbuf) {
+    const int64_t m = int64_t(reinterpret_cast<uintptr_t>(bufs[bi]) & 15u);
+    if (bufs[bi] == nullptr) continue;
+    if (first < 0) first = m;
+    else if (m != first) return false;
+  }
+  return true;
+}
 
 std::mutex g_occ_mu;
 std::map<std::pair<int, int>, int> g_occ;  // (device, kernel index) -> blocks per SM
@@ -272,17 +480,21 @@ reshard_status_t launch_program(const reshard_plan_s* plan, const Program& prog,
   for (int i = 0; i < nbufs; ++i) kp.bufs[i] = bufs[i];
   for (int i = nbufs; i < RESHARD_MAX_EXEC_BUFFERS; ++i) kp.bufs[i] = nullptr;
 
+  kp.flags = destinations_congruent(prog, bufs) ? kFlagDstCongruent : 0u;
+  kp.pad = 0;
+
   // A fully 16-byte-aligned fan-out goes through the TMA-staged pipeline.
   if (prog.staged && w_log2 == 4) return launch_fanout_staged(plan, kp, stream);
 
   const int planes = prog.has_planes ? 1 : 0;
+  const int kidx = choose_kernel(prog, w_log2);
   int bps = 1;
-  reshard_status_t st = occupancy(dev, w_log2, planes, &bps);
+  reshard_status_t st = occupancy(dev, kidx, planes, &bps);
   if (st != RESHARD_OK) return st;
   const int64_t max_grid = int64_t(plan->num_sms) * bps;
   const unsigned grid = unsigned(total < max_grid ? total : max_grid);
   void* args[] = {&kp};
-  cudaError_t ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[w_log2][planes]),
+  cudaError_t ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[kidx][planes]),
                                     dim3(grid), dim3(kThreads), args, 0,
                                     static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess)
@@ -310,8 +522,9 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
   int w_log2 = 4;
   while (w_log2 > 0 && (align & ((uint64_t(1) << w_log2) - 1)) != 0) --w_log2;
   const int planes = prog.has_planes ? 1 : 0;
+  const int kidx = choose_kernel(prog, w_log2);
   int bps = 1;
-  reshard_status_t st = occupancy(dev, w_log2, planes, &bps);
+  reshard_status_t st = occupancy(dev, kidx, planes, &bps);
   if (st != RESHARD_OK) return st;
 
   KernelParams kp;
@@ -324,11 +537,13 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
   kp.nbufs = nbufs;
   for (int i = 0; i < nbufs; ++i) kp.bufs[i] = bufs[i];
   for (int i = nbufs; i < RESHARD_MAX_EXEC_BUFFERS; ++i) kp.bufs[i] = nullptr;
+  kp.flags = destinations_congruent(prog, bufs) ? kFlagDstCongruent : 0u;
+  kp.pad = 0;
 
   const int64_t max_grid = int64_t(num_sms) * bps;
   const unsigned grid = unsigned(total < max_grid ? total : max_grid);
   void* args[] = {&kp};
-  ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[w_log2][planes]), dim3(grid),
+  ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[kidx][planes]), dim3(grid),
                         dim3(kThreads), args, 0, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(ce));

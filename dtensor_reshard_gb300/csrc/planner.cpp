@@ -261,7 +261,12 @@ void finish_program(Program& P) {
                     uint64_t(t.src_row_stride) | uint64_t(t.dst_row_stride) |
                     uint64_t(t.src_plane_stride) | uint64_t(t.dst_plane_stride);
     if (t.nplanes > 1) P.has_planes = true;
+    const int64_t bytes = int64_t(t.row_bytes) * t.nrows * t.nplanes;
+    P.tile_bytes += bytes;
+    if (t.row_bytes >= 512) P.long_row_bytes += bytes;
   }
+  for (size_t g = 0; g + 1 < P.goff.size(); ++g)
+    P.max_fanout = std::max<int>(P.max_fanout, int(P.goff[g + 1] - P.goff[g]));
 }
 
 int64_t tile_bytes(const reshard_tile_t& t) {

@@ -62,14 +62,15 @@ def _upload(arrs, misalign=0):
 
 
 def run_and_compare(oracle, spec, kernel=rs.KERNEL_FANOUT, misalign=0, stream=None,
-                    path="reshard"):
+                    path="reshard", dst_misalign=None):
     _cuda()
     glob = global_tensor(spec)
     srcs = [helpers.to_bytes(s) for s in helpers.scatter_with_oracle(
         oracle, glob, spec.src_mesh, spec.src_placements)]
     want = helpers.expected_dst(oracle, spec, srcs)
     dsrc = _upload(srcs, misalign)
-    ddst = [Guarded(w.size, misalign) for w in want]
+    ddst = [Guarded(w.size, misalign if dst_misalign is None else dst_misalign(r))
+            for r, w in enumerate(want)]
     plan = helpers.spec_plan(spec)
     sptr = [g.ptr for g in dsrc]
     dptr = [g.ptr for g in ddst]
@@ -169,6 +170,15 @@ def test_misaligned_buffers(oracle, misalign):
     """Base pointers off the 16-byte grid take the narrower vector paths."""
     for spec in (workload(2, reduced=True).tensors[0], EDGE[4], EDGE[6]):
         run_and_compare(oracle, spec, misalign=misalign)
+
+
+@pytest.mark.parametrize("kernel", [rs.KERNEL_FANOUT, rs.KERNEL_BOXCOPY])
+def test_destinations_with_different_alignments(oracle, kernel):
+    """Replicas whose buffers differ in address mod 16 (one fan-out group)."""
+    for spec in (_spec((300, 97), "bf16", (2,), ("S0",), (2, 3), ("R", "S1")),
+                 _spec((7, 4099), "u8", (3,), ("S1",), (5,), ("R",)),
+                 _spec((64, 1024), "fp32", (4,), ("S0",), (8,), ("R",))):
+        run_and_compare(oracle, spec, kernel=kernel, misalign=3, dst_misalign=lambda r: r % 16)
 
 
 def test_nan_payloads_and_negative_zero_survive(oracle):
