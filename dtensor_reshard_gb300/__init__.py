@@ -56,7 +56,7 @@ class reshard_stats_t(ctypes.Structure):
                 ("boxcopy_read_bytes", ctypes.c_int64), ("boxcopy_write_bytes", ctypes.c_int64),
                 ("gb_read_bytes", ctypes.c_int64), ("gb_write_bytes", ctypes.c_int64),
                 ("max_replica_read_bytes", ctypes.c_int64), ("max_fanout", ctypes.c_int64),
-                ("planner_ns", ctypes.c_int64)]
+                ("planner_ns", ctypes.c_int64), ("inplace_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         out = {}
@@ -98,6 +98,13 @@ def _load():
                                  ctypes.POINTER(reshard_placement_t),
                                  ctypes.POINTER(reshard_mesh_t),
                                  ctypes.POINTER(reshard_placement_t), vpp], ctypes.c_int),
+        "reshard_plan_create_inplace": ([i64p, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.POINTER(reshard_mesh_t),
+                                         ctypes.POINTER(reshard_placement_t),
+                                         ctypes.POINTER(reshard_mesh_t),
+                                         ctypes.POINTER(reshard_placement_t), i64p, vpp],
+                                        ctypes.c_int),
+        "reshard_plan_alias": ([vp, ctypes.c_int64, i64p, i64p], ctypes.c_int),
         "reshard_plan_upload": ([vp], ctypes.c_int),
         "reshard_execute": ([vp, vpp, vpp, vp], ctypes.c_int),
         "reshard_execute_ex": ([vp, vpp, vpp, ctypes.c_int32, vp], ctypes.c_int),
@@ -238,6 +245,32 @@ def reshard_plan_create(global_shape, dtype, src_mesh, src_placements, dst_mesh,
                                   _placements(dst_placements), ctypes.byref(h))
     _check(st, "reshard_plan_create")
     return Plan(h.value, global_shape, dtype, src_mesh, src_placements, dst_mesh, dst_placements)
+
+
+def reshard_plan_create_inplace(global_shape, dtype, src_mesh, src_placements, dst_mesh,
+                                dst_placements, src_alias) -> Plan:
+    """In-place plan: src_alias[s] = destination rank whose buffer holds source shard s (-1:
+    none).  Executions need src_ptrs[s] = dst_ptrs[src_alias[s]] + reshard_plan_alias offset."""
+    shape = (ctypes.c_int64 * max(1, len(global_shape)))(*[int(s) for s in global_shape])
+    alias = (ctypes.c_int64 * max(1, len(src_alias)))(*[int(a) for a in src_alias])
+    h = ctypes.c_void_p()
+    dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    st = _lib.reshard_plan_create_inplace(shape, len(global_shape), dt,
+                                          ctypes.byref(_mesh(src_mesh)),
+                                          _placements(src_placements),
+                                          ctypes.byref(_mesh(dst_mesh)),
+                                          _placements(dst_placements), alias, ctypes.byref(h))
+    _check(st, "reshard_plan_create_inplace")
+    return Plan(h.value, global_shape, dtype, src_mesh, src_placements, dst_mesh, dst_placements)
+
+
+def reshard_plan_alias(plan: Plan, src_rank: int):
+    """(destination rank or -1, byte offset) where source rank src_rank lives."""
+    d = ctypes.c_int64()
+    o = ctypes.c_int64()
+    _check(_lib.reshard_plan_alias(plan, int(src_rank), ctypes.byref(d), ctypes.byref(o)),
+           "reshard_plan_alias")
+    return d.value, o.value
 
 
 def reshard_plan_upload(plan: Plan):

@@ -90,6 +90,10 @@ struct reshard_plan_s {
   rs::Layout src, dst;
   rs::Program prog[4];
   reshard_stats_t stats = {};
+  // in-place plans: source rank s lives inside destination rank alias_dst[s]
+  // (-1: separate buffer) at byte offset alias_off[s]
+  bool inplace = false;
+  std::vector<int64_t> alias_dst, alias_off;
   // device binding
   int device = -1;
   void* d_mem = nullptr;

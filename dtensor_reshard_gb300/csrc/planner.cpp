@@ -305,10 +305,6 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   const int32_t nd = P->ndim;
   const int64_t eb = P->elem_bytes;
   const int64_t M = P->src.nranks, N = P->dst.nranks;
-  P->src.box.resize(M);
-  P->dst.box.resize(N);
-  for (int64_t r = 0; r < M; ++r) resolve_rank(nd, P->gshape, P->src, r, &P->src.box[r]);
-  for (int64_t r = 0; r < N; ++r) resolve_rank(nd, P->gshape, P->dst, r, &P->dst.box[r]);
 
   reshard_stats_t& S = P->stats;
   S.global_bytes = eb;
@@ -377,22 +373,30 @@ reshard_status_t build_plan(reshard_plan_s* P) {
 
   // ---- step 6 (groups first): destination groups
   const uint16_t scratch_buf = uint16_t(M + N);
-  std::vector<std::vector<uint16_t>> fan_groups_of(dc.size());  // FANOUT program
   Program& PF = P->prog[RESHARD_PROGRAM_FANOUT];
   Program& PB = P->prog[RESHARD_PROGRAM_BOXCOPY];
   Program& PG = P->prog[RESHARD_PROGRAM_GATHER];
   Program& PS = P->prog[RESHARD_PROGRAM_SLICE];
   for (Program* p : {&PF, &PB, &PG, &PS}) p->goff.push_back(0);
-  for (size_t di = 0; di < dc.size(); ++di) {
-    const auto& rk = dc[di].ranks;
-    S.max_fanout = std::max<int64_t>(S.max_fanout, int64_t(rk.size()));
-    for (size_t a = 0; a < rk.size(); a += kMaxGroup) {
-      fan_groups_of[di].push_back(uint16_t(PF.goff.size() - 1));
-      for (size_t b = a; b < std::min(rk.size(), a + size_t(kMaxGroup)); ++b)
-        PF.gbuf.push_back(uint16_t(M + rk[b]));
+  for (size_t di = 0; di < dc.size(); ++di)
+    S.max_fanout = std::max<int64_t>(S.max_fanout, int64_t(dc[di].ranks.size()));
+  // FANOUT groups, one per distinct list of target ranks (a destination class,
+  // minus the ranks that already hold the region in place), at most kMaxGroup each
+  std::map<std::vector<int64_t>, std::vector<uint16_t>> group_ids;
+  bool too_many_groups = false;
+  auto fan_groups = [&](const std::vector<int64_t>& ranks) -> const std::vector<uint16_t>& {
+    auto it = group_ids.find(ranks);
+    if (it != group_ids.end()) return it->second;
+    std::vector<uint16_t> ids;
+    for (size_t a = 0; a < ranks.size(); a += kMaxGroup) {
+      if (PF.goff.size() > 65535) too_many_groups = true;
+      ids.push_back(uint16_t(PF.goff.size() - 1));
+      for (size_t b = a; b < std::min(ranks.size(), a + size_t(kMaxGroup)); ++b)
+        PF.gbuf.push_back(uint16_t(M + ranks[b]));
       PF.goff.push_back(uint32_t(PF.gbuf.size()));
     }
-  }
+    return group_ids.emplace(ranks, ids).first->second;
+  };
   // one group per destination rank (BOXCOPY and SLICE)
   for (Program* p : {&PB, &PS}) {
     for (int64_t r = 0; r < N; ++r) {
@@ -407,6 +411,18 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   int64_t gst[RESHARD_MAX_TENSOR_NDIM];
   row_major_strides(nd, P->gshape, gst);
   for (const Region& g : regions) {
+    // destination ranks that still need the region (in-place plans drop the
+    // rank whose buffer already holds a source replica of it)
+    std::vector<int64_t> targets;
+    for (int64_t r : dc[g.d].ranks) {
+      bool in_place = false;
+      if (P->inplace)
+        for (int64_t s : sc[g.s].ranks)
+          if (P->alias_dst[size_t(s)] == r) in_place = true;
+      if (!in_place) targets.push_back(r);
+    }
+    S.inplace_bytes += g.bytes * int64_t(dc[g.d].ranks.size() - targets.size());
+    if (targets.empty()) continue;
     const Box& sb = P->src.box[size_t(g.replica)];
     const Box& db = dc[g.d].box;
     int64_t sst[RESHARD_MAX_TENSOR_NDIM], dst[RESHARD_MAX_TENSOR_NDIM];
@@ -417,11 +433,12 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       s0 += (g.lo[d] - sb.off[d]) * sst[d];
       d0 += (g.lo[d] - db.off[d]) * dst[d];
     }
-    for (uint16_t grp : fan_groups_of[g.d])
+    for (uint16_t grp : fan_groups(targets))
       emit_box(PF, uint16_t(g.replica), grp, nd, g.ext, s0, sst, d0, dst, eb);
-    for (int64_t r : dc[g.d].ranks)
+    for (int64_t r : targets)
       emit_box(PB, uint16_t(g.replica), uint16_t(r), nd, g.ext, s0, sst, d0, dst, eb);
   }
+  if (too_many_groups) return fail(RESHARD_ERR_UNSUPPORTED, "more than 65535 fan-out groups");
   // gather: one replica of every source class into the full tensor
   {
     std::vector<size_t> order(sc.size());
@@ -485,21 +502,60 @@ reshard_status_t fail(reshard_status_t st, const std::string& msg) {
 
 using rs::fail;
 
-extern "C" {
+namespace rs {
+namespace {
 
-reshard_status_t reshard_plan_create(const int64_t* global_shape, int32_t tensor_ndim,
-                                     reshard_dtype_t dtype, const reshard_mesh_t* src_mesh,
-                                     const reshard_placement_t* src_placements,
-                                     const reshard_mesh_t* dst_mesh,
-                                     const reshard_placement_t* dst_placements,
-                                     reshard_plan_t* out_plan) {
+// In-place declaration: source rank s is stored inside destination rank
+// alias[s].  Valid when s's box lies inside that rank's box and occupies one
+// contiguous range of its row-major local layout (leading dims of extent 1,
+// one partial dim, trailing dims full).  Records the byte offset.
+reshard_status_t read_aliases(reshard_plan_s* P, const int64_t* alias) {
+  const int64_t M = P->src.nranks, N = P->dst.nranks;
+  P->inplace = true;
+  P->alias_dst.assign(size_t(M), -1);
+  P->alias_off.assign(size_t(M), 0);
+  for (int64_t s = 0; s < M; ++s) {
+    const int64_t d = alias[s];
+    if (d < 0) continue;
+    if (d >= N) return fail(RESHARD_ERR_INVALID_ARG, "alias rank out of range");
+    const Box& sb = P->src.box[size_t(s)];
+    const Box& db = P->dst.box[size_t(d)];
+    if (box_volume(P->ndim, sb) == 0) continue;  // nothing to hold
+    int k0 = -1;
+    for (int k = 0; k < P->ndim; ++k) {
+      if (sb.off[k] < db.off[k] || sb.off[k] + sb.shp[k] > db.off[k] + db.shp[k])
+        return fail(RESHARD_ERR_SHAPE, "source rank " + std::to_string(s) +
+                                           " is not inside destination rank " + std::to_string(d));
+      if (k0 < 0 && sb.shp[k] != 1) k0 = k;
+    }
+    for (int k = (k0 < 0 ? P->ndim : k0 + 1); k < P->ndim; ++k)
+      if (sb.shp[k] != db.shp[k])
+        return fail(RESHARD_ERR_SHAPE, "source rank " + std::to_string(s) +
+                                           " is not one contiguous range of destination rank " +
+                                           std::to_string(d));
+    int64_t st[RESHARD_MAX_TENSOR_NDIM];
+    row_major_strides(P->ndim, db.shp, st);
+    int64_t off = 0;
+    for (int k = 0; k < P->ndim; ++k) off += (sb.off[k] - db.off[k]) * st[k];
+    P->alias_dst[size_t(s)] = d;
+    P->alias_off[size_t(s)] = off * P->elem_bytes;
+  }
+  return RESHARD_OK;
+}
+
+reshard_status_t create_plan(const int64_t* global_shape, int32_t tensor_ndim,
+                             reshard_dtype_t dtype, const reshard_mesh_t* src_mesh,
+                             const reshard_placement_t* src_placements,
+                             const reshard_mesh_t* dst_mesh,
+                             const reshard_placement_t* dst_placements, const int64_t* alias,
+                             reshard_plan_t* out_plan) {
   const auto t0 = std::chrono::steady_clock::now();
   if (!out_plan) return fail(RESHARD_ERR_INVALID_ARG, "out_plan is NULL");
   *out_plan = nullptr;
   if (tensor_ndim < 1 || tensor_ndim > RESHARD_MAX_TENSOR_NDIM)
     return fail(RESHARD_ERR_UNSUPPORTED, "tensor ndim must be 1..4");
   if (!global_shape) return fail(RESHARD_ERR_INVALID_ARG, "global_shape is NULL");
-  const int eb = rs::elem_size(dtype);
+  const int eb = elem_size(dtype);
   if (!eb) return fail(RESHARD_ERR_INVALID_ARG, "unknown dtype");
   int64_t numel = 1;
   for (int d = 0; d < tensor_ndim; ++d) {
@@ -513,14 +569,21 @@ reshard_status_t reshard_plan_create(const int64_t* global_shape, int32_t tensor
   P->ndim = tensor_ndim;
   P->elem_bytes = eb;
   for (int d = 0; d < tensor_ndim; ++d) P->gshape[d] = global_shape[d];
-  reshard_status_t st = rs::read_layout("source", tensor_ndim, src_mesh, src_placements, &P->src);
+  reshard_status_t st = read_layout("source", tensor_ndim, src_mesh, src_placements, &P->src);
   if (st == RESHARD_OK)
-    st = rs::read_layout("destination", tensor_ndim, dst_mesh, dst_placements, &P->dst);
+    st = read_layout("destination", tensor_ndim, dst_mesh, dst_placements, &P->dst);
   if (st == RESHARD_OK && P->src.nranks + P->dst.nranks + 1 > 65535)
     st = fail(RESHARD_ERR_UNSUPPORTED, "M + N + 1 must fit in 16 bits");
   if (st == RESHARD_OK) {
     try {
-      st = rs::build_plan(P);
+      P->src.box.resize(size_t(P->src.nranks));
+      P->dst.box.resize(size_t(P->dst.nranks));
+      for (int64_t r = 0; r < P->src.nranks; ++r)
+        resolve_rank(P->ndim, P->gshape, P->src, r, &P->src.box[size_t(r)]);
+      for (int64_t r = 0; r < P->dst.nranks; ++r)
+        resolve_rank(P->ndim, P->gshape, P->dst, r, &P->dst.box[size_t(r)]);
+      if (alias) st = read_aliases(P, alias);
+      if (st == RESHARD_OK) st = build_plan(P);
     } catch (const std::bad_alloc&) {
       st = fail(RESHARD_ERR_NO_MEMORY, "host allocation failed while planning");
     }
@@ -529,14 +592,51 @@ reshard_status_t reshard_plan_create(const int64_t* global_shape, int32_t tensor
     delete P;
     return st;
   }
-  P->magic = rs::kPlanMagic;
+  P->magic = kPlanMagic;
   P->stats.planner_ns = std::chrono::duration_cast<std::chrono::nanoseconds>(
                             std::chrono::steady_clock::now() - t0).count();
   {
-    std::lock_guard<std::mutex> lk(rs::g_registry_mu);
-    rs::registry().insert(P);
+    std::lock_guard<std::mutex> lk(g_registry_mu);
+    registry().insert(P);
   }
   *out_plan = P;
+  return RESHARD_OK;
+}
+
+}  // namespace
+}  // namespace rs
+
+extern "C" {
+
+reshard_status_t reshard_plan_create(const int64_t* global_shape, int32_t tensor_ndim,
+                                     reshard_dtype_t dtype, const reshard_mesh_t* src_mesh,
+                                     const reshard_placement_t* src_placements,
+                                     const reshard_mesh_t* dst_mesh,
+                                     const reshard_placement_t* dst_placements,
+                                     reshard_plan_t* out_plan) {
+  return rs::create_plan(global_shape, tensor_ndim, dtype, src_mesh, src_placements, dst_mesh,
+                         dst_placements, nullptr, out_plan);
+}
+
+reshard_status_t reshard_plan_create_inplace(const int64_t* global_shape, int32_t tensor_ndim,
+                                             reshard_dtype_t dtype, const reshard_mesh_t* src_mesh,
+                                             const reshard_placement_t* src_placements,
+                                             const reshard_mesh_t* dst_mesh,
+                                             const reshard_placement_t* dst_placements,
+                                             const int64_t* src_alias, reshard_plan_t* out_plan) {
+  if (!src_alias) return fail(RESHARD_ERR_INVALID_ARG, "src_alias is NULL");
+  return rs::create_plan(global_shape, tensor_ndim, dtype, src_mesh, src_placements, dst_mesh,
+                         dst_placements, src_alias, out_plan);
+}
+
+reshard_status_t reshard_plan_alias(reshard_plan_t plan, int64_t src_rank, int64_t* dst_rank,
+                                    int64_t* byte_offset) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (src_rank < 0 || src_rank >= plan->src.nranks)
+    return fail(RESHARD_ERR_INVALID_ARG, "rank out of range");
+  if (!dst_rank || !byte_offset) return fail(RESHARD_ERR_INVALID_ARG, "null output");
+  *dst_rank = plan->inplace ? plan->alias_dst[size_t(src_rank)] : -1;
+  *byte_offset = plan->inplace ? plan->alias_off[size_t(src_rank)] : 0;
   return RESHARD_OK;
 }
 
@@ -649,6 +749,17 @@ reshard_status_t buffer_table(reshard_plan_t plan, const void* const* src_ptrs,
     (*bufs)[size_t(M + r)] = static_cast<unsigned char*>(dst_ptrs[r]);
   }
   (*bufs)[size_t(M + N)] = static_cast<unsigned char*>(scratch);
+  if (plan->inplace) {
+    for (int64_t r = 0; r < M; ++r) {
+      const int64_t d = plan->alias_dst[size_t(r)];
+      if (d < 0) continue;
+      if ((*bufs)[size_t(r)] != (*bufs)[size_t(M + d)] + plan->alias_off[size_t(r)])
+        return fail(RESHARD_ERR_INVALID_ARG,
+                    "in-place plan: source rank " + std::to_string(r) +
+                        " must point into destination rank " + std::to_string(d) +
+                        " at byte offset " + std::to_string(plan->alias_off[size_t(r)]));
+    }
+  }
   return RESHARD_OK;
 }
 

@@ -136,6 +136,7 @@ typedef struct reshard_stats {
   int64_t max_replica_read_bytes;  /* busiest source replica's bytes read (fan-out plan) */
   int64_t max_fanout;          /* largest number of destination replicas of one box */
   int64_t planner_ns;          /* wall time of reshard_plan_create */
+  int64_t inplace_bytes;       /* destination bytes already in place (in-place plans), not written */
 } reshard_stats_t;
 
 /*
@@ -178,6 +179,37 @@ reshard_status_t reshard_plan_create(const int64_t* global_shape, int32_t tensor
                                      const reshard_mesh_t* dst_mesh,
                                      const reshard_placement_t* dst_placements,
                                      reshard_plan_t* out_plan);
+
+/*
+ * In-place plan (HybridFlow's 3D-HybridEngine: siliconandsystems.com HybridFlow
+ * summary, section on moving the actor without redundant copies -- generation
+ * ranks are assigned at a stride so that each rank's generation shard contains
+ * its own training shard, and no weight is held twice).  src_alias[s] names the
+ * destination rank whose buffer ALREADY HOLDS source shard s (or -1 when s has
+ * a buffer of its own).  Source rank s's box must lie inside that destination
+ * box and form one contiguous range of its row-major local layout (leading
+ * dims of extent 1, one partial dim, trailing dims full); otherwise
+ * RESHARD_ERR_SHAPE.  The plan then skips every copy whose bytes are already in
+ * place: a region is written only to the destination replicas that do not
+ * hold it (reshard_stats_t.inplace_bytes counts the bytes skipped).
+ * Executions of such a plan require src_ptrs[s] == dst_ptrs[src_alias[s]] +
+ * the offset reported by reshard_plan_alias() for every aliased s
+ * (RESHARD_ERR_INVALID_ARG otherwise); source and destination buffers may then
+ * overlap exactly in that way, and no copy writes a byte that another copy
+ * of the same execution reads.  Other arguments and errors as
+ * reshard_plan_create.
+ */
+reshard_status_t reshard_plan_create_inplace(const int64_t* global_shape, int32_t tensor_ndim,
+                                             reshard_dtype_t dtype, const reshard_mesh_t* src_mesh,
+                                             const reshard_placement_t* src_placements,
+                                             const reshard_mesh_t* dst_mesh,
+                                             const reshard_placement_t* dst_placements,
+                                             const int64_t* src_alias, reshard_plan_t* out_plan);
+
+/* Destination rank (-1 if none) and byte offset at which source rank src_rank lives in an
+ * in-place plan.  Errors: BAD_HANDLE, INVALID_ARG. */
+reshard_status_t reshard_plan_alias(reshard_plan_t plan, int64_t src_rank, int64_t* dst_rank,
+                                    int64_t* byte_offset);
 
 /*
  * Copy the plan's descriptor tables to the CURRENT device (one cudaMalloc and

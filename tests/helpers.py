@@ -73,3 +73,35 @@ def run_program_cpu(plan, program, bufs):
 def spec_plan(spec):
     return rs.reshard_plan_create(spec.global_shape, spec.dtype, spec.src_mesh,
                                   spec.src_placements, spec.dst_mesh, spec.dst_placements)
+
+
+def contiguous_inside(src_box, dst_box):
+    """True when src_box lies in dst_box as one contiguous range of dst's row-major layout."""
+    (so, ss), (do, ds) = src_box, dst_box
+    if math.prod(ss) == 0:
+        return False
+    for a, b, c, d in zip(so, ss, do, ds):
+        if a < c or a + b > c + d:
+            return False
+    k0 = next((k for k, e in enumerate(ss) if e != 1), len(ss))
+    return all(ss[k] == ds[k] for k in range(k0 + 1, len(ss)))
+
+
+def alias_offset_bytes(src_box, dst_box, elem_bytes):
+    (so, _), (do, ds) = src_box, dst_box
+    strides = [math.prod(ds[k + 1:]) for k in range(len(ds))]
+    return sum((a - c) * st for a, c, st in zip(so, do, strides)) * elem_bytes
+
+
+def pick_aliases(o, spec, rng=None):
+    """A valid in-place alias map (first containing destination rank, or -1)."""
+    sb = o.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+    db = o.boxes(spec.global_shape, spec.dst_mesh, spec.dst_placements)
+    out = []
+    for s in range(len(sb)):
+        cands = [d for d in range(len(db)) if contiguous_inside(sb[s], db[d])]
+        if not cands or (rng is not None and rng.random() < 0.25):
+            out.append(-1)
+        else:
+            out.append(cands[0] if rng is None else rng.choice(cands))
+    return out

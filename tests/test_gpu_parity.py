@@ -293,3 +293,96 @@ def test_full_moe_refit(oracle, idx):
 def test_full_uneven_stress_sampled(oracle):
     for spec in workload(4).tensors:
         _full_size_check(oracle, spec, samples=300)
+
+
+# ---------------------------------------------------------------------- in place
+def run_inplace(oracle, spec, alias, kernel=rs.KERNEL_FANOUT):
+    _cuda()
+    glob = global_tensor(spec)
+    sboxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+    srcs = [helpers.to_bytes(helpers.slice_box(glob, o, s)) for o, s in sboxes]
+    want = helpers.expected_dst(oracle, spec, srcs)
+    plan = rs.reshard_plan_create_inplace(spec.global_shape, spec.dtype, spec.src_mesh,
+                                          spec.src_placements, spec.dst_mesh, spec.dst_placements,
+                                          alias)
+    ddst = [Guarded(w.size) for w in want]
+    sptr, own = [], []
+    for s in range(spec.n_src):
+        d, off = rs.reshard_plan_alias(plan, s)
+        n = srcs[s].size
+        if d >= 0 and n:
+            ddst[d].payload()[off:off + n].copy_(torch.from_numpy(srcs[s]).cuda())
+            sptr.append(ddst[d].ptr + off)
+        else:
+            g = Guarded(n)
+            if n:
+                g.payload().copy_(torch.from_numpy(srcs[s]).cuda())
+            own.append(g)
+            sptr.append(g.ptr)
+    rs.reshard_execute_ex(plan, sptr, [g.ptr for g in ddst], kernel)
+    torch.cuda.synchronize()
+    for r, (g, w) in enumerate(zip(ddst, want)):
+        assert np.array_equal(g.payload().cpu().numpy(), w), (spec.name, r, kernel)
+        assert g.guards_intact()
+    for g in own:
+        assert g.guards_intact()
+    assert rs.reshard_device_status() == 0
+    return rs.reshard_plan_stats(plan)
+
+
+@pytest.mark.parametrize("kernel", [rs.KERNEL_FANOUT, rs.KERNEL_BOXCOPY])
+def test_inplace_hybridflow_divisible(oracle, kernel):
+    spec = TensorSpec("hf", (2048, 819), "bf16", (8,), ("S0",), (2, 4), ("S0", "R"),
+                      init=("bits",), seed=31)
+    st = run_inplace(oracle, spec, list(range(8)), kernel)
+    assert st["inplace_bytes"] == spec.global_bytes
+
+
+@pytest.mark.parametrize("kernel", [rs.KERNEL_FANOUT, rs.KERNEL_BOXCOPY])
+def test_inplace_reduced_and_random(oracle, kernel):
+    for spec in workload(3, reduced=True).tensors:
+        run_inplace(oracle, spec, helpers.pick_aliases(oracle, spec), kernel)
+    rng = random.Random(41)
+    n = 0
+    while n < 40:
+        nd = rng.choice((1, 2, 3))
+        gshape = tuple(rng.randint(1, 40) for _ in range(nd))
+        sm = tuple(rng.randint(1, 4) for _ in range(rng.randint(1, 2)))
+        dm = tuple(rng.randint(1, 4) for _ in range(rng.randint(1, 2)))
+        sp = tuple(rng.choice(["R"] + [f"S{d}" for d in range(nd)]) for _ in sm)
+        dp = tuple(rng.choice(["R"] + [f"S{d}" for d in range(nd)]) for _ in dm)
+        spec = _spec(gshape, rng.choice(("bf16", "fp32", "u8")), sm, sp, dm, dp, seed=n)
+        alias = helpers.pick_aliases(oracle, spec, rng)
+        if all(a < 0 for a in alias):
+            continue
+        run_inplace(oracle, spec, alias, kernel)
+        n += 1
+
+
+def test_full_hybridflow_layer_inplace(oracle):
+    """Full-size gate projection, in place: every generation buffer starts out holding its
+    own training shard and must end up equal to its slice of the global tensor."""
+    dev = _cuda()
+    spec = workload(3).tensors[0]
+    glob = global_tensor(spec, device=dev)
+    dboxes = oracle.boxes(spec.global_shape, spec.dst_mesh, spec.dst_placements)
+    sboxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+    plan = rs.reshard_plan_create_inplace(spec.global_shape, spec.dtype, spec.src_mesh,
+                                          spec.src_placements, spec.dst_mesh, spec.dst_placements,
+                                          list(range(8)))
+    dsts = [torch.empty(s, dtype=glob.dtype, device=dev) for _, s in dboxes]
+    for d in dsts:
+        d.view(-1).view(torch.uint8).fill_(FILL_BYTE)
+    sptr = []
+    for s, (o, shp) in enumerate(sboxes):
+        d, off = rs.reshard_plan_alias(plan, s)
+        piece = helpers.slice_box(glob, o, shp).reshape(-1).view(torch.uint8)
+        flat = dsts[d].reshape(-1).view(torch.uint8)
+        flat[off:off + piece.numel()].copy_(piece)
+        sptr.append(dsts[d].data_ptr() + off)
+    rs.reshard_execute(plan, sptr, dsts)
+    torch.cuda.synchronize()
+    for r, (o, s) in enumerate(dboxes):
+        assert torch.equal(dsts[r].reshape(-1).view(torch.uint8),
+                           helpers.slice_box(glob, o, s).reshape(-1).view(torch.uint8)), r
+    assert rs.reshard_device_status() == 0

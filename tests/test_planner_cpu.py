@@ -190,3 +190,105 @@ def test_empty_and_degenerate_layouts(oracle):
                  _case((5, 1), "bf16", (1, 1), ("R", "S1"), (1,), ("R",), 3),
                  _case((1, 1, 1), "u8", (2, 2), ("S0", "S2"), (3,), ("S1",), 4)):
         _check_spec(oracle, spec)
+
+
+# ------------------------------------------------------------------------------ in place
+def _inplace_cpu(oracle, spec, alias):
+    glob = global_tensor(spec)
+    sboxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+    dboxes = oracle.boxes(spec.global_shape, spec.dst_mesh, spec.dst_placements)
+    srcs = [helpers.to_bytes(helpers.slice_box(glob, o, s)) for o, s in sboxes]
+    want = helpers.expected_dst(oracle, spec, srcs)
+    plan = rs.reshard_plan_create_inplace(spec.global_shape, spec.dtype, spec.src_mesh,
+                                          spec.src_placements, spec.dst_mesh,
+                                          spec.dst_placements, alias)
+    M = spec.n_src
+    for program in (rs.PROGRAM_FANOUT, rs.PROGRAM_BOXCOPY):
+        dsts = [np.full(w.size, 0xA5, dtype=np.uint8) for w in want]
+        views = []
+        for s, a in enumerate(alias):
+            d, off = rs.reshard_plan_alias(plan, s)
+            if a >= 0 and srcs[s].size:
+                assert d == a and off == helpers.alias_offset_bytes(sboxes[s], dboxes[a],
+                                                                    spec.elem_bytes)
+                v = dsts[a][off:off + srcs[s].size]
+                v[:] = srcs[s]
+                views.append(v)
+            else:
+                views.append(srcs[s].copy())
+        bufs = views + dsts + [np.zeros(0, dtype=np.uint8)]
+        writes = helpers.run_program_cpu(plan, program, bufs)
+        for r, w in enumerate(want):
+            assert np.array_equal(dsts[r], w), (spec, program, r)
+            assert (writes[M + r] <= 1).all()
+        # no copy writes a byte that is a source of the same execution
+        for s, a in enumerate(alias):
+            if a >= 0 and srcs[s].size:
+                _, off = rs.reshard_plan_alias(plan, s)
+                assert not writes[M + a][off:off + srcs[s].size].any()
+    st = rs.reshard_plan_stats(plan)
+    assert st["fanout_write_bytes"] + st["inplace_bytes"] == st["dst_bytes"]
+    return st
+
+
+def test_inplace_hybridflow(oracle):
+    """Strided generation ranks: every training shard is already inside its rank's
+    generation shard, so a quarter of the destination bytes are never written."""
+    for spec in workload(3, reduced=False).tensors[:1] + (
+            TensorSpec("hf", (64, 24), "bf16", (8,), ("S0",), (2, 4), ("S0", "R"),
+                       init=("bits",), seed=3),):
+        if spec.numel > 1 << 22:
+            plan = rs.reshard_plan_create_inplace(spec.global_shape, spec.dtype, spec.src_mesh,
+                                                  spec.src_placements, spec.dst_mesh,
+                                                  spec.dst_placements, list(range(8)))
+            st = rs.reshard_plan_stats(plan)
+            assert st["inplace_bytes"] == spec.global_bytes
+            assert st["fanout_write_bytes"] == 3 * spec.global_bytes
+            continue
+        st = _inplace_cpu(oracle, spec, list(range(8)))
+        assert st["inplace_bytes"] == spec.global_bytes
+
+
+def test_inplace_random_layouts(oracle):
+    rng = random.Random(23)
+    done = 0
+    for i in range(400):
+        nd = rng.choice((1, 2, 3))
+        gshape = tuple(rng.randint(1, 9) for _ in range(nd))
+        sm = tuple(rng.randint(1, 4) for _ in range(rng.randint(1, 2)))
+        dm = tuple(rng.randint(1, 4) for _ in range(rng.randint(1, 2)))
+        sp = tuple(rng.choice(["R"] + [f"S{d}" for d in range(nd)]) for _ in sm)
+        dp = tuple(rng.choice(["R"] + [f"S{d}" for d in range(nd)]) for _ in dm)
+        spec = _case(gshape, "bf16", sm, sp, dm, dp, seed=i)
+        alias = helpers.pick_aliases(oracle, spec, rng)
+        if all(a < 0 for a in alias):
+            continue
+        _inplace_cpu(oracle, spec, alias)
+        done += 1
+    assert done > 50
+
+
+def test_inplace_rejects_impossible_aliases():
+    # source rank 0 (rows 0-3) is not inside destination rank 1 (rows 4-7)
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_plan_create_inplace((8, 8), "bf16", (2,), ("S0",), (2,), ("S0",), [1, -1])
+    assert e.value.status == 3
+    # a 4x4 corner inside the full 8x8 matrix: inside, but not one contiguous range
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_plan_create_inplace((8, 8), "bf16", (2, 2), ("S0", "S1"), (1,), ("R",),
+                                       [0, -1, -1, -1])
+    assert e.value.status == 3
+    with pytest.raises(rs.ReshardError):
+        rs.reshard_plan_create_inplace((8, 8), "bf16", (2,), ("S0",), (2,), ("S0",), [5, -1])
+
+
+def test_inplace_execute_requires_aliased_pointers():
+    import ctypes
+    plan = rs.reshard_plan_create_inplace((8, 8), "bf16", (2,), ("S0",), (2, 2), ("S0", "R"),
+                                          [0, 2])
+    dsts = [0x10000, 0x20000, 0x30000, 0x40000]
+    # source 1 sits inside destination 2 at its offset; source 0 points elsewhere
+    srcs = [0x90000, 0x30000 + rs.reshard_plan_alias(plan, 1)[1]]
+    rc = rs._lib.reshard_execute(plan, rs._ptr_array(srcs), rs._ptr_array(dsts), None)
+    assert rc == 1 and "in-place" in rs.reshard_last_error()
+    del ctypes
