@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=("moe_refit", "hybridflow", "ffn_up"),
                     default="moe_refit")
     ap.add_argument("--kernel", choices=("fanout", "boxcopy"), default="fanout")
+    ap.add_argument("--batch", action="store_true",
+                    help="launch all reshard tensors as one batch (measured: no gain on GB300)")
     ap.add_argument("--reshard-only", action="store_true",
                     help="leave out the gather-and-broadcast tensors (profiling captures)")
     ap.add_argument("--experts", type=int, default=256,
@@ -287,17 +289,34 @@ def oracle_sample(jobs, seconds):
 
 
 # ------------------------------------------------------------------------------ timing
-def device_time(jobs, stream, steps, warmup, kernel, dist_ctx, gpu_uuid):
-    """Device-timed steps; returns (ms_per_step, dominant kernel avg ms, clocks)."""
+def make_step(jobs, kernel, batch):
+    """The step as a list of (is_dominant, callable) launches on a stream."""
+    import dtensor_reshard_gb300 as rs
+    ops = []
+    rjobs = [j for j in jobs if j.spec.path == "reshard"]
+    if batch is not None and rjobs:
+        ops.append((True, lambda st: rs.reshard_batch_execute(
+            batch, [j.srcs for j in rjobs], [j.dsts for j in rjobs], st)))
+    else:
+        for j in rjobs:
+            ops.append((True, lambda st, j=j: run_job(j, st, kernel)))
+    for j in jobs:
+        if j.spec.path != "reshard":
+            ops.append((False, lambda st, j=j: run_job(j, st, kernel)))
+    return ops
+
+
+def device_time(ops, stream, steps, warmup, dist_ctx, gpu_uuid):
+    """Device-timed steps; returns (ms_per_step, dominant launch times in ms, clocks)."""
     import torch
 
     for _ in range(warmup):
-        for j in jobs:
-            run_job(j, stream, kernel)
+        for _, fn in ops:
+            fn(stream)
     torch.cuda.synchronize()
-    dom = [j for j in jobs if j.spec.path == "reshard"]
+    ndom = sum(1 for d, _ in ops if d)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps * len(dom))]
+          for _ in range(steps * ndom)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_uuid)
@@ -307,14 +326,14 @@ def device_time(jobs, stream, steps, warmup, kernel, dist_ctx, gpu_uuid):
     start.record(stream)
     e = 0
     for _ in range(steps):
-        for j in jobs:
-            if j.spec.path == "reshard":
+        for dom, fn in ops:
+            if dom:
                 ev[e][0].record(stream)
-                run_job(j, stream, kernel)
+                fn(stream)
                 ev[e][1].record(stream)
                 e += 1
             else:
-                run_job(j, stream, kernel)
+                fn(stream)
     end.record(stream)
     torch.cuda.synchronize()
     dist_ctx.barrier()
@@ -476,21 +495,24 @@ def ours_arm(args, rank, world, local):
     setup_s = time.perf_counter() - t0
     stream = torch.cuda.current_stream(dev)
 
-    ms_step, dom_ms, clocks = device_time(jobs, stream, args.steps, args.warmup, kernel, dctx,
-                                          gpu_uuid)
+    dom_jobs = [j for j in jobs if j.spec.path == "reshard"]
+    batch = None
+    if args.batch and kernel == rs.KERNEL_FANOUT and len(dom_jobs) > 1:
+        batch = rs.reshard_batch_create([j.plan for j in dom_jobs])
+    ops = make_step(jobs, kernel, batch)
+    ms_step, dom_ms, clocks = device_time(ops, stream, args.steps, args.warmup, dctx, gpu_uuid)
     ms_step_max = dctx.max(ms_step)
     eff_bytes = sum(j.effective_bytes for j in jobs)
     total_bytes = dctx.sum(eff_bytes)
     value = total_bytes / (ms_step_max * 1e-3) / 1e9
 
     peak, peak_kind = load_peaks()
-    dom_jobs = [j for j in jobs if j.spec.path == "reshard"]
     dom_bytes = sum((j.stats["fanout_read_bytes"] + j.stats["fanout_write_bytes"])
                     if kernel == rs.KERNEL_FANOUT else
                     (j.stats["boxcopy_read_bytes"] + j.stats["boxcopy_write_bytes"])
                     for j in dom_jobs)
     dom_launch_ms = sum(dom_ms) / len(dom_ms)
-    dom_bytes_per_launch = dom_bytes / len(dom_jobs)
+    dom_bytes_per_launch = dom_bytes / (1 if batch is not None else len(dom_jobs))
     achieved = dom_bytes_per_launch / (dom_launch_ms * 1e-3) / 1e9
     traffic = load_profile_traffic()
     traffic_val = None
@@ -514,7 +536,9 @@ def ours_arm(args, rank, world, local):
             cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                    "sample": desc, "seconds": round(secs, 2)}
 
-    launches = args.steps * sum(launches_of(j, kernel) for j in jobs)
+    launches = args.steps * (sum(launches_of(j, kernel) for j in jobs if j.spec.path != "reshard")
+                             + (1 if batch is not None else
+                                sum(launches_of(j, kernel) for j in dom_jobs)))
     st_tot = {k: sum(j.stats[k] for j in jobs) for k in (
         "global_bytes", "dst_bytes", "src_bytes", "fanout_read_bytes", "fanout_write_bytes",
         "boxcopy_read_bytes", "boxcopy_write_bytes", "gb_read_bytes", "gb_write_bytes")}
@@ -529,6 +553,8 @@ def ours_arm(args, rank, world, local):
         "config": {
             "workload": w.name, "tensors": len(jobs),
             "reshard_kernel": args.kernel,
+            "reshard_launch": "one batch launch for all reshard tensors" if batch is not None
+                              else "one launch per tensor",
             "step": "%d tensors via reshard_execute + %d via gather_broadcast_execute" % (
                 len(dom_jobs), len(jobs) - len(dom_jobs)),
             "global_bytes_per_step": st_tot["global_bytes"],
@@ -541,7 +567,8 @@ def ours_arm(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic_val, "peak_kind": peak_kind,
-                     "kernel": "fanout_staged_kernel (TMA bulk copies, fan-out)",
+                     "kernel": "fanout_staged_kernel (TMA bulk copies, fan-out)"
+                               + (", whole batch per launch" if batch is not None else ""),
                      "algorithmic_bytes_per_launch": int(dom_bytes_per_launch),
                      "avg_launch_ms": round(dom_launch_ms, 4)},
         "bytes_vs_gather_broadcast": {
@@ -687,7 +714,26 @@ def report(args):
             for j in jobs:
                 rs.gather_broadcast_execute(j.plan, j.srcs, j.dsts, scratch, gmax, stream)
 
+        batches = []
+        if len(jobs) > 1:
+            # one launch per batch; batches split where the rank count would overflow a launch
+            cur, nb = [], 0
+            for j in jobs:
+                n = j.plan.n_src + j.plan.n_dst
+                if cur and nb + n + 1 > rs.MAX_EXEC_BUFFERS:
+                    batches.append(cur)
+                    cur, nb = [], 0
+                cur.append(j)
+                nb += n
+            batches.append(cur)
+            batches = [(rs.reshard_batch_create([j.plan for j in b]), b) for b in batches]
+
+        def k2b():
+            for bt, b in batches:
+                rs.reshard_batch_execute(bt, [j.srcs for j in b], [j.dsts for j in b], stream)
+
         t2, t1, tg = timed(k2, reps, flush), timed(k1, reps, flush), timed(gb, reps, flush)
+        t2b = timed(k2b, reps, flush) if batches else None
         b2 = sum(j.stats["fanout_read_bytes"] + j.stats["fanout_write_bytes"] for j in jobs)
         b1 = sum(j.stats["boxcopy_read_bytes"] + j.stats["boxcopy_write_bytes"] for j in jobs)
         bg = sum(j.stats["gb_read_bytes"] + j.stats["gb_write_bytes"] for j in jobs)
@@ -695,6 +741,8 @@ def report(args):
             "workload": w.name, "tensors": len(jobs), "G": G, "D": D,
             "l2_flush": flush,
             "fanout_ms": round(t2, 4), "boxcopy_ms": round(t1, 4),
+            "fanout_batched_ms": round(t2b, 4) if t2b else None,
+            "fanout_batched_roofline_frac": round(b2 / t2b / 1e6 / peak, 4) if t2b else None,
             "gather_broadcast_ms": round(tg, 4),
             "effective_GBps": round((G + D) / t2 / 1e6, 1),
             "fanout_hbm_GBps": round(b2 / t2 / 1e6, 1),
@@ -710,7 +758,7 @@ def report(args):
         }
         rows.append(row)
         print(json.dumps(row), file=sys.stderr)
-        del jobs, scratch
+        del jobs, scratch, batches
         torch.cuda.empty_cache()
     rows.append(report_inplace(dev, timed, peak))
     print(json.dumps(rows[-1]), file=sys.stderr)

@@ -105,6 +105,10 @@ def _load():
                                          ctypes.POINTER(reshard_placement_t), i64p, vpp],
                                         ctypes.c_int),
         "reshard_plan_alias": ([vp, ctypes.c_int64, i64p, i64p], ctypes.c_int),
+        "reshard_batch_create": ([ctypes.POINTER(vp), ctypes.c_int32, vpp], ctypes.c_int),
+        "reshard_batch_execute": ([vp, ctypes.POINTER(vpp), ctypes.POINTER(vpp), vp],
+                                  ctypes.c_int),
+        "reshard_batch_destroy": ([vp], ctypes.c_int),
         "reshard_plan_upload": ([vp], ctypes.c_int),
         "reshard_execute": ([vp, vpp, vpp, vp], ctypes.c_int),
         "reshard_execute_ex": ([vp, vpp, vpp, ctypes.c_int32, vp], ctypes.c_int),
@@ -271,6 +275,55 @@ def reshard_plan_alias(plan: Plan, src_rank: int):
     _check(_lib.reshard_plan_alias(plan, int(src_rank), ctypes.byref(d), ctypes.byref(o)),
            "reshard_plan_alias")
     return d.value, o.value
+
+
+class Batch:
+    """Owning wrapper of a reshard_batch_t (keeps its plans alive)."""
+
+    def __init__(self, handle: int, plans):
+        self.handle = handle
+        self.plans = list(plans)
+
+    @property
+    def _as_parameter_(self):
+        if not self.handle:
+            raise ReshardError(6, "batch", "batch already destroyed")
+        return ctypes.c_void_p(self.handle)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            try:
+                _lib.reshard_batch_destroy(ctypes.c_void_p(h))
+            except Exception:  # noqa: BLE001 - interpreter shutdown
+                pass
+            self.handle = None
+
+
+def reshard_batch_create(plans) -> Batch:
+    arr = (ctypes.c_void_p * len(plans))(*[p.handle for p in plans])
+    h = ctypes.c_void_p()
+    _check(_lib.reshard_batch_create(arr, len(plans), ctypes.byref(h)), "reshard_batch_create")
+    return Batch(h.value, plans)
+
+
+def reshard_batch_execute(batch: Batch, src_ptrs_per_plan, dst_ptrs_per_plan, stream=None):
+    """src_ptrs_per_plan[i] / dst_ptrs_per_plan[i]: plan i's pointer lists."""
+    srcs = [_ptr_array(x) for x in src_ptrs_per_plan]
+    dsts = [_ptr_array(x) for x in dst_ptrs_per_plan]
+    sa = (ctypes.POINTER(ctypes.c_void_p) * len(srcs))(
+        *[ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)) for a in srcs])
+    da = (ctypes.POINTER(ctypes.c_void_p) * len(dsts))(
+        *[ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)) for a in dsts])
+    _check(_lib.reshard_batch_execute(batch, sa, da, _stream(stream)), "reshard_batch_execute")
+
+
+def reshard_batch_destroy(batch: Batch):
+    if not batch.handle:
+        raise ReshardError(6, "reshard_batch_destroy", "batch already destroyed")
+    st = _lib.reshard_batch_destroy(batch)
+    batch.handle = None
+    _check(st, "reshard_batch_destroy")
 
 
 def reshard_plan_upload(plan: Plan):

@@ -103,6 +103,13 @@ struct reshard_plan_s {
 
 namespace rs {
 
+// Host side shared by the plan and batch entry points (planner.cpp).
+reshard_status_t upload_plan(reshard_plan_s* plan);
+reshard_status_t buffer_table(reshard_plan_s* plan, const void* const* src_ptrs,
+                              void* const* dst_ptrs, void* scratch,
+                              std::vector<unsigned char*>* bufs);
+bool plan_live(const reshard_plan_s* plan);
+
 // Error reporting (thread-local message).
 reshard_status_t fail(reshard_status_t st, const std::string& msg);
 

@@ -493,6 +493,8 @@ reshard_status_t build_plan(reshard_plan_s* P) {
 
 }  // namespace
 
+bool plan_live(const reshard_plan_s* plan) { return live(plan); }
+
 reshard_status_t fail(reshard_status_t st, const std::string& msg) {
   g_last_error = msg;
   return st;
@@ -660,6 +662,14 @@ reshard_status_t reshard_plan_destroy(reshard_plan_t plan) {
 
 reshard_status_t reshard_plan_upload(reshard_plan_t plan) {
   if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  return rs::upload_plan(plan);
+}
+
+}  // extern "C"
+
+namespace rs {
+
+reshard_status_t upload_plan(reshard_plan_s* plan) {
   int dev = -1;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
@@ -724,9 +734,10 @@ reshard_status_t reshard_plan_upload(reshard_plan_t plan) {
   return RESHARD_OK;
 }
 
-}  // extern "C"
+}  // namespace rs
 
-namespace {
+
+namespace rs {
 
 // Build the buffer table [src..., dst..., scratch] and check null pointers.
 reshard_status_t buffer_table(reshard_plan_t plan, const void* const* src_ptrs,
@@ -763,7 +774,7 @@ reshard_status_t buffer_table(reshard_plan_t plan, const void* const* src_ptrs,
   return RESHARD_OK;
 }
 
-}  // namespace
+}  // namespace rs
 
 extern "C" {
 
@@ -773,7 +784,7 @@ reshard_status_t reshard_execute_ex(reshard_plan_t plan, const void* const* src_
   if (kernel != RESHARD_KERNEL_FANOUT && kernel != RESHARD_KERNEL_BOXCOPY)
     return fail(RESHARD_ERR_INVALID_ARG, "unknown kernel");
   std::vector<unsigned char*> bufs;
-  reshard_status_t st = buffer_table(plan, src_ptrs, dst_ptrs, nullptr, &bufs);
+  reshard_status_t st = rs::buffer_table(plan, src_ptrs, dst_ptrs, nullptr, &bufs);
   if (st != RESHARD_OK) return st;
   st = reshard_plan_upload(plan);
   if (st != RESHARD_OK) return st;
@@ -797,7 +808,7 @@ reshard_status_t gather_broadcast_execute(reshard_plan_t plan, const void* const
       return fail(RESHARD_ERR_INVALID_ARG, "full_scratch is smaller than the global tensor");
   }
   std::vector<unsigned char*> bufs;
-  reshard_status_t st = buffer_table(plan, src_ptrs, dst_ptrs, full_scratch, &bufs);
+  reshard_status_t st = rs::buffer_table(plan, src_ptrs, dst_ptrs, full_scratch, &bufs);
   if (st != RESHARD_OK) return st;
   st = reshard_plan_upload(plan);
   if (st != RESHARD_OK) return st;

@@ -99,6 +99,7 @@ typedef struct reshard_mesh {
 } reshard_mesh_t;
 
 typedef struct reshard_plan_s* reshard_plan_t;
+typedef struct reshard_batch_s* reshard_batch_t;
 
 /* Which copy kernel an execution uses. */
 typedef enum reshard_kernel {
@@ -324,6 +325,38 @@ reshard_status_t reshard_selftest_wait_timeout(uint32_t polls, void* stream);
  */
 reshard_status_t gather_broadcast_execute_static(reshard_plan_t plan, const void* const* src_ptrs,
                                                  void* const* dst_ptrs, void* stream);
+
+/*
+ * Whole-model batching: the fan-out reshards of several plans (e.g. every
+ * feed-forward weight of a model) as ONE kernel launch.  The plans' copy
+ * descriptors are concatenated over a combined buffer table, so the work is
+ * spread evenly over the GPU with no launch boundary between tensors.  The
+ * pages route the feed-forward projections (most of the parameters) through
+ * the Reshard collective and the small irregular weights through
+ * gather-and-broadcast (news.bpdata.com, section "Integracio es hibrid megoldas
+ * a NeMo RL-ben"); a batch is the unit for the first group.
+ *
+ * reshard_batch_create: plans[nplans] stay owned by the caller and must outlive
+ * the batch (executions check them).  The sum over plans of M + N must be below
+ * RESHARD_MAX_EXEC_BUFFERS (else UNSUPPORTED: split the model into several
+ * batches).  Errors: INVALID_ARG, BAD_HANDLE, UNSUPPORTED, NO_MEMORY.
+ */
+reshard_status_t reshard_batch_create(const reshard_plan_t* plans, int32_t nplans,
+                                      reshard_batch_t* out_batch);
+
+/*
+ * Execute every plan of the batch: src_ptrs[i] and dst_ptrs[i] are plan i's
+ * pointer arrays, exactly as for reshard_execute (in-place plans included).
+ * When every copy can use 16-byte accesses with these buffers the batch is one
+ * launch of the fan-out kernel (its descriptor tables are uploaded on first use,
+ * like a plan's); otherwise each plan is executed in turn with its own kernel.
+ * Errors: as reshard_execute.
+ */
+reshard_status_t reshard_batch_execute(reshard_batch_t batch, const void* const* const* src_ptrs,
+                                       void* const* const* dst_ptrs, void* stream);
+
+/* Release a batch (not its plans).  Errors: BAD_HANDLE. */
+reshard_status_t reshard_batch_destroy(reshard_batch_t batch);
 
 /*
  * Local box of one rank (news.bpdata.com, section "A megkozelites": the DTensor

@@ -143,3 +143,28 @@ def test_stats_of_the_large_workloads():
 
 def test_version_string():
     assert "sm_103a" in rs.reshard_version()
+
+
+def test_batch_host_checks():
+    import ctypes as C
+    a = rs.reshard_plan_create((8, 8), "bf16", (2,), ("S0",), (4,), ("S1",))
+    b = rs.reshard_plan_create((16,), "fp32", (4,), ("S0",), (2,), ("S0",))
+    batch = rs.reshard_batch_create([a, b])
+    # a plan destroyed behind the batch's back is detected before any device work
+    rs.reshard_plan_destroy(b)
+    sa = (C.POINTER(C.c_void_p) * 2)(C.cast(rs._ptr_array([1, 2]), C.POINTER(C.c_void_p)),
+                                      C.cast(rs._ptr_array([1] * 4), C.POINTER(C.c_void_p)))
+    da = (C.POINTER(C.c_void_p) * 2)(C.cast(rs._ptr_array([3] * 4), C.POINTER(C.c_void_p)),
+                                      C.cast(rs._ptr_array([4, 5]), C.POINTER(C.c_void_p)))
+    assert rs._lib.reshard_batch_execute(batch, sa, da, None) == 6
+    rs.reshard_batch_destroy(batch)
+    assert rs._lib.reshard_batch_destroy(C.c_void_p(0)) == 6
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_batch_create([b])
+    assert e.value.status == 6
+    # too many ranks for one launch
+    big = [rs.reshard_plan_create((4096,), "fp32", (256,), ("S0",), (256,), ("S0",))
+           for _ in range(2)]
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_batch_create(big)
+    assert e.value.status == 2

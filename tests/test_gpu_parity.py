@@ -386,3 +386,65 @@ def test_full_hybridflow_layer_inplace(oracle):
         assert torch.equal(dsts[r].reshape(-1).view(torch.uint8),
                            helpers.slice_box(glob, o, s).reshape(-1).view(torch.uint8)), r
     assert rs.reshard_device_status() == 0
+
+
+# ---------------------------------------------------------------------- batches
+def _batch_case(oracle, specs, misalign=0):
+    plans, sptrs, dptrs, want, keep = [], [], [], [], []
+    for spec in specs:
+        glob = global_tensor(spec)
+        srcs = [helpers.to_bytes(s) for s in helpers.scatter_with_oracle(
+            oracle, glob, spec.src_mesh, spec.src_placements)]
+        w = helpers.expected_dst(oracle, spec, srcs)
+        ds = _upload(srcs, misalign)
+        dd = [Guarded(x.size, misalign) for x in w]
+        plans.append(helpers.spec_plan(spec))
+        sptrs.append([g.ptr for g in ds])
+        dptrs.append([g.ptr for g in dd])
+        want.append(w)
+        keep.append((ds, dd))
+    return plans, sptrs, dptrs, want, keep
+
+
+@pytest.mark.parametrize("misalign", [0, 2])
+def test_batch_of_plans(oracle, misalign):
+    """One launch for several tensors (aligned), or one plan at a time (misaligned)."""
+    specs = list(workload(3, reduced=True).tensors) + list(
+        t for t in workload(5, reduced=True).tensors if t.path == "reshard")
+    plans, sptrs, dptrs, want, keep = _batch_case(oracle, specs, misalign)
+    batch = rs.reshard_batch_create(plans)
+    for _ in range(2):
+        rs.reshard_batch_execute(batch, sptrs, dptrs)
+    torch.cuda.synchronize()
+    for (ds, dd), w in zip(keep, want):
+        for g, x in zip(dd, w):
+            assert np.array_equal(g.payload().cpu().numpy(), x)
+            assert g.guards_intact()
+    assert rs.reshard_device_status() == 0
+
+
+def test_batch_with_inplace_plan(oracle):
+    spec = TensorSpec("hf", (2048, 264), "bf16", (8,), ("S0",), (2, 4), ("S0", "R"),
+                      init=("bits",), seed=77)
+    glob = global_tensor(spec)
+    sboxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+    srcs = [helpers.to_bytes(helpers.slice_box(glob, o, s)) for o, s in sboxes]
+    want = helpers.expected_dst(oracle, spec, srcs)
+    p_in = rs.reshard_plan_create_inplace(spec.global_shape, spec.dtype, spec.src_mesh,
+                                          spec.src_placements, spec.dst_mesh,
+                                          spec.dst_placements, list(range(8)))
+    dd = [Guarded(x.size) for x in want]
+    sp = []
+    for s in range(8):
+        d, off = rs.reshard_plan_alias(p_in, s)
+        dd[d].payload()[off:off + srcs[s].size].copy_(torch.from_numpy(srcs[s]).cuda())
+        sp.append(dd[d].ptr + off)
+    other = workload(2, reduced=True).tensors[0]
+    plans2, sptrs2, dptrs2, want2, keep2 = _batch_case(oracle, [other])
+    batch = rs.reshard_batch_create([p_in] + plans2)
+    rs.reshard_batch_execute(batch, [sp] + sptrs2, [[g.ptr for g in dd]] + dptrs2)
+    torch.cuda.synchronize()
+    for g, x in zip(dd, want):
+        assert np.array_equal(g.payload().cpu().numpy(), x)
+    for g, x in zip(keep2[0][1], want2[0]):
+        assert np.array_equal(g.payload().cpu().numpy(), x)
