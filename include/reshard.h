@@ -231,7 +231,10 @@ reshard_status_t reshard_plan_upload(reshard_plan_t plan);
  *
  * src_ptrs[M]  device pointers of the source shards (NULL allowed only for an
  *              empty shard).  dst_ptrs[N] likewise for the destinations.
- * Destination buffers must not overlap each other or any source buffer.
+ * Destination buffers must not overlap each other or any source buffer
+ * (except as declared for in-place plans).  Once the plan is uploaded and one
+ * execution has run on the device, executions can be recorded into a CUDA graph
+ * by stream capture and replayed; the graph keeps the buffer addresses.
  * Errors: BAD_HANDLE, INVALID_ARG (null pointer for a non-empty shard),
  * UNSUPPORTED (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS), CUDA (launch failed).
  */

@@ -448,3 +448,56 @@ def test_batch_with_inplace_plan(oracle):
         assert np.array_equal(g.payload().cpu().numpy(), x)
     for g, x in zip(keep2[0][1], want2[0]):
         assert np.array_equal(g.payload().cpu().numpy(), x)
+
+
+# ---------------------------------------------------------------------- CUDA graphs
+def test_cuda_graph_capture_and_replay(oracle):
+    """A refit step recorded once into a CUDA graph replays exactly, and picks up new source
+    values written into the same buffers (plans uploaded and kernels warmed up first)."""
+    dev = _cuda()
+    specs = list(workload(3, reduced=True).tensors[:3]) + [
+        t for t in workload(5, reduced=True).tensors if t.path == "reshard"]
+    cases = []
+    for spec in specs:
+        plan = helpers.spec_plan(spec)
+        rs.reshard_plan_upload(plan)
+        boxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+        srcs = [torch.empty(s, dtype=torch.bfloat16, device=dev) for _, s in boxes]
+        dboxes = oracle.boxes(spec.global_shape, spec.dst_mesh, spec.dst_placements)
+        dsts = [torch.empty(s, dtype=torch.bfloat16, device=dev) for _, s in dboxes]
+        cases.append((spec, plan, boxes, srcs, dsts))
+
+    def load(seed_shift):
+        wants = []
+        for spec, plan, boxes, srcs, dsts in cases:
+            sp = TensorSpec(spec.name, spec.global_shape, spec.dtype, spec.src_mesh,
+                            spec.src_placements, spec.dst_mesh, spec.dst_placements,
+                            init=("bits",), seed=spec.seed + seed_shift)
+            glob = global_tensor(sp)
+            host = [helpers.slice_box(glob, o, s) for o, s in boxes]
+            for d, h in zip(srcs, host):
+                d.copy_(h)
+            wants.append(helpers.expected_dst(oracle, sp, [helpers.to_bytes(h) for h in host]))
+            for d in dsts:
+                d.view(-1).view(torch.uint8).fill_(FILL_BYTE)
+        torch.cuda.synchronize()
+        return wants
+
+    def step(stream):
+        for spec, plan, boxes, srcs, dsts in cases:
+            rs.reshard_execute(plan, srcs, dsts, stream)
+
+    wants = load(0)
+    step(torch.cuda.current_stream())          # warm-up: first launches outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(torch.cuda.current_stream())
+    for shift in (0, 1000):
+        wants = load(shift)
+        graph.replay()
+        torch.cuda.synchronize()
+        for (spec, plan, boxes, srcs, dsts), want in zip(cases, wants):
+            for d, w in zip(dsts, want):
+                assert np.array_equal(helpers.to_bytes(d), w), (spec.name, shift)
+    assert rs.reshard_device_status() == 0
