@@ -78,6 +78,22 @@ class reshard_tile_t(ctypes.Structure):
 assert ctypes.sizeof(reshard_tile_t) == 64
 
 
+class reshard_tblock_t(ctypes.Structure):
+    _fields_ = [("wide_off", ctypes.c_int64), ("row_bytes", ctypes.c_uint32),
+                ("nrows", ctypes.c_uint32), ("seg_begin", ctypes.c_uint32),
+                ("seg_count", ctypes.c_uint32), ("wide", ctypes.c_uint16),
+                ("direction", ctypes.c_uint16), ("pad", ctypes.c_uint32)]
+
+
+class reshard_tseg_t(ctypes.Structure):
+    _fields_ = [("narrow_off", ctypes.c_int64), ("width", ctypes.c_uint32),
+                ("col", ctypes.c_uint32), ("narrow", ctypes.c_uint16), ("pad16", ctypes.c_uint16),
+                ("pad32", ctypes.c_uint32)]
+
+
+assert ctypes.sizeof(reshard_tblock_t) == 32 and ctypes.sizeof(reshard_tseg_t) == 24
+
+
 class ReshardError(RuntimeError):
     def __init__(self, status: int, where: str, msg: str):
         super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}")
@@ -126,6 +142,10 @@ def _load():
                                   ctypes.POINTER(ctypes.POINTER(ctypes.c_uint16)), i64p],
                                  ctypes.c_int),
         "reshard_tile_units": ([ctypes.POINTER(reshard_tile_t)], ctypes.c_int64),
+        "reshard_plan_transposes": ([vp, ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.POINTER(reshard_tblock_t)), i64p,
+                                     ctypes.POINTER(ctypes.POINTER(reshard_tseg_t)), i64p],
+                                    ctypes.c_int),
         "reshard_plan_destroy": ([vp], ctypes.c_int),
         "reshard_last_error": ([], ctypes.c_char_p),
         "reshard_version": ([], ctypes.c_char_p),
@@ -404,6 +424,20 @@ def reshard_plan_program(plan: Plan, program: int):
     goff = [go[i] for i in range(g + 1)]
     gbuf = [gb[i] for i in range(goff[-1])] if g >= 0 and goff else []
     return tiles, prefix, goff, gbuf
+
+
+def reshard_plan_transposes(plan: Plan, program: int):
+    """(blocks, segments) of a program's transpose blocks, copied to Python dicts."""
+    bp = ctypes.POINTER(reshard_tblock_t)()
+    nb = ctypes.c_int64()
+    sp = ctypes.POINTER(reshard_tseg_t)()
+    ns = ctypes.c_int64()
+    _check(_lib.reshard_plan_transposes(plan, int(program), ctypes.byref(bp), ctypes.byref(nb),
+                                        ctypes.byref(sp), ctypes.byref(ns)),
+           "reshard_plan_transposes")
+    blocks = [{f: getattr(bp[i], f) for f, _ in reshard_tblock_t._fields_} for i in range(nb.value)]
+    segs = [{f: getattr(sp[i], f) for f, _ in reshard_tseg_t._fields_} for i in range(ns.value)]
+    return blocks, segs
 
 
 def reshard_tile_units(tile: dict) -> int:

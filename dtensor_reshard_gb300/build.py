@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(PKG, "libreshard.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["planner.cpp", "batch.cpp", "kernels.cu", "bulk_fanout.cu", "static_scratch.cu"]
+SOURCES = ["planner.cpp", "batch.cpp", "kernels.cu", "bulk_fanout.cu", "transpose.cu",
+           "static_scratch.cu"]
 
 
 def nvcc() -> str:

@@ -81,6 +81,20 @@ reshard_status_t reshard_batch_create(const reshard_plan_t* plans, int32_t nplan
         t.dst_group = uint16_t(gbase + t.dst_group);
         C.tiles.push_back(t);
       }
+      const uint32_t sbase = uint32_t(C.tsegs.size());
+      for (reshard_tblock_t b : F.tblocks) {
+        b.wide = uint16_t(b.direction == 0 ? gbase + b.wide : base + b.wide);
+        b.seg_begin += sbase;
+        C.tblocks.push_back(b);
+      }
+      for (size_t k = 0; k < F.tblocks.size(); ++k) {
+        const reshard_tblock_t& b = F.tblocks[k];
+        for (uint32_t j = b.seg_begin; j < b.seg_begin + b.seg_count; ++j) {
+          reshard_tseg_t sg = F.tsegs[j];
+          sg.narrow = uint16_t(b.direction == 0 ? base + sg.narrow : gbase + sg.narrow);
+          C.tsegs.push_back(sg);
+        }
+      }
       C.align_bits |= F.align_bits;
       C.has_planes = C.has_planes || F.has_planes;
       C.max_fanout = std::max(C.max_fanout, F.max_fanout);

@@ -78,7 +78,23 @@ struct Program {
   int64_t tile_bytes = 0;   // source bytes of all tiles
   int64_t long_row_bytes = 0;  // ... of those in rows of at least 512 bytes (runs included)
   int64_t total_units() const { return prefix.empty() ? 0 : prefix.back(); }
+  // transpose blocks (narrow innermost pieces grouped by shared rows)
+  std::vector<reshard_tblock_t> tblocks;
+  std::vector<reshard_tseg_t> tsegs;
+  const reshard_tblock_t* d_tblocks = nullptr;
+  const reshard_tseg_t* d_tsegs = nullptr;
 };
+
+// Narrow pieces (bytes per row) below this go through transpose blocks, and a
+// block holds at most this many bytes of wide rows in shared memory.
+constexpr int64_t kTransposeMaxWidth = 64;
+constexpr int64_t kTransposeBlockBytes = 32 * 1024;
+// Blocks a transpose group aims for (smaller blocks when the group is small).
+constexpr int64_t kTransposeMinBlocks = 512;
+// Most segments one transpose group may have (the kernel stages them in shared memory).
+constexpr int64_t kTransposeMaxSegs = 128;
+// Most narrow replica pointers one scatter block may address.
+constexpr int64_t kTransposeMaxReplicaPtrs = 1024;
 
 }  // namespace rs
 
@@ -125,6 +141,10 @@ reshard_status_t launch_program_tables(const Program& p, const reshard_tile_t* d
 // TMA-staged fan-out (bulk_fanout.cu) for a 16-byte-aligned program.
 reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelParams& kp,
                                       void* stream);
+// Transpose blocks of a program (transpose.cu); no-op when it has none.
+reshard_status_t launch_transposes(const reshard_plan_s* plan, const Program& prog,
+                                   unsigned char* const* bufs, int nbufs, uint32_t flags,
+                                   void* stream);
 // Occupancy of the copy kernel on the current device (blocks per SM).
 reshard_status_t copy_kernel_occupancy(int* blocks_per_sm);
 

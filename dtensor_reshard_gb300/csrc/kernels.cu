@@ -455,7 +455,7 @@ reshard_status_t copy_kernel_occupancy(int* blocks_per_sm) {
   return occupancy(dev, 4, 0, blocks_per_sm);
 }
 
-reshard_status_t launch_program(const reshard_plan_s* plan, const Program& prog,
+static reshard_status_t launch_tiles(const reshard_plan_s* plan, const Program& prog,
                                 unsigned char* const* bufs, int nbufs, void* stream) {
   const int64_t total = prog.total_units();
   if (total == 0) return RESHARD_OK;
@@ -506,6 +506,17 @@ reshard_status_t launch_program(const reshard_plan_s* plan, const Program& prog,
 // Launch one program whose tables live at caller-given device addresses (the
 // allocation-free entry point keeps them in a static device array).  Same kernel
 // and grid rule as launch_program; needs no uploaded plan.
+reshard_status_t launch_program(const reshard_plan_s* plan, const Program& prog,
+                                unsigned char* const* bufs, int nbufs, void* stream) {
+  reshard_status_t st = launch_tiles(plan, prog, bufs, nbufs, stream);
+  if (st != RESHARD_OK || prog.tblocks.empty()) return st;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device)
+    return fail(RESHARD_ERR_INVALID_ARG, "current device differs from the plan's device");
+  const uint32_t flags = destinations_congruent(prog, bufs) ? kFlagDstCongruent : 0u;
+  return launch_transposes(plan, prog, bufs, nbufs, flags, stream);
+}
+
 reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t* d_tiles,
                                        const int64_t* d_prefix, const uint32_t* d_goff,
                                        const uint16_t* d_gbuf, int num_sms,

@@ -20,6 +20,7 @@
 
 #include <algorithm>
 #include <chrono>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -301,6 +302,33 @@ reshard_status_t read_layout(const char* side, int32_t nd, const reshard_mesh_t*
   return RESHARD_OK;
 }
 
+// A region seen from one side as `rows` rows of `width` bytes at `stride`
+// bytes apart starting at byte `base` (outer dims must collapse to one stride).
+struct RowView {
+  bool ok = false;
+  int64_t base = 0, stride = 0, rows = 1, width = 0;
+};
+
+RowView row_view(int32_t nd, const int64_t* lo, const int64_t* ext, const Box& side, int64_t eb) {
+  RowView v;
+  int64_t st[RESHARD_MAX_TENSOR_NDIM];
+  row_major_strides(nd, side.shp, st);
+  v.width = ext[nd - 1] * eb;
+  for (int k = 0; k < nd; ++k) v.base += (lo[k] - side.off[k]) * st[k] * eb;
+  std::vector<Dim> m;
+  for (int k = 0; k + 1 < nd; ++k) {
+    if (ext[k] <= 1) continue;
+    const Dim d = {ext[k], st[k], 0};
+    if (!m.empty() && m.back().ss == d.e * d.ss) m.back() = {m.back().e * d.e, d.ss, 0};
+    else m.push_back(d);
+  }
+  if (m.size() > 1) return v;
+  v.rows = m.empty() ? 1 : m[0].e;
+  v.stride = m.empty() ? 0 : m[0].ss * eb;
+  v.ok = true;
+  return v;
+}
+
 reshard_status_t build_plan(reshard_plan_s* P) {
   const int32_t nd = P->ndim;
   const int64_t eb = P->elem_bytes;
@@ -407,10 +435,139 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   PG.gbuf.push_back(scratch_buf);
   PG.goff.push_back(1);
 
-  // ---- step 5: tiles
+  // ---- step 5a: transpose blocks for narrow innermost pieces (fan-out program)
+  std::vector<char> consumed(regions.size(), 0);
+  if (!P->inplace && nd >= 2) {
+    struct Piece {
+      size_t ri;
+      RowView wide, narrow;
+      int64_t col;
+    };
+    // Emits the blocks of one group; `gather` = narrow sources into one destination class.
+    auto emit_group = [&](std::vector<Piece>& ps, bool gather, int64_t rows, int64_t L,
+                          int64_t wide_base, const std::vector<uint16_t>& wide_ids) {
+      std::sort(ps.begin(), ps.end(), [](const Piece& a, const Piece& b) { return a.col < b.col; });
+      // rows per block: enough blocks to occupy the GPU, at most one shared-memory image
+      const int64_t nb = std::max<int64_t>(
+          1, std::min<int64_t>(kTransposeBlockBytes / L, (rows + kTransposeMinBlocks - 1) /
+                                                             kTransposeMinBlocks));
+      for (uint16_t wid : wide_ids) {
+        for (int64_t r0 = 0; r0 < rows; r0 += nb) {
+          reshard_tblock_t blk = {};
+          blk.wide_off = wide_base + r0 * L;
+          blk.row_bytes = uint32_t(L);
+          blk.nrows = uint32_t(std::min(nb, rows - r0));
+          blk.seg_begin = uint32_t(PF.tsegs.size());
+          blk.wide = wid;
+          blk.direction = gather ? 0 : 1;
+          for (const Piece& pc : ps) {
+            const Region& g = regions[pc.ri];
+            std::vector<uint16_t> nids;
+            if (gather) nids.push_back(uint16_t(g.replica));
+            else nids = fan_groups(dc[g.d].ranks);
+            for (uint16_t nid : nids) {
+              reshard_tseg_t sg = {};
+              sg.narrow_off = pc.narrow.base + r0 * pc.narrow.width;
+              sg.width = uint32_t(pc.narrow.width);
+              sg.col = uint32_t(pc.col);
+              sg.narrow = nid;
+              PF.tsegs.push_back(sg);
+            }
+          }
+          blk.seg_count = uint32_t(PF.tsegs.size()) - blk.seg_begin;
+          PF.tblocks.push_back(blk);
+        }
+      }
+      for (const Piece& pc : ps) consumed[pc.ri] = 1;
+    };
+    // Checks a candidate group: same rows, narrow sides dense, wide side covered exactly.
+    auto try_group = [&](const std::vector<size_t>& members, bool gather) {
+      if (members.size() < 2 || members.size() > size_t(kTransposeMaxSegs)) return;
+      std::vector<Piece> ps;
+      int64_t rows = -1, L = -1, base = INT64_MAX;
+      for (size_t ri : members) {
+        if (consumed[ri]) return;
+        const Region& g = regions[ri];
+        const Box& sb = P->src.box[size_t(g.replica)];
+        const Box& db = dc[g.d].box;
+        const RowView sv = row_view(nd, g.lo, g.ext, sb, eb);
+        const RowView dv = row_view(nd, g.lo, g.ext, db, eb);
+        if (!sv.ok || !dv.ok) return;
+        const RowView& wide = gather ? dv : sv;
+        const RowView& narrow = gather ? sv : dv;
+        if (narrow.width >= kTransposeMaxWidth) return;
+        if (rows < 0) rows = wide.rows;
+        if (wide.rows != rows || rows < 2) return;
+        if (narrow.stride != narrow.width) return;  // narrow side dense
+        if (L < 0) L = wide.stride;
+        if (wide.stride != L) return;
+        base = std::min(base, wide.base);
+        ps.push_back({ri, wide, narrow, 0});
+      }
+      if (L <= 0 || L > kTransposeBlockBytes) return;
+      int64_t covered = 0;
+      for (Piece& pc : ps) {
+        pc.col = pc.wide.base - base;
+        if (pc.col < 0 || pc.col + pc.wide.width > L) return;
+        covered += pc.wide.width;
+      }
+      if (covered != L) return;  // with disjoint regions: exact cover of every wide row
+      // Measured on GB300 (uneven-stress tensors): regrouping pays when a gather
+      // fans out to several destination replicas, or when the pieces are tiny
+      // (at most 4 bytes) and numerous; otherwise per-piece copies are faster.
+      int64_t max_w = 0;
+      for (const Piece& pc : ps) max_w = std::max(max_w, pc.narrow.width);
+      const bool fanned = gather && dc[regions[members[0]].d].ranks.size() >= 2;
+      if (!fanned && !(max_w <= 4 && ps.size() >= 16)) return;
+      if (!gather) {
+        size_t nsegs = 0;
+        for (const Piece& pc : ps) {
+          const size_t R = dc[regions[pc.ri].d].ranks.size();
+          nsegs += (R + kMaxGroup - 1) / kMaxGroup;
+        }
+        if (nsegs > size_t(kTransposeMaxSegs)) return;
+        size_t nptrs = 0;
+        for (const Piece& pc : ps) nptrs += dc[regions[pc.ri].d].ranks.size();
+        if (nptrs > size_t(kTransposeMaxReplicaPtrs)) return;
+      }
+      std::vector<uint16_t> wide_ids;
+      if (gather) wide_ids = fan_groups(dc[regions[members[0]].d].ranks);
+      else wide_ids.push_back(uint16_t(regions[members[0]].replica));
+      emit_group(ps, gather, rows, L, base, wide_ids);
+    };
+    // gather: all regions into one destination class
+    for (size_t di = 0; di < dc.size(); ++di) {
+      std::vector<size_t> members;
+      for (size_t ri = 0; ri < regions.size(); ++ri)
+        if (regions[ri].d == di) members.push_back(ri);
+      try_group(members, true);
+    }
+    // scatter: all regions out of one source class, read from one replica
+    for (size_t si = 0; si < sc.size(); ++si) {
+      std::vector<size_t> members;
+      for (size_t ri = 0; ri < regions.size(); ++ri)
+        if (regions[ri].s == si && !consumed[ri]) members.push_back(ri);
+      if (members.size() < 2) continue;
+      bool same = true;
+      for (size_t ri : members) same = same && regions[ri].replica == regions[members[0]].replica;
+      if (!same) {
+        std::vector<int64_t> saved;
+        for (size_t ri : members) saved.push_back(regions[ri].replica);
+        for (size_t ri : members) regions[ri].replica = regions[members[0]].replica;
+        try_group(members, false);
+        if (!consumed[members[0]])
+          for (size_t k = 0; k < members.size(); ++k) regions[members[k]].replica = saved[k];
+      } else {
+        try_group(members, false);
+      }
+    }
+  }
+
+  // ---- step 5b: tiles
   int64_t gst[RESHARD_MAX_TENSOR_NDIM];
   row_major_strides(nd, P->gshape, gst);
-  for (const Region& g : regions) {
+  for (size_t ri = 0; ri < regions.size(); ++ri) {
+    const Region& g = regions[ri];
     // destination ranks that still need the region (in-place plans drop the
     // rank whose buffer already holds a source replica of it)
     std::vector<int64_t> targets;
@@ -433,8 +590,9 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       s0 += (g.lo[d] - sb.off[d]) * sst[d];
       d0 += (g.lo[d] - db.off[d]) * dst[d];
     }
-    for (uint16_t grp : fan_groups(targets))
-      emit_box(PF, uint16_t(g.replica), grp, nd, g.ext, s0, sst, d0, dst, eb);
+    if (!consumed[ri])
+      for (uint16_t grp : fan_groups(targets))
+        emit_box(PF, uint16_t(g.replica), grp, nd, g.ext, s0, sst, d0, dst, eb);
     for (int64_t r : targets)
       emit_box(PB, uint16_t(g.replica), uint16_t(r), nd, g.ext, s0, sst, d0, dst, eb);
   }
@@ -478,6 +636,19 @@ reshard_status_t build_plan(reshard_plan_s* P) {
     const int64_t R = P->prog[0].goff[t.dst_group + 1] - P->prog[0].goff[t.dst_group];
     S.fanout_read_bytes += tile_bytes(t);
     S.fanout_write_bytes += R * tile_bytes(t);
+  }
+  for (const reshard_tblock_t& b : PF.tblocks) {
+    const int64_t bytes = int64_t(b.row_bytes) * b.nrows;
+    S.fanout_read_bytes += bytes;
+    if (b.direction == 0) {
+      S.fanout_write_bytes += bytes * int64_t(PF.goff[b.wide + 1] - PF.goff[b.wide]);
+    } else {
+      for (uint32_t k = b.seg_begin; k < b.seg_begin + b.seg_count; ++k) {
+        const reshard_tseg_t& sg = PF.tsegs[k];
+        S.fanout_write_bytes +=
+            int64_t(sg.width) * b.nrows * int64_t(PF.goff[sg.narrow + 1] - PF.goff[sg.narrow]);
+      }
+    }
   }
   for (const reshard_tile_t& t : PB.tiles) {
     S.boxcopy_read_bytes += tile_bytes(t);
@@ -688,12 +859,14 @@ reshard_status_t upload_plan(reshard_plan_s* plan) {
   // one allocation: per program tiles | prefix | goff | gbuf, each 256-byte aligned
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t total = 0;
-  size_t offs[4][4];
+  size_t offs[4][6];
   for (int k = 0; k < 4; ++k) {
     const rs::Program& p = plan->prog[k];
-    const size_t sz[4] = {p.tiles.size() * sizeof(reshard_tile_t), p.prefix.size() * sizeof(int64_t),
-                          p.goff.size() * sizeof(uint32_t), p.gbuf.size() * sizeof(uint16_t)};
-    for (int j = 0; j < 4; ++j) {
+    const size_t sz[6] = {p.tiles.size() * sizeof(reshard_tile_t), p.prefix.size() * sizeof(int64_t),
+                          p.goff.size() * sizeof(uint32_t), p.gbuf.size() * sizeof(uint16_t),
+                          p.tblocks.size() * sizeof(reshard_tblock_t),
+                          p.tsegs.size() * sizeof(reshard_tseg_t)};
+    for (int j = 0; j < 6; ++j) {
       offs[k][j] = total;
       total += up(sz[j]);
     }
@@ -710,6 +883,10 @@ reshard_status_t upload_plan(reshard_plan_s* plan) {
     if (!p.prefix.empty()) std::memcpy(&host[offs[k][1]], p.prefix.data(), p.prefix.size() * sizeof(int64_t));
     if (!p.goff.empty()) std::memcpy(&host[offs[k][2]], p.goff.data(), p.goff.size() * sizeof(uint32_t));
     if (!p.gbuf.empty()) std::memcpy(&host[offs[k][3]], p.gbuf.data(), p.gbuf.size() * sizeof(uint16_t));
+    if (!p.tblocks.empty())
+      std::memcpy(&host[offs[k][4]], p.tblocks.data(), p.tblocks.size() * sizeof(reshard_tblock_t));
+    if (!p.tsegs.empty())
+      std::memcpy(&host[offs[k][5]], p.tsegs.data(), p.tsegs.size() * sizeof(reshard_tseg_t));
   }
   void* d = nullptr;
   ce = cudaMalloc(&d, std::max<size_t>(total, 256));
@@ -726,6 +903,8 @@ reshard_status_t upload_plan(reshard_plan_s* plan) {
     p.d_prefix = reinterpret_cast<const int64_t*>(base + offs[k][1]);
     p.d_goff = reinterpret_cast<const uint32_t*>(base + offs[k][2]);
     p.d_gbuf = reinterpret_cast<const uint16_t*>(base + offs[k][3]);
+    p.d_tblocks = reinterpret_cast<const reshard_tblock_t*>(base + offs[k][4]);
+    p.d_tsegs = reinterpret_cast<const reshard_tseg_t*>(base + offs[k][5]);
   }
   plan->d_mem = d;
   plan->device = dev;
@@ -851,6 +1030,19 @@ reshard_status_t reshard_plan_program(reshard_plan_t plan, int32_t program,
   if (group_offsets) *group_offsets = p.goff.data();
   if (group_buffers) *group_buffers = p.gbuf.data();
   if (ngroups) *ngroups = int64_t(p.goff.size()) - 1;
+  return RESHARD_OK;
+}
+
+reshard_status_t reshard_plan_transposes(reshard_plan_t plan, int32_t program,
+                                         const reshard_tblock_t** blocks, int64_t* nblocks,
+                                         const reshard_tseg_t** segs, int64_t* nsegs) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (program < 0 || program > 3) return fail(RESHARD_ERR_INVALID_ARG, "unknown program");
+  const rs::Program& p = plan->prog[program];
+  if (blocks) *blocks = p.tblocks.data();
+  if (nblocks) *nblocks = int64_t(p.tblocks.size());
+  if (segs) *segs = p.tsegs.data();
+  if (nsegs) *nsegs = int64_t(p.tsegs.size());
   return RESHARD_OK;
 }
 

@@ -160,6 +160,38 @@ typedef struct reshard_tile {
 } reshard_tile_t;
 
 /*
+ * Transpose blocks (read-only view, for inspection and tests).  When a tensor is
+ * sharded on its innermost dim into narrow pieces (under 64 bytes per row) on
+ * one side and into whole rows on the other, per-piece copies would write a few
+ * bytes per row.  The planner then groups the pieces that share their rows: a
+ * block is nrows consecutive rows of row_bytes on the "wide" side (one buffer
+ * or destination group, contiguous) and seg_count narrow segments, each a
+ * dense run of nrows x width bytes on its own buffer or destination group,
+ * occupying bytes [col, col + width) of every wide row.  The kernel assembles
+ * or splits the rows in shared memory, so both sides move contiguous bytes.
+ *   direction 0 (gather):  narrow sources -> wide destination group;
+ *   direction 1 (scatter): wide source -> narrow destination groups.
+ */
+typedef struct reshard_tblock {
+  int64_t wide_off;    /* bytes: row 0 of the block in the wide buffer(s) */
+  uint32_t row_bytes;  /* wide row length */
+  uint32_t nrows;
+  uint32_t seg_begin, seg_count;
+  uint16_t wide;       /* gather: destination group; scatter: source buffer index */
+  uint16_t direction;  /* 0 gather, 1 scatter */
+  uint32_t pad;
+} reshard_tblock_t;
+
+typedef struct reshard_tseg {
+  int64_t narrow_off;  /* bytes: row 0 of the block in the narrow buffer(s) */
+  uint32_t width;      /* bytes per row */
+  uint32_t col;        /* byte offset of the segment inside a wide row */
+  uint16_t narrow;     /* gather: source buffer index; scatter: destination group */
+  uint16_t pad16;
+  uint32_t pad32;
+} reshard_tseg_t;
+
+/*
  * Plan a reshard of one tensor (steps: resolve both layouts, intersect every
  * source box with every destination box, pick one source replica per region
  * balancing bytes read across replicas, collapse contiguous dims into copy
@@ -387,6 +419,15 @@ reshard_status_t reshard_plan_program(reshard_plan_t plan, int32_t program,
                                       const int64_t** unit_prefix,
                                       const uint32_t** group_offsets,
                                       const uint16_t** group_buffers, int64_t* ngroups);
+
+/*
+ * Read-only view of a program's transpose blocks (see reshard_tblock_t), valid
+ * until the plan is destroyed.  Only the FANOUT program has any.  Any output
+ * pointer may be NULL.  Errors: BAD_HANDLE, INVALID_ARG.
+ */
+reshard_status_t reshard_plan_transposes(reshard_plan_t plan, int32_t program,
+                                         const reshard_tblock_t** blocks, int64_t* nblocks,
+                                         const reshard_tseg_t** segs, int64_t* nsegs);
 
 /*
  * Work units of a tile: a single-row tile is split into 4096-byte units, a

@@ -67,7 +67,37 @@ def run_program_cpu(plan, program, bufs):
                     assert 0 <= do and do + n <= dst.size, ("destination out of bounds", t)
                     dst[do:do + n] = src[so:so + n]
                     writes[di][do:do + n] += 1
+    run_transposes_cpu(plan, program, bufs, writes)
     return writes
+
+
+def run_transposes_cpu(plan, program, bufs, writes):
+    """Execute a program's transpose blocks on host buffers (test only)."""
+    blocks, segs = rs.reshard_plan_transposes(plan, program)
+    _, _, goff, gbuf = rs.reshard_plan_program(plan, program)
+    for b in blocks:
+        L, nr = b["row_bytes"], b["nrows"]
+        for k in range(b["seg_begin"], b["seg_begin"] + b["seg_count"]):
+            sg = segs[k]
+            w, col = sg["width"], sg["col"]
+            if b["direction"] == 0:   # narrow source -> wide destination group
+                src = bufs[sg["narrow"]][sg["narrow_off"]:sg["narrow_off"] + nr * w]
+                assert src.size == nr * w, ("source out of bounds", b, sg)
+                for di in gbuf[goff[b["wide"]]:goff[b["wide"] + 1]]:
+                    lo = b["wide_off"]
+                    assert lo >= 0 and lo + nr * L <= bufs[di].size, ("dst out of bounds", b)
+                    bufs[di][lo:lo + nr * L].reshape(nr, L)[:, col:col + w] = src.reshape(nr, w)
+                    writes[di][lo:lo + nr * L].reshape(nr, L)[:, col:col + w] += 1
+            else:                      # wide source -> narrow destination group
+                lo = b["wide_off"]
+                wide = bufs[b["wide"]][lo:lo + nr * L]
+                assert wide.size == nr * L, ("source out of bounds", b)
+                piece = wide.reshape(nr, L)[:, col:col + w].reshape(-1)
+                for di in gbuf[goff[sg["narrow"]]:goff[sg["narrow"] + 1]]:
+                    o = sg["narrow_off"]
+                    assert o >= 0 and o + nr * w <= bufs[di].size, ("dst out of bounds", sg)
+                    bufs[di][o:o + nr * w] = piece
+                    writes[di][o:o + nr * w] += 1
 
 
 def spec_plan(spec):

@@ -501,3 +501,24 @@ def test_cuda_graph_capture_and_replay(oracle):
             for d, w in zip(dsts, want):
                 assert np.array_equal(helpers.to_bytes(d), w), (spec.name, shift)
     assert rs.reshard_device_status() == 0
+
+
+# ---------------------------------------------------------------------- transpose blocks
+TRANSPOSE_CASES = [
+    _spec((74, 65, 1721), "fp16", (61,), ("S2",), (3,), ("R",), seed=1),        # gather, R=3
+    _spec((1338, 65), "fp16", (18,), ("S0",), (38,), ("S1",), seed=2),          # scatter, 2-4 B
+    _spec((900, 7, 23), "bf16", (2, 5), ("R", "S2"), (2,), ("R",), seed=3),     # gather, R=2
+    _spec((300, 40), "u8", (1,), ("R",), (40,), ("S1",), seed=4),               # scatter, 1 B
+    _spec((40, 45, 17), "fp32", (6,), ("S0",), (17,), ("S2",), seed=5),         # scatter 3-D
+    _spec((4097, 20), "u8", (20,), ("S1",), (4,), ("R",), seed=6),              # gather, 1 B, R=4
+]
+
+
+@pytest.mark.parametrize("i", range(len(TRANSPOSE_CASES)))
+@pytest.mark.parametrize("misalign", [0, 3])
+def test_transpose_blocks(oracle, i, misalign):
+    spec = TRANSPOSE_CASES[i]
+    blocks, _ = rs.reshard_plan_transposes(helpers.spec_plan(spec), rs.PROGRAM_FANOUT)
+    assert blocks, "layout expected to use transpose blocks"
+    run_and_compare(oracle, spec, misalign=misalign)
+    run_and_compare(oracle, spec, misalign=misalign, dst_misalign=lambda r: (r * 5) % 16)
