@@ -447,6 +447,13 @@ reshard_status_t build_plan(reshard_plan_s* P) {
     auto emit_group = [&](std::vector<Piece>& ps, bool gather, int64_t rows, int64_t L,
                           int64_t wide_base, const std::vector<uint16_t>& wide_ids) {
       std::sort(ps.begin(), ps.end(), [](const Piece& a, const Piece& b) { return a.col < b.col; });
+      // narrow buffer (gather) or destination groups (scatter) of every piece, once
+      std::vector<std::vector<uint16_t>> narrow_ids(ps.size());
+      for (size_t i = 0; i < ps.size(); ++i) {
+        const Region& g = regions[ps[i].ri];
+        if (gather) narrow_ids[i].push_back(uint16_t(g.replica));
+        else narrow_ids[i] = fan_groups(dc[g.d].ranks);
+      }
       // rows per block: enough blocks to occupy the GPU, at most one shared-memory image
       const int64_t nb = std::max<int64_t>(
           1, std::min<int64_t>(kTransposeBlockBytes / L, (rows + kTransposeMinBlocks - 1) /
@@ -460,12 +467,9 @@ reshard_status_t build_plan(reshard_plan_s* P) {
           blk.seg_begin = uint32_t(PF.tsegs.size());
           blk.wide = wid;
           blk.direction = gather ? 0 : 1;
-          for (const Piece& pc : ps) {
-            const Region& g = regions[pc.ri];
-            std::vector<uint16_t> nids;
-            if (gather) nids.push_back(uint16_t(g.replica));
-            else nids = fan_groups(dc[g.d].ranks);
-            for (uint16_t nid : nids) {
+          for (size_t i = 0; i < ps.size(); ++i) {
+            const Piece& pc = ps[i];
+            for (uint16_t nid : narrow_ids[i]) {
               reshard_tseg_t sg = {};
               sg.narrow_off = pc.narrow.base + r0 * pc.narrow.width;
               sg.width = uint32_t(pc.narrow.width);
@@ -535,18 +539,18 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       else wide_ids.push_back(uint16_t(regions[members[0]].replica));
       emit_group(ps, gather, rows, L, base, wide_ids);
     };
-    // gather: all regions into one destination class
-    for (size_t di = 0; di < dc.size(); ++di) {
-      std::vector<size_t> members;
-      for (size_t ri = 0; ri < regions.size(); ++ri)
-        if (regions[ri].d == di) members.push_back(ri);
-      try_group(members, true);
+    std::vector<std::vector<size_t>> into(dc.size()), outof(sc.size());
+    for (size_t ri = 0; ri < regions.size(); ++ri) {
+      into[regions[ri].d].push_back(ri);
+      outof[regions[ri].s].push_back(ri);
     }
+    // gather: all regions into one destination class
+    for (size_t di = 0; di < dc.size(); ++di) try_group(into[di], true);
     // scatter: all regions out of one source class, read from one replica
     for (size_t si = 0; si < sc.size(); ++si) {
       std::vector<size_t> members;
-      for (size_t ri = 0; ri < regions.size(); ++ri)
-        if (regions[ri].s == si && !consumed[ri]) members.push_back(ri);
+      for (size_t ri : outof[si])
+        if (!consumed[ri]) members.push_back(ri);
       if (members.size() < 2) continue;
       bool same = true;
       for (size_t ri : members) same = same && regions[ri].replica == regions[members[0]].replica;
