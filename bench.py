@@ -229,9 +229,9 @@ _HOST_SRC = {}
 def oracle_sample(jobs, seconds):
     """Time the CPU oracle on a bounded sample of the workload's reshard tensors.
 
-    Sample: for every reshard tensor, destination rank 0, consecutive slices of its
-    outermost dim from the start, processed a few slices at a time until the tensor's
-    share of ``seconds`` of CPU time is spent.  Only the source shards a chunk touches
+    Sample: for every reshard tensor, destination rank 0, chunks of slices of its
+    outermost dim taken in bit-reversed order (so any prefix is spread evenly over
+    the tensor), until the tensor's share of ``seconds`` of CPU time is spent.  Only the source shards a chunk touches
     are copied to the host (outside the timed calls).
     Returns (effective GB/s, sample description, cores used, CPU seconds).
     """
@@ -253,14 +253,22 @@ def oracle_sample(jobs, seconds):
             continue
         per = math.prod(dshp[1:])
         chunk = max(1, (4 << 20) // max(1, per))
+        nchunks = (dshp[0] + chunk - 1) // chunk
+        # chunk order: bit-reversed, so that every prefix is spread over the whole dim
+        bits = max(1, (nchunks - 1).bit_length())
+        order = [c for c in (int(format(i, f"0{bits}b")[::-1], 2) for i in range(1 << bits))
+                 if c < nchunks]
         sboxes = o.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
         out = np.empty(math.prod(dshp) * spec.elem_bytes, dtype=np.uint8)
         t_spent, done, n = 0.0, 0, 0
-        while t_spent < budget and done < dshp[0]:
-            k = min(chunk, dshp[0] - done)
+        for ci in order:
+            if t_spent >= budget:
+                break
+            first = ci * chunk
+            k = min(chunk, dshp[0] - first)
             lo = list(doff)
             hi = [a + b for a, b in zip(doff, dshp)]
-            lo[0], hi[0] = doff[0] + done, doff[0] + done + k
+            lo[0], hi[0] = doff[0] + first, doff[0] + first + k
             ptrs = []
             for s, (so, ss) in enumerate(sboxes):
                 touch = math.prod(ss) and all(
@@ -275,14 +283,15 @@ def oracle_sample(jobs, seconds):
             t0 = time.perf_counter()
             o.reshard_elems(spec.global_shape, spec.elem_bytes, spec.src_mesh,
                             spec.src_placements, spec.dst_mesh, spec.dst_placements, ptrs,
-                            out.ctypes.data, 0, done * per, (done + k) * per)
+                            out.ctypes.data, 0, first * per, (first + k) * per)
             t_spent += time.perf_counter() - t0
             n += k * per
             done += k
         st = j.stats
         tot_t += t_spent
         tot_b += n * spec.elem_bytes * (1.0 + st["global_bytes"] / st["dst_bytes"])
-        desc.append(f"{spec.name}: dst rank 0, first {done} of dim 0 ({n} elements)")
+        desc.append(f"{spec.name}: dst rank 0, {done} of {dshp[0]} dim-0 slices spread over "
+                    f"the tensor ({n} elements)")
     if tot_t == 0:
         return None
     return tot_b / tot_t / 1e9, "; ".join(desc), 1, tot_t
