@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -110,7 +111,8 @@ struct reshard_plan_s {
   // (-1: separate buffer) at byte offset alias_off[s]
   bool inplace = false;
   std::vector<int64_t> alias_dst, alias_off;
-  // device binding
+  // device binding (set once by upload_plan, under upload_mu)
+  std::mutex upload_mu;
   int device = -1;
   void* d_mem = nullptr;
   int num_sms = 0;

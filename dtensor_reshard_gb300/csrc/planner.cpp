@@ -845,6 +845,7 @@ reshard_status_t reshard_plan_upload(reshard_plan_t plan) {
 namespace rs {
 
 reshard_status_t upload_plan(reshard_plan_s* plan) {
+  std::lock_guard<std::mutex> lock(plan->upload_mu);
   int dev = -1;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));

@@ -522,3 +522,59 @@ def test_transpose_blocks(oracle, i, misalign):
     assert blocks, "layout expected to use transpose blocks"
     run_and_compare(oracle, spec, misalign=misalign)
     run_and_compare(oracle, spec, misalign=misalign, dst_misalign=lambda r: (r * 5) % 16)
+
+
+# ---------------------------------------------------------------------- concurrency
+def test_first_use_from_several_host_threads(oracle):
+    """Eight host threads execute one fresh plan at once (each into its own buffers): the
+    plan's first upload is serialised and every result is exact."""
+    import threading
+    _cuda()
+    spec = workload(2, reduced=True).tensors[0]
+    glob = global_tensor(spec)
+    srcs = [helpers.to_bytes(s) for s in helpers.scatter_with_oracle(
+        oracle, glob, spec.src_mesh, spec.src_placements)]
+    want = helpers.expected_dst(oracle, spec, srcs)
+    plan = helpers.spec_plan(spec)
+    dsrc = _upload(srcs)
+    outs = [[Guarded(w.size) for w in want] for _ in range(8)]
+    errors = []
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream()
+            rs.reshard_execute(plan, [g.ptr for g in dsrc], [g.ptr for g in outs[i]], s)
+            s.synchronize()
+        except Exception as e:  # noqa: BLE001 - collected and asserted below
+            errors.append(e)
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(8)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for dd in outs:
+        for g, w in zip(dd, want):
+            assert np.array_equal(g.payload().cpu().numpy(), w)
+
+
+def test_two_plans_on_two_streams(oracle):
+    _cuda()
+    a, b = workload(3, reduced=True).tensors[:2]
+    cases = []
+    for spec in (a, b):
+        glob = global_tensor(spec)
+        srcs = [helpers.to_bytes(s) for s in helpers.scatter_with_oracle(
+            oracle, glob, spec.src_mesh, spec.src_placements)]
+        want = helpers.expected_dst(oracle, spec, srcs)
+        cases.append((helpers.spec_plan(spec), _upload(srcs), [Guarded(w.size) for w in want],
+                      want, torch.cuda.Stream()))
+    for _ in range(3):
+        for plan, ds, dd, _, st in cases:
+            rs.reshard_execute(plan, [g.ptr for g in ds], [g.ptr for g in dd], st)
+    torch.cuda.synchronize()
+    for _, _, dd, want, _ in cases:
+        for g, w in zip(dd, want):
+            assert np.array_equal(g.payload().cpu().numpy(), w)
