@@ -48,8 +48,10 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("moe_refit", "hybridflow", "ffn_up"),
+    ap.add_argument("--workload", choices=("moe_refit", "hybridflow", "ffn_up", "uneven_stress"),
                     default="moe_refit")
+    ap.add_argument("--tensors", default=None,
+                    help="comma-separated tensor names to keep from the workload (profiling)")
     ap.add_argument("--kernel", choices=("fanout", "boxcopy"), default="fanout")
     ap.add_argument("--batch", action="store_true",
                     help="launch all reshard tensors as one batch (measured: no gain on GB300)")
@@ -439,11 +441,16 @@ class DistCtx:
         return x if self.world == 1 else self._reduce(x, self.dist.ReduceOp.SUM)
 
 
-def pick_workload(name, experts=256):
-    from inputs import ffn_up, hybridflow, moe_refit
+def pick_workload(name, experts=256, tensors=None):
+    from inputs import Workload, ffn_up, hybridflow, moe_refit, uneven_stress
     if name == "moe_refit":
-        return moe_refit(experts=experts)
-    return {"hybridflow": hybridflow, "ffn_up": ffn_up}[name]()
+        w = moe_refit(experts=experts)
+    else:
+        w = {"hybridflow": hybridflow, "ffn_up": ffn_up, "uneven_stress": uneven_stress}[name]()
+    if tensors:
+        keep = set(tensors.split(","))
+        w = Workload(w.name + ":" + tensors, tuple(t for t in w.tensors if t.name in keep), w.note)
+    return w
 
 
 # ------------------------------------------------------------------------------ arms
@@ -453,7 +460,7 @@ def reference_arm(args, rank, world):
         return 0
     import torch
     dev = torch.device("cuda:0") if torch.cuda.is_available() else None
-    w = pick_workload(args.workload, args.experts)
+    w = pick_workload(args.workload, args.experts, args.tensors)
     if dev is None:
         print(json.dumps({"impl": "reference", "unavailable": "no CUDA device to build inputs"}))
         return 0
@@ -498,7 +505,7 @@ def ours_arm(args, rank, world, local):
     if gpu_uuid and not gpu_uuid.startswith("GPU-") and len(gpu_uuid) > 8:
         gpu_uuid = "GPU-" + gpu_uuid
     kernel = rs.KERNEL_FANOUT if args.kernel == "fanout" else rs.KERNEL_BOXCOPY
-    w = pick_workload(args.workload, args.experts)
+    w = pick_workload(args.workload, args.experts, args.tensors)
     t0 = time.perf_counter()
     jobs = build_jobs(w, dev, with_gb=not args.reshard_only)
     setup_s = time.perf_counter() - t0
