@@ -29,9 +29,12 @@ namespace rs {
 namespace {
 
 constexpr int kTThreads = 256;
-constexpr int kTUnroll = 4;   // narrow-side elements in flight per thread
 constexpr int kTVecUnroll = 4;  // wide-side 16-byte loads in flight per thread
 constexpr int kImageBytes = int(kTransposeBlockBytes) + 64;
+// staging area for the narrow side: every segment's dense range in whole 16-byte
+// granules (at most one extra granule per segment)
+constexpr int kStageBytes = int(kTransposeBlockBytes) + 32 * int(kTransposeMaxSegs) + 64;
+constexpr int kDynSmem = kImageBytes + kStageBytes;
 constexpr int kMaxReplicaPtrs = int(kTransposeMaxReplicaPtrs);
 
 struct TransposeParams {
@@ -62,9 +65,11 @@ struct SegInfo {
   int64_t off;               // scatter: narrow byte offset at the block's row 0
   uint32_t units;            // width / U
   uint32_t col;              // byte column inside a wide row
-  uint32_t start;            // first flat element of the segment
   uint32_t m, l;             // fast division by units
   uint32_t rbeg, rcnt;       // scatter: replica pointers [rbeg, rbeg + rcnt) of ptrs[]
+  uint32_t gstart;           // first staging granule of the segment
+  uint32_t gmis;             // narrow global address mod 16 (replica 0 for scatter)
+  uint32_t nbytes;           // width * nrows
 };
 
 template <int U> struct UType;
@@ -73,63 +78,105 @@ template <> struct UType<2> { using T = uint16_t; };
 template <> struct UType<4> { using T = uint32_t; };
 template <> struct UType<8> { using T = uint2; };
 
-// segment of flat element e (largest k with start[k] <= e)
-__device__ __forceinline__ int find_seg(const SegInfo* si, int K, uint32_t e) {
+// segment owning staging granule g (largest k with gstart[k] <= g)
+__device__ __forceinline__ int find_granule(const SegInfo* si, int K, uint32_t g) {
   int lo = 0, hi = K - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (si[mid].start <= e) lo = mid;
+    if (si[mid].gstart <= g) lo = mid;
     else hi = mid - 1;
   }
   return lo;
 }
 
-// gather, phase 1: every segment's dense range -> its columns of the image
-template <int U>
-__device__ __forceinline__ void gather_in(const SegInfo* si, int K, uint32_t total,
-                                          unsigned char* img, uint32_t mis, uint32_t L) {
-  using T = typename UType<U>::T;
+// gather, phase 1a: every segment's dense source range -> staging, as whole aligned
+// 16-byte granules (granule j of segment k at staging byte 16 (gstart_k + j))
+__device__ __forceinline__ void gather_stage(const SegInfo* si, int K, uint32_t ngran,
+                                             unsigned char* stg) {
 #pragma unroll 1
-  for (uint32_t e0 = threadIdx.x; e0 < total; e0 += kTThreads * kTUnroll) {
-    T v[kTUnroll];
-    uint32_t dsto[kTUnroll];
+  for (uint32_t g0 = threadIdx.x; g0 < ngran; g0 += kTThreads * kTVecUnroll) {
+    uint4 v[kTVecUnroll];
 #pragma unroll
-    for (int j = 0; j < kTUnroll; ++j) {
-      const uint32_t e = e0 + j * kTThreads;
-      if (e < total) {
-        const SegInfo& s = si[find_seg(si, K, e)];
-        const uint32_t local = e - s.start;
-        const uint32_t row = fastdiv(local, s.m, s.l);
-        const uint32_t c = local - row * s.units;
-        v[j] = *reinterpret_cast<const T*>(s.src + size_t(local) * U);
-        dsto[j] = mis + row * L + s.col + c * U;
+    for (int j = 0; j < kTVecUnroll; ++j) {
+      const uint32_t g = g0 + j * kTThreads;
+      if (g < ngran) {
+        const SegInfo& s = si[find_granule(si, K, g)];
+        v[j] = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(g - s.gstart)));
       }
     }
 #pragma unroll
-    for (int j = 0; j < kTUnroll; ++j)
-      if (e0 + j * kTThreads < total) *reinterpret_cast<T*>(img + dsto[j]) = v[j];
+    for (int j = 0; j < kTVecUnroll; ++j) {
+      const uint32_t g = g0 + j * kTThreads;
+      if (g < ngran) *reinterpret_cast<uint4*>(stg + 16 * size_t(g)) = v[j];
+    }
   }
 }
 
-// scatter, phase 2: image columns -> every segment's dense range on each replica
+// gather, phase 1b: staging -> columns of the image (shared memory only), one
+// warp per segment, lanes over its elements
 template <int U>
-__device__ __forceinline__ void scatter_out(const SegInfo* si, int K, uint32_t total,
-                                            const unsigned char* img, uint32_t mis, uint32_t L,
-                                            unsigned char* const* ptrs) {
+__device__ __forceinline__ void gather_place(const SegInfo* si, int K, uint32_t nr,
+                                             const unsigned char* stg, unsigned char* img,
+                                             uint32_t mis, uint32_t L) {
   using T = typename UType<U>::T;
-#pragma unroll 1
-  for (uint32_t e0 = threadIdx.x; e0 < total; e0 += kTThreads * kTUnroll) {
-#pragma unroll
-    for (int j = 0; j < kTUnroll; ++j) {
-      const uint32_t e = e0 + j * kTThreads;
-      if (e < total) {
-        const SegInfo& s = si[find_seg(si, K, e)];
-        const uint32_t local = e - s.start;
-        const uint32_t row = fastdiv(local, s.m, s.l);
-        const uint32_t c = local - row * s.units;
-        const T v = *reinterpret_cast<const T*>(img + mis + row * L + s.col + c * U);
-        for (uint32_t r = 0; r < s.rcnt; ++r)
-          *reinterpret_cast<T*>(ptrs[s.rbeg + r] + s.off + int64_t(local) * U) = v;
+  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
+  for (int k = warp; k < K; k += kTThreads / 32) {
+    const SegInfo& s = si[k];
+    const uint32_t n = s.units * nr;
+    const unsigned char* from = stg + 16 * s.gstart + s.gmis;
+    unsigned char* to = img + mis + s.col;
+#pragma unroll 4
+    for (uint32_t local = lane; local < n; local += 32) {
+      const uint32_t row = fastdiv(local, s.m, s.l);
+      const uint32_t c = local - row * s.units;
+      *reinterpret_cast<T*>(to + row * L + c * U) = *reinterpret_cast<const T*>(from + local * U);
+    }
+  }
+}
+
+// scatter, phase 2a: image columns -> staging, laid out so that every segment's
+// destination range (replica 0) falls on whole 16-byte granules; warp per segment
+template <int U>
+__device__ __forceinline__ void scatter_stage(const SegInfo* si, int K, uint32_t nr,
+                                              const unsigned char* img, uint32_t mis, uint32_t L,
+                                              unsigned char* stg) {
+  using T = typename UType<U>::T;
+  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
+  for (int k = warp; k < K; k += kTThreads / 32) {
+    const SegInfo& s = si[k];
+    const uint32_t n = s.units * nr;
+    const unsigned char* from = img + mis + s.col;
+    unsigned char* to = stg + 16 * s.gstart + s.gmis;
+#pragma unroll 4
+    for (uint32_t local = lane; local < n; local += 32) {
+      const uint32_t row = fastdiv(local, s.m, s.l);
+      const uint32_t c = local - row * s.units;
+      *reinterpret_cast<T*>(to + local * U) = *reinterpret_cast<const T*>(from + row * L + c * U);
+    }
+  }
+}
+
+// scatter, phase 2b: staging granules -> every replica of every segment, warp per
+// segment; whole granules of replicas aligned like replica 0 go out as 16-byte stores
+__device__ __forceinline__ void scatter_write(const SegInfo* si, int K, const unsigned char* stg,
+                                              unsigned char* const* ptrs) {
+  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
+  for (int k = warp; k < K; k += kTThreads / 32) {
+    const SegInfo& s = si[k];
+    const uint32_t end = s.gmis + s.nbytes;      // segment end, granule-relative bytes
+    const uint32_t ng = (end + 15u) >> 4;
+    for (uint32_t j = lane; j < ng; j += 32) {
+      const uint32_t lo = j == 0 ? s.gmis : 0u;
+      const uint32_t hi = min(16u, end - 16u * j);
+      const unsigned char* src = stg + 16 * size_t(s.gstart + j);
+      const uint4 v = *reinterpret_cast<const uint4*>(src);
+      for (uint32_t r = 0; r < s.rcnt; ++r) {
+        unsigned char* base = ptrs[s.rbeg + r] + s.off;  // segment byte 0 of this replica
+        if (lo == 0 && hi == 16 && (reinterpret_cast<uintptr_t>(base) & 15u) == s.gmis) {
+          __stcs(reinterpret_cast<uint4*>(base - s.gmis + 16 * size_t(j)), v);
+        } else {
+          for (uint32_t b = lo; b < hi; ++b) base[16 * j + b - s.gmis] = src[b];
+        }
       }
     }
   }
@@ -137,11 +184,13 @@ __device__ __forceinline__ void scatter_out(const SegInfo* si, int K, uint32_t t
 
 __global__ void __launch_bounds__(kTThreads, 3)
     reshard_transpose_kernel(const __grid_constant__ TransposeParams p) {
-  extern __shared__ __align__(16) unsigned char img[];
+  extern __shared__ __align__(16) unsigned char dyn[];
+  unsigned char* img = dyn;                // wide rows, shifted by the wide address mod 16
+  unsigned char* stg = dyn + kImageBytes;  // narrow ranges in whole 16-byte granules
   __shared__ SegInfo si[kTransposeMaxSegs];
   __shared__ unsigned char* ptrs[kMaxReplicaPtrs];
   __shared__ unsigned int s_align;
-  __shared__ uint32_t s_total;
+  __shared__ uint32_t s_ngran;
   const bool congruent = (p.flags & kFlagDstCongruent) != 0;
   const int64_t b0 = p.nblocks * int64_t(blockIdx.x) / int64_t(gridDim.x);
   const int64_t b1 = p.nblocks * int64_t(blockIdx.x + 1) / int64_t(gridDim.x);
@@ -172,15 +221,18 @@ __global__ void __launch_bounds__(kTThreads, 3)
       unsigned int a = sg.width | (mis + sg.col);
       if (gather) {
         si[k].src = p.bufs[sg.narrow] + sg.narrow_off;
+        si[k].gmis = unsigned(reinterpret_cast<uintptr_t>(si[k].src) & 15u);
         a |= unsigned(reinterpret_cast<uintptr_t>(si[k].src));
       } else {
         si[k].off = sg.narrow_off;
         const uint32_t g0 = p.goff[sg.narrow];
         const uint32_t rc = p.goff[sg.narrow + 1] - g0;
         si[k].rcnt = rc;
-        for (uint32_t r = 0; r < rc; ++r)
-          a |= unsigned(reinterpret_cast<uintptr_t>(p.bufs[p.gbuf[g0 + r]] + sg.narrow_off));
+        si[k].gmis =
+            unsigned(reinterpret_cast<uintptr_t>(p.bufs[p.gbuf[g0]] + sg.narrow_off) & 15u);
+        a |= si[k].gmis;
       }
+      si[k].nbytes = sg.width * nr;
       si[k].col = sg.col;
       si[k].units = sg.width;  // bytes for now
       atomicOr(&s_align, a);
@@ -189,41 +241,41 @@ __global__ void __launch_bounds__(kTThreads, 3)
     const unsigned int al = s_align;
     const uint32_t U = (al & 1u) ? 1u : (al & 2u) ? 2u : (al & 4u) ? 4u : 8u;
     if (threadIdx.x < 32) {
-      // element counts, exclusive prefix and replica pointer slots in segment order:
+      // staging granules and replica pointer slots, exclusive prefix in segment order:
       // each lane owns segments [4 lane, 4 lane + 4) (K <= 128), then a warp scan
       const int lane = int(threadIdx.x);
-      uint32_t cnt[4], rc[4], csum = 0, rsum = 0;
+      uint32_t rc[4], gc[4], rsum = 0, gsum = 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t k = uint32_t(4 * lane + q);
-        cnt[q] = k < K ? (si[k].units / U) * nr : 0u;
         rc[q] = (k < K && !gather) ? si[k].rcnt : 0u;
-        csum += cnt[q];
+        gc[q] = k < K ? (si[k].gmis + si[k].nbytes + 15u) >> 4 : 0u;
         rsum += rc[q];
+        gsum += gc[q];
       }
-      uint32_t cinc = csum, rinc = rsum;
+      uint32_t rinc = rsum, ginc = gsum;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t a = __shfl_up_sync(0xffffffffu, cinc, d);
         const uint32_t b = __shfl_up_sync(0xffffffffu, rinc, d);
+        const uint32_t c = __shfl_up_sync(0xffffffffu, ginc, d);
         if (lane >= d) {
-          cinc += a;
           rinc += b;
+          ginc += c;
         }
       }
-      uint32_t start = cinc - csum, rb = rinc - rsum;
+      uint32_t rb = rinc - rsum, gs = ginc - gsum;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t k = uint32_t(4 * lane + q);
         if (k < K) {
           si[k].units /= U;
-          si[k].start = start;
           si[k].rbeg = rb;
+          si[k].gstart = gs;
         }
-        start += cnt[q];
         rb += rc[q];
+        gs += gc[q];
       }
-      if (lane == 31) s_total = cinc;
+      if (lane == 31) s_ngran = ginc;
     }
     __syncthreads();
     for (uint32_t k = threadIdx.x; k < K; k += kTThreads) {
@@ -235,14 +287,16 @@ __global__ void __launch_bounds__(kTThreads, 3)
       }
     }
     __syncthreads();
-    const uint32_t total = s_total;
+    const uint32_t ngran = s_ngran;
 
     if (gather) {
+      gather_stage(si, int(K), ngran, stg);
+      __syncthreads();
       switch (U) {
-        case 1: gather_in<1>(si, int(K), total, img, mis, L); break;
-        case 2: gather_in<2>(si, int(K), total, img, mis, L); break;
-        case 4: gather_in<4>(si, int(K), total, img, mis, L); break;
-        default: gather_in<8>(si, int(K), total, img, mis, L); break;
+        case 1: gather_place<1>(si, int(K), nr, stg, img, mis, L); break;
+        case 2: gather_place<2>(si, int(K), nr, stg, img, mis, L); break;
+        case 4: gather_place<4>(si, int(K), nr, stg, img, mis, L); break;
+        default: gather_place<8>(si, int(K), nr, stg, img, mis, L); break;
       }
       __syncthreads();
       // image [mis, mis + n) -> each replica's [wide_off, wide_off + n)
@@ -281,11 +335,13 @@ __global__ void __launch_bounds__(kTThreads, 3)
       }
       __syncthreads();
       switch (U) {
-        case 1: scatter_out<1>(si, int(K), total, img, mis, L, ptrs); break;
-        case 2: scatter_out<2>(si, int(K), total, img, mis, L, ptrs); break;
-        case 4: scatter_out<4>(si, int(K), total, img, mis, L, ptrs); break;
-        default: scatter_out<8>(si, int(K), total, img, mis, L, ptrs); break;
+        case 1: scatter_stage<1>(si, int(K), nr, img, mis, L, stg); break;
+        case 2: scatter_stage<2>(si, int(K), nr, img, mis, L, stg); break;
+        case 4: scatter_stage<4>(si, int(K), nr, img, mis, L, stg); break;
+        default: scatter_stage<8>(si, int(K), nr, img, mis, L, stg); break;
       }
+      __syncthreads();
+      scatter_write(si, int(K), stg, ptrs);
     }
   }
 }
@@ -309,10 +365,10 @@ reshard_status_t launch_transposes(const reshard_plan_s* plan, const Program& pr
     auto it = g_t_occ.find(dev);
     if (it == g_t_occ.end()) {
       ce = cudaFuncSetAttribute(reinterpret_cast<const void*>(reshard_transpose_kernel),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kImageBytes);
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
       if (ce == cudaSuccess)
         ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &bps, reinterpret_cast<const void*>(reshard_transpose_kernel), kTThreads, kImageBytes);
+            &bps, reinterpret_cast<const void*>(reshard_transpose_kernel), kTThreads, kDynSmem);
       if (ce != cudaSuccess)
         return fail(RESHARD_ERR_CUDA, std::string("transpose kernel set-up: ") + cudaGetErrorString(ce));
       bps = bps > 0 ? bps : 1;
@@ -335,7 +391,7 @@ reshard_status_t launch_transposes(const reshard_plan_s* plan, const Program& pr
   const unsigned grid = unsigned(tp.nblocks < max_grid ? tp.nblocks : max_grid);
   void* args[] = {&tp};
   ce = cudaLaunchKernel(reinterpret_cast<const void*>(reshard_transpose_kernel), dim3(grid),
-                        dim3(kTThreads), args, kImageBytes, static_cast<cudaStream_t>(stream));
+                        dim3(kTThreads), args, kDynSmem, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(ce));
   return RESHARD_OK;
