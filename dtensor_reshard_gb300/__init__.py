@@ -128,6 +128,8 @@ def _load():
         "reshard_plan_upload": ([vp], ctypes.c_int),
         "reshard_execute": ([vp, vpp, vpp, vp], ctypes.c_int),
         "reshard_execute_ex": ([vp, vpp, vpp, ctypes.c_int32, vp], ctypes.c_int),
+        "reshard_plan_path": ([vp, vpp, vpp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                               ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
         "gather_broadcast_execute": ([vp, vpp, vpp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "gather_broadcast_execute_static": ([vp, vpp, vpp, vp], ctypes.c_int),
         "reshard_device_status": ([ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
@@ -358,6 +360,18 @@ def reshard_execute(plan: Plan, src_ptrs, dst_ptrs, stream=None):
 def reshard_execute_ex(plan: Plan, src_ptrs, dst_ptrs, kernel: int, stream=None):
     _check(_lib.reshard_execute_ex(plan, _ptr_array(src_ptrs), _ptr_array(dst_ptrs),
                                    int(kernel), _stream(stream)), "reshard_execute_ex")
+
+
+PATHS = {0: "none", 1: "vector", 2: "tma_fanout", 3: "realign", 4: "staged", 5: "staged_bulk"}
+
+
+def reshard_plan_path(plan: Plan, src_ptrs, dst_ptrs, kernel: int = 0):
+    """(path name, access width in bytes) that reshard_execute_ex would take with these
+    buffers; decided on the host, nothing is launched."""
+    path, width = ctypes.c_int32(), ctypes.c_int32()
+    _check(_lib.reshard_plan_path(plan, _ptr_array(src_ptrs), _ptr_array(dst_ptrs), int(kernel),
+                                  ctypes.byref(path), ctypes.byref(width)), "reshard_plan_path")
+    return PATHS[int(path.value)], int(width.value)
 
 
 def gather_broadcast_execute(plan: Plan, src_ptrs, dst_ptrs, full_scratch, scratch_bytes: int,

@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["planner.cpp", "batch.cpp", "kernels.cu", "bulk_fanout.cu", "transpose.cu",
-           "static_scratch.cu"]
+           "static_scratch.cu", "realign_staged.cu"]
+HEADERS = ["internal.h", "staging.cuh"]
 
 
 def nvcc() -> str:
@@ -39,7 +40,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
     """Compile and link libreshard.so; returns its path.  Raises on failure."""
     os.makedirs(BUILD_DIR, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
-    deps = srcs + [os.path.join(CSRC, "internal.h"), os.path.join(INCLUDE, "reshard.h")]
+    deps = srcs + [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "reshard.h")]
     if (not force and os.path.exists(LIB_PATH)
             and os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(d) for d in deps)):
         return LIB_PATH

@@ -27,182 +27,18 @@
 #include <string>
 
 #include "internal.h"
+#include "staging.cuh"
 
 namespace rs {
 namespace {
 
+using namespace staging;
+
 constexpr int kStages = 2;
 constexpr uint32_t kStageBytes = 32 * 1024;
 constexpr int kStagedThreads = 64;
-// try_wait polls before a wait is declared lost (a poll may suspend the thread
-// for a short, hardware-defined time: this is of the order of a second).
-constexpr uint32_t kWaitPolls = 1u << 22;
-
-enum : unsigned int {
-  kStatusProducerWait = 1,  // producer gave up waiting for a free stage
-  kStatusConsumerWait = 2,  // consumer gave up waiting for a loaded stage
-  kStatusSelfTest = 3       // the self-test's deliberately unanswered wait ran out
-};
 
 __device__ unsigned int g_device_status;
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive_expect(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-// Wait for the phase with the given parity to complete; false after `polls` polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t polls) {
-  for (uint32_t i = 0; i < polls; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
-        "selp.u32 %0, 1, 0, p; }"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(sdst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_addr(ssrc)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_all_but_newest() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// One chunk: at most kStageBytes of one tile.
-struct Chunk {
-  int ti;
-  uint32_t kind;   // 0: piece [a, b) of a run; 1: whole rows [a, b); 2: bytes [b, b+bytes) of row a
-  int64_t a, b;
-  uint32_t bytes;
-};
-
-// Walks the chunks of this CTA's unit range; the producer and the consumer each
-// run their own copy and see the same sequence.
-struct ChunkWalker {
-  const KernelParams* p;
-  int64_t u0, u1;
-  int ti;
-  int64_t pos, end;
-  uint32_t kind, per;  // per: rows per chunk (kind 1) or pieces per row (kind 2)
-  reshard_tile_t t;
-  bool live;
-
-  __device__ void enter_tile() {
-    t = p->tiles[ti];
-    const int64_t tb = p->prefix[ti], te = p->prefix[ti + 1];
-    const int64_t a = u0 - tb, b = (u1 < te ? u1 : te) - tb;
-    if (t.nrows == 1 && t.nplanes == 1) {
-      kind = 0;
-      pos = a * kUnitBytes;
-      end = min(b * kUnitBytes, int64_t(t.row_bytes));
-      return;
-    }
-    const int64_t upr = t.row_bytes >= kUnitBytes ? 1 : kUnitBytes / t.row_bytes;
-    const int64_t rows = int64_t(t.nrows) * t.nplanes;
-    const int64_t r0 = a * upr, r1 = min(b * upr, rows);
-    if (t.row_bytes <= kStageBytes) {
-      kind = 1;
-      per = kStageBytes / t.row_bytes;
-      pos = r0;
-      end = r1;
-    } else {
-      kind = 2;
-      per = (t.row_bytes + kStageBytes - 1) / kStageBytes;
-      pos = r0 * per;
-      end = r1 * per;
-    }
-  }
-  __device__ void start(const KernelParams* kp) {
-    p = kp;
-    u0 = kp->total_units * int64_t(blockIdx.x) / int64_t(gridDim.x);
-    u1 = kp->total_units * int64_t(blockIdx.x + 1) / int64_t(gridDim.x);
-    live = u0 < u1;
-    if (!live) return;
-    int lo = 0, hi = kp->ntiles - 1;  // largest tile with prefix <= u0
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (kp->prefix[mid] <= u0) lo = mid;
-      else hi = mid - 1;
-    }
-    ti = lo;
-    enter_tile();
-  }
-  __device__ bool next(Chunk* c) {
-    while (live && pos >= end) {
-      const int64_t te = p->prefix[ti + 1];
-      if (te >= u1) {
-        live = false;
-        break;
-      }
-      u0 = te;
-      ++ti;
-      enter_tile();
-    }
-    if (!live) return false;
-    c->ti = ti;
-    c->kind = kind;
-    if (kind == 0) {
-      const int64_t e = min(end, pos + int64_t(kStageBytes));
-      c->a = pos;
-      c->b = e;
-      c->bytes = uint32_t(e - pos);
-      pos = e;
-    } else if (kind == 1) {
-      const int64_t e = min(end, pos + int64_t(per));
-      c->a = pos;
-      c->b = e;
-      c->bytes = uint32_t((e - pos) * t.row_bytes);
-      pos = e;
-    } else {
-      const int64_t row = pos / per, piece = pos - row * per;
-      const int64_t b0 = piece * kStageBytes;
-      const int64_t b1 = min(int64_t(t.row_bytes), b0 + int64_t(kStageBytes));
-      c->a = row;
-      c->b = b0;
-      c->bytes = uint32_t(b1 - b0);
-      pos += 1;
-    }
-    return true;
-  }
-};
-
-__device__ __forceinline__ int64_t src_row(const reshard_tile_t& t, int64_t r) {
-  const int64_t pl = r / t.nrows, q = r - pl * t.nrows;
-  return t.src_off + pl * t.src_plane_stride + q * t.src_row_stride;
-}
-__device__ __forceinline__ int64_t dst_row(const reshard_tile_t& t, int64_t r) {
-  const int64_t pl = r / t.nrows, q = r - pl * t.nrows;
-  return t.dst_off + pl * t.dst_plane_stride + q * t.dst_row_stride;
-}
 
 __global__ void __launch_bounds__(kStagedThreads)
     fanout_staged_kernel(const __grid_constant__ KernelParams p, unsigned int* status) {
@@ -219,7 +55,7 @@ __global__ void __launch_bounds__(kStagedThreads)
   }
   __syncthreads();
 
-  ChunkWalker w;
+  ChunkWalker<kStageBytes, 0> w;
   w.start(&p);
   Chunk c;
   uint32_t n = 0;
@@ -344,6 +180,14 @@ reshard_status_t device_state(DeviceState* out) {
 }
 
 }  // namespace
+
+reshard_status_t device_status_word(unsigned int** status) {
+  DeviceState d;
+  reshard_status_t st = device_state(&d);
+  if (st != RESHARD_OK) return st;
+  *status = d.status;
+  return RESHARD_OK;
+}
 
 reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelParams& kp,
                                       void* stream) {

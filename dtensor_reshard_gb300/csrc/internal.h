@@ -22,11 +22,28 @@ constexpr int64_t kMaxRunBytes = int64_t(1) << 30;
 // Largest destination group one tile fans out to (larger groups are split).
 constexpr int kMaxGroup = 256;
 
+// Fixed work of one row (offsets, partial first and last words, a row-table
+// entry), counted in bytes of streaming when rows are grouped into units.
+constexpr int64_t kRowCostBytes = 256;
+
+#ifdef __CUDACC__
+#define RS_HOST_DEVICE __host__ __device__
+#else
+#define RS_HOST_DEVICE
+#endif
+
+// Rows per work unit of a multi-row tile: rows whose bytes plus fixed work
+// come to about kUnitBytes (at least one).
+RS_HOST_DEVICE inline uint32_t rows_per_unit(uint32_t row_bytes) {
+  const int64_t cost = int64_t(row_bytes) + kRowCostBytes;
+  return cost >= kUnitBytes ? 1u : uint32_t(kUnitBytes / cost);
+}
+
 // Work units of a tile (must match the kernels' reading of a tile).
 inline int64_t tile_units(const reshard_tile_t& t) {
   if (t.nrows == 1 && t.nplanes == 1) return (int64_t(t.row_bytes) + kUnitBytes - 1) / kUnitBytes;
-  int64_t rows = int64_t(t.nrows) * int64_t(t.nplanes);
-  int64_t upr = t.row_bytes >= kUnitBytes ? 1 : kUnitBytes / t.row_bytes;
+  const int64_t rows = int64_t(t.nrows) * int64_t(t.nplanes);
+  const int64_t upr = rows_per_unit(t.row_bytes);
   return (rows + upr - 1) / upr;
 }
 
@@ -40,11 +57,14 @@ struct KernelParams {
   int64_t total_units;
   int32_t ntiles;
   int32_t nbufs;
-  uint32_t flags;  // kFlagDstCongruent: every destination buffer has the same address mod 16
+  uint32_t flags;  // kFlag* bits below
   uint32_t pad;
   unsigned char* bufs[RESHARD_MAX_EXEC_BUFFERS];
 };
 constexpr uint32_t kFlagDstCongruent = 1u;
+// The realigning staged kernel writes whole granules with bulk copies from an
+// output stage (only together with kFlagDstCongruent).
+constexpr uint32_t kFlagBulkStores = 2u;
 
 struct Box {
   int64_t off[RESHARD_MAX_TENSOR_NDIM];
@@ -78,6 +98,7 @@ struct Program {
   int max_fanout = 0;       // largest destination group
   int64_t tile_bytes = 0;   // source bytes of all tiles
   int64_t long_row_bytes = 0;  // ... of those in rows of at least 512 bytes (runs included)
+  int64_t wide_row_bytes = 0;  // ... of those in rows of at least 8 KiB (runs included)
   int64_t total_units() const { return prefix.empty() ? 0 : prefix.back(); }
   // transpose blocks (narrow innermost pieces grouped by shared rows)
   std::vector<reshard_tblock_t> tblocks;
@@ -140,9 +161,24 @@ reshard_status_t launch_program_tables(const Program& p, const reshard_tile_t* d
                                        const int64_t* d_prefix, const uint32_t* d_goff,
                                        const uint16_t* d_gbuf, int num_sms,
                                        unsigned char* const* bufs, int nbufs, void* stream);
+// The copy path an execution of `prog` with buffer table bufs[nbufs] takes
+// (host-side decision, no device access).  allow_tma_fanout: false for the
+// allocation-free entry point, whose programs never use the TMA fan-out.
+struct Dispatch {
+  int path = RESHARD_PATH_NONE;  // reshard_path_t
+  int w_log2 = 0;                // widest common access, log2 bytes
+  int kidx = 0;                  // copy-kernel table index (kernels.cu)
+  uint32_t flags = 0;            // kFlag* bits for the kernel
+};
+Dispatch decide(const Program& prog, unsigned char* const* bufs, int nbufs, bool allow_tma_fanout);
 // TMA-staged fan-out (bulk_fanout.cu) for a 16-byte-aligned program.
 reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelParams& kp,
                                       void* stream);
+// TMA-staged realigning copy (realign_staged.cu) for a program that is not
+// 16-byte aligned, on a grid of num_sms x its resident CTAs per SM.
+reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, void* stream);
+// Device address of the status word that bounded waits report into (bulk_fanout.cu).
+reshard_status_t device_status_word(unsigned int** status);
 // Transpose blocks of a program (transpose.cu); no-op when it has none.
 reshard_status_t launch_transposes(const reshard_plan_s* plan, const Program& prog,
                                    unsigned char* const* bufs, int nbufs, uint32_t flags,

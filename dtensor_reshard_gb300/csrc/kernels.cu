@@ -28,6 +28,7 @@
 #include <utility>
 
 #include "internal.h"
+#include "staging.cuh"
 
 namespace rs {
 namespace {
@@ -100,7 +101,7 @@ __device__ __forceinline__ void copy_run(const unsigned char* __restrict__ src,
 // planes x rows: row r = p * nrows + q starts at src + p*sps + q*srs and at
 // dofs + p*dps + q*drs in every destination (PLANES = false: one plane).
 // Rows are vpr vectors of W bytes.  Rows of at least kThreads vectors are
-// streamed one at a time by the whole CTA; shorter rows are packed
+// streamed as one flat range of vectors by the whole CTA; shorter rows are packed
 // kThreads / vpr to a pass, one thread per vector, and every thread carries
 // kUnroll rows at once.
 template <int W, bool PLANES>
@@ -122,9 +123,40 @@ __device__ __forceinline__ void copy_rows(const reshard_tile_t& t, const unsigne
     return int64_t(p) * t.dst_plane_stride + int64_t(r - p * t.nrows) * t.dst_row_stride;
   };
   if (vpr >= uint32_t(kThreads)) {
+    // long rows: the block walks (row, vector) pairs flat, kThreads vectors apart,
+    // so every thread keeps kUnroll loads in flight whatever the row length.  As
+    // vpr >= kThreads a step crosses at most one row boundary.  The store cursor
+    // repeats the load cursor's walk instead of holding kUnroll offsets.
+    uint32_t lrow = r_begin, lcol = threadIdx.x;
+    int64_t lbase = src_row(lrow);
+    uint32_t srow = r_begin, scol = threadIdx.x;
+    int64_t sbase = t.dst_off + dst_row(srow);
 #pragma unroll 1
-    for (uint32_t row = r_begin; row < r_end; ++row)
-      copy_run<W>(s0 + src_row(row), sdst, R, t.dst_off + dst_row(row), t.row_bytes);
+    while (lrow < r_end) {
+      V v[kUnroll];
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        if (lrow < r_end) v[k] = load_stream<V>(s0 + lbase + int64_t(lcol) * W);
+        lcol += kThreads;
+        if (lcol >= vpr) {
+          lcol -= vpr;
+          lbase = src_row(++lrow);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        if (srow < r_end) {
+          const int64_t d = sbase + int64_t(scol) * W;
+#pragma unroll 1
+          for (int j = 0; j < R; ++j) store_stream<V>(sdst[j] + d, v[k]);
+        }
+        scol += kThreads;
+        if (scol >= vpr) {
+          scol -= vpr;
+          sbase = t.dst_off + dst_row(++srow);
+        }
+      }
+    }
     return;
   }
   const uint32_t step = uint32_t(kThreads) / vpr;  // rows per pass
@@ -191,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, PLANES ? 2 : 4)
       const int64_t b1 = min(b * kUnitBytes, int64_t(t.row_bytes));
       copy_run<W>(src + t.src_off + b0, s_dst, R, t.dst_off + b0, uint32_t(b1 - b0));
     } else {
-      const uint32_t upr = t.row_bytes >= kUnitBytes ? 1u : uint32_t(kUnitBytes) / t.row_bytes;
+      const uint32_t upr = rows_per_unit(t.row_bytes);
       const uint64_t rows = uint64_t(t.nrows) * t.nplanes;
       const uint32_t r_begin = uint32_t(a * upr);
       const uint32_t r_end = uint32_t(min(uint64_t(b) * upr, rows));
@@ -218,18 +250,7 @@ __device__ __forceinline__ uint4 load16_cached(const unsigned char* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// Bytes [o, o + 16) of the 32 bytes A:B, with q = o / 4 and
-// sel = 0x3210 + 0x1111 * (o % 4) (byte-permute selector).
-__device__ __forceinline__ uint4 funnel16(const uint4& A, const uint4& B, uint32_t q,
-                                          uint32_t sel) {
-  const uint32_t x0 = q == 0 ? A.x : q == 1 ? A.y : q == 2 ? A.z : A.w;
-  const uint32_t x1 = q == 0 ? A.y : q == 1 ? A.z : q == 2 ? A.w : B.x;
-  const uint32_t x2 = q == 0 ? A.z : q == 1 ? A.w : q == 2 ? B.x : B.y;
-  const uint32_t x3 = q == 0 ? A.w : q == 1 ? B.x : q == 2 ? B.y : B.z;
-  const uint32_t x4 = q == 0 ? B.x : q == 1 ? B.y : q == 2 ? B.z : B.w;
-  return make_uint4(__byte_perm(x0, x1, sel), __byte_perm(x1, x2, sel), __byte_perm(x2, x3, sel),
-                    __byte_perm(x3, x4, sel));
-}
+using staging::funnel16;
 
 constexpr int kRealignUnroll = 4;
 
@@ -336,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, PLANES ? 2 : 3)
     __syncthreads();
     const unsigned char* src = p.bufs[t.src_buf];
     const bool run = t.nrows == 1 && t.nplanes == 1;
-    const uint32_t upr = t.row_bytes >= kUnitBytes ? 1u : uint32_t(kUnitBytes) / t.row_bytes;
+    const uint32_t upr = rows_per_unit(t.row_bytes);
     const uint64_t rows = uint64_t(t.nrows) * t.nplanes;
     const uint32_t r_begin = run ? 0u : uint32_t(a * upr);
     const uint32_t r_end = run ? 1u : uint32_t(min(uint64_t(b) * upr, rows));
@@ -388,6 +409,21 @@ __global__ void __launch_bounds__(kThreads, PLANES ? 2 : 3)
 
 using KernelFn = void (*)(KernelParams);
 
+// choose_kernel's answer for the TMA-staged realigning kernel (realign_staged.cu).
+constexpr int kStagedRealign = -1;
+// Source bytes from which a fan-out program goes through that kernel, and
+// from which a one-replica program with 4-byte elements does.
+constexpr int64_t kStagedFanoutMinBytes = int64_t(48) << 20;
+constexpr int64_t kStagedW4MinBytes = int64_t(128) << 20;
+// Fan-out from which that kernel writes through bulk copies from an output
+// stage (when most bytes are in rows of at least 8 KiB: a bulk copy per row
+// and replica costs the copy engine about as much as 1 KB of streaming).
+constexpr int kBulkStoreFanout = 2;
+
+bool bulk_stores(const Program& prog) {
+  return prog.max_fanout >= kBulkStoreFanout && 2 * prog.wide_row_bytes >= prog.tile_bytes;
+}
+
 // Instantiations indexed by [log2 W][planes].
 // [0]: realigning kernel (any alignment); [k], k = 1..4: 2^k-byte vector kernel;
 // [5]: byte kernel.
@@ -400,14 +436,27 @@ const KernelFn kKernels[6][2] = {
     {reshard_copy_kernel<1, false>, reshard_copy_kernel<1, true>},
 };
 
-// Kernel for a program whose widest common access is 2^w_log2 bytes: the
-// 16-byte vector kernel when everything is aligned; otherwise the realigning
-// kernel when the program fans out to several replicas over mostly long rows
-// (16-byte stores then pay for the byte permutes), else the element-width
-// kernel (measured on the uneven-stress tensors).
+// Kernel for a program whose widest common access is 2^w_log2 bytes (rule
+// fitted to per-tensor timings of the uneven-stress tensors):
+//   everything 16-byte aligned: the 16-byte vector kernel (or the TMA fan-out);
+//   fan-out to several replicas: the TMA-staged realigning kernel with bulk
+//     stores when most bytes are in rows of at least 8 KiB and the program is
+//     large enough to fill its pipelines, else the register realigning kernel
+//     when most bytes are in rows of at least 512 bytes;
+//   one replica, rows of at least 512 bytes: the staged kernel when the
+//     element width would be 1 or 2 bytes, or 4 bytes in a large program (its
+//     loads stay wide whatever the alignment);
+//   otherwise the element-width kernel.
 int choose_kernel(const Program& prog, int w_log2) {
   if (w_log2 == 4) return 4;
-  if (prog.max_fanout >= 2 && 2 * prog.long_row_bytes >= prog.tile_bytes) return 0;
+  const bool long_rows = 2 * prog.long_row_bytes >= prog.tile_bytes;
+  const bool wide_rows = 2 * prog.wide_row_bytes >= prog.tile_bytes;
+  if (prog.max_fanout >= 2) {
+    if (wide_rows && prog.tile_bytes >= kStagedFanoutMinBytes) return kStagedRealign;
+    if (long_rows) return 0;
+  } else if (long_rows && (w_log2 <= 1 || (w_log2 == 2 && prog.tile_bytes >= kStagedW4MinBytes))) {
+    return kStagedRealign;
+  }
   return w_log2 == 0 ? 5 : w_log2;
 }
 
@@ -447,6 +496,33 @@ reshard_status_t occupancy(int device, int w_log2, int planes, int* blocks) {
 
 }  // namespace
 
+Dispatch decide(const Program& prog, unsigned char* const* bufs, int nbufs, bool allow_tma_fanout) {
+  Dispatch d;
+  if (prog.total_units() == 0) return d;
+  // widest access every tile of the program allows with these buffers
+  uint64_t align = prog.align_bits;
+  for (int i = 0; i < nbufs; ++i) align |= reinterpret_cast<uint64_t>(bufs[i]);
+  d.w_log2 = 4;
+  while (d.w_log2 > 0 && (align & ((uint64_t(1) << d.w_log2) - 1)) != 0) --d.w_log2;
+  d.flags = destinations_congruent(prog, bufs) ? kFlagDstCongruent : 0u;
+  if (allow_tma_fanout && prog.staged && d.w_log2 == 4) {
+    d.path = RESHARD_PATH_TMA_FANOUT;
+    return d;
+  }
+  d.kidx = choose_kernel(prog, d.w_log2);
+  if (d.kidx == kStagedRealign) {
+    if (bulk_stores(prog)) d.flags |= kFlagBulkStores;
+    d.path = (d.flags & kFlagDstCongruent) && (d.flags & kFlagBulkStores)
+                 ? RESHARD_PATH_STAGED_BULK
+                 : RESHARD_PATH_STAGED;
+  } else if (d.kidx == 0) {
+    d.path = RESHARD_PATH_REALIGN;
+  } else {
+    d.path = RESHARD_PATH_VECTOR;
+  }
+  return d;
+}
+
 reshard_status_t copy_kernel_occupancy(int* blocks_per_sm) {
   int dev = 0;
   cudaError_t ce = cudaGetDevice(&dev);
@@ -464,11 +540,7 @@ static reshard_status_t launch_tiles(const reshard_plan_s* plan, const Program& 
   if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device)
     return fail(RESHARD_ERR_INVALID_ARG, "current device differs from the plan's device");
 
-  // Widest access every tile of the program allows with these buffers.
-  uint64_t align = prog.align_bits;
-  for (int i = 0; i < nbufs; ++i) align |= reinterpret_cast<uint64_t>(bufs[i]);
-  int w_log2 = 4;
-  while (w_log2 > 0 && (align & ((uint64_t(1) << w_log2) - 1)) != 0) --w_log2;
+  const Dispatch d = decide(prog, bufs, nbufs, true);
   KernelParams kp;
   kp.tiles = prog.d_tiles;
   kp.prefix = prog.d_prefix;
@@ -479,15 +551,15 @@ static reshard_status_t launch_tiles(const reshard_plan_s* plan, const Program& 
   kp.nbufs = nbufs;
   for (int i = 0; i < nbufs; ++i) kp.bufs[i] = bufs[i];
   for (int i = nbufs; i < RESHARD_MAX_EXEC_BUFFERS; ++i) kp.bufs[i] = nullptr;
-
-  kp.flags = destinations_congruent(prog, bufs) ? kFlagDstCongruent : 0u;
+  kp.flags = d.flags;
   kp.pad = 0;
 
   // A fully 16-byte-aligned fan-out goes through the TMA-staged pipeline.
-  if (prog.staged && w_log2 == 4) return launch_fanout_staged(plan, kp, stream);
+  if (d.path == RESHARD_PATH_TMA_FANOUT) return launch_fanout_staged(plan, kp, stream);
+  if (d.kidx == kStagedRealign) return launch_realign_staged(plan->num_sms, kp, stream);
 
   const int planes = prog.has_planes ? 1 : 0;
-  const int kidx = choose_kernel(prog, w_log2);
+  const int kidx = d.kidx;
   int bps = 1;
   reshard_status_t st = occupancy(dev, kidx, planes, &bps);
   if (st != RESHARD_OK) return st;
@@ -528,15 +600,14 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
-  uint64_t align = prog.align_bits;
-  for (int i = 0; i < nbufs; ++i) align |= reinterpret_cast<uint64_t>(bufs[i]);
-  int w_log2 = 4;
-  while (w_log2 > 0 && (align & ((uint64_t(1) << w_log2) - 1)) != 0) --w_log2;
+  const Dispatch d = decide(prog, bufs, nbufs, false);
   const int planes = prog.has_planes ? 1 : 0;
-  const int kidx = choose_kernel(prog, w_log2);
+  const int kidx = d.kidx;
   int bps = 1;
-  reshard_status_t st = occupancy(dev, kidx, planes, &bps);
-  if (st != RESHARD_OK) return st;
+  if (kidx != kStagedRealign) {
+    reshard_status_t st = occupancy(dev, kidx, planes, &bps);
+    if (st != RESHARD_OK) return st;
+  }
 
   KernelParams kp;
   kp.tiles = d_tiles;
@@ -548,8 +619,9 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
   kp.nbufs = nbufs;
   for (int i = 0; i < nbufs; ++i) kp.bufs[i] = bufs[i];
   for (int i = nbufs; i < RESHARD_MAX_EXEC_BUFFERS; ++i) kp.bufs[i] = nullptr;
-  kp.flags = destinations_congruent(prog, bufs) ? kFlagDstCongruent : 0u;
+  kp.flags = d.flags;
   kp.pad = 0;
+  if (kidx == kStagedRealign) return launch_realign_staged(num_sms, kp, stream);
 
   const int64_t max_grid = int64_t(num_sms) * bps;
   const unsigned grid = unsigned(total < max_grid ? total : max_grid);

@@ -265,6 +265,7 @@ void finish_program(Program& P) {
     const int64_t bytes = int64_t(t.row_bytes) * t.nrows * t.nplanes;
     P.tile_bytes += bytes;
     if (t.row_bytes >= 512) P.long_row_bytes += bytes;
+    if (t.row_bytes >= 8192) P.wide_row_bytes += bytes;
   }
   for (size_t g = 0; g + 1 < P.goff.size(); ++g)
     P.max_fanout = std::max<int>(P.max_fanout, int(P.goff[g + 1] - P.goff[g]));
@@ -975,6 +976,25 @@ reshard_status_t reshard_execute_ex(reshard_plan_t plan, const void* const* src_
   const rs::Program& p =
       plan->prog[kernel == RESHARD_KERNEL_FANOUT ? RESHARD_PROGRAM_FANOUT : RESHARD_PROGRAM_BOXCOPY];
   return rs::launch_program(plan, p, bufs.data(), int(bufs.size()), stream);
+}
+
+reshard_status_t reshard_plan_path(reshard_plan_t plan, const void* const* src_ptrs,
+                                   void* const* dst_ptrs, int32_t kernel, int32_t* path,
+                                   int32_t* width) {
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (kernel != RESHARD_KERNEL_FANOUT && kernel != RESHARD_KERNEL_BOXCOPY)
+    return fail(RESHARD_ERR_INVALID_ARG, "unknown kernel");
+  std::vector<unsigned char*> bufs;
+  reshard_status_t st = rs::buffer_table(plan, src_ptrs, dst_ptrs, nullptr, &bufs);
+  if (st != RESHARD_OK) return st;
+  if (bufs.size() > size_t(RESHARD_MAX_EXEC_BUFFERS))
+    return fail(RESHARD_ERR_UNSUPPORTED, "too many buffers");
+  const rs::Program& p =
+      plan->prog[kernel == RESHARD_KERNEL_FANOUT ? RESHARD_PROGRAM_FANOUT : RESHARD_PROGRAM_BOXCOPY];
+  const rs::Dispatch d = rs::decide(p, bufs.data(), int(bufs.size()), true);
+  if (path) *path = d.path;
+  if (width) *width = 1 << d.w_log2;
+  return RESHARD_OK;
 }
 
 reshard_status_t reshard_execute(reshard_plan_t plan, const void* const* src_ptrs,

@@ -112,6 +112,17 @@ typedef enum reshard_kernel {
   RESHARD_KERNEL_BOXCOPY = 1
 } reshard_kernel_t;
 
+/* Copy path of an execution's tiles (reshard_plan_path); transpose blocks,
+ * when a program has any, always run in their own kernel after the tiles. */
+typedef enum reshard_path {
+  RESHARD_PATH_NONE = 0,        /* the program has no tiles */
+  RESHARD_PATH_VECTOR = 1,      /* element-width vector kernel (1..16-byte accesses) */
+  RESHARD_PATH_TMA_FANOUT = 2,  /* 16-byte aligned: TMA bulk copies through shared memory */
+  RESHARD_PATH_REALIGN = 3,     /* aligned 16-byte loads and stores, bytes realigned in registers */
+  RESHARD_PATH_STAGED = 4,      /* TMA-staged realigning copy, stores from registers */
+  RESHARD_PATH_STAGED_BULK = 5  /* TMA-staged realigning copy, bulk stores to every replica */
+} reshard_path_t;
+
 /* Copy programs a plan holds (for inspection and for the CPU test executor). */
 typedef enum reshard_program {
   RESHARD_PROGRAM_FANOUT = 0,  /* reshard, read-once fan-out */
@@ -430,9 +441,24 @@ reshard_status_t reshard_plan_transposes(reshard_plan_t plan, int32_t program,
                                          const reshard_tseg_t** segs, int64_t* nsegs);
 
 /*
+ * The copy path reshard_execute_ex(plan, src_ptrs, dst_ptrs, kernel, ...)
+ * would take with these buffers, decided on the host exactly as an execution
+ * decides it (from the tiles' offsets, strides and row lengths, the buffers'
+ * addresses mod 16, the fan-out and the program's size); nothing is launched
+ * and no device memory is touched, so any pointers that pass the execution's
+ * argument checks may be given.  *path receives a reshard_path_t, *width the
+ * widest access in bytes every tile allows (1..16).  Either output may be
+ * NULL.  Errors: BAD_HANDLE, INVALID_ARG (as reshard_execute_ex), UNSUPPORTED.
+ */
+reshard_status_t reshard_plan_path(reshard_plan_t plan, const void* const* src_ptrs,
+                                   void* const* dst_ptrs, int32_t kernel, int32_t* path,
+                                   int32_t* width);
+
+/*
  * Work units of a tile: a single-row tile is split into 4096-byte units, a
- * multi-row tile into units of max(1, 4096 / row_bytes) rows.  Each CTA of a
- * copy kernel takes an equal share of a program's units.  Returns 0 for NULL.
+ * multi-row tile into units of max(1, 4096 / (row_bytes + 256)) rows (256
+ * bytes stand for each row's fixed work).  Each CTA of a copy kernel takes an
+ * equal share of a program's units.  Returns 0 for NULL.
  */
 int64_t reshard_tile_units(const reshard_tile_t* tile);
 

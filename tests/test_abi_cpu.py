@@ -168,3 +168,55 @@ def test_batch_host_checks():
     with pytest.raises(rs.ReshardError) as e:
         rs.reshard_batch_create(big)
     assert e.value.status == 2
+
+
+def _fake_ptrs(plan, side, n, mis):
+    """Distinct 256-byte aligned fake addresses + mis(rank); NULL for empty shards."""
+    out = []
+    for r in range(n):
+        shp, _ = rs.reshard_plan_local_shape(plan, side, r)
+        out.append(0 if 0 in shp else ((r + 1 + 4096 * side) << 24) + mis(r))
+    return out
+
+
+@pytest.mark.parametrize("gshape,dtype,sm,sp,dm,dp,smis,dmis,kernel,want", [
+    # 16-byte aligned: TMA fan-out, or the 16-byte vector kernel for box copies
+    ((1024, 1024), "bf16", (2,), ("S0",), (4,), ("S1",), 0, 0, 0, ("tma_fanout", 16)),
+    ((1024, 1024), "bf16", (2,), ("S0",), (4,), ("S1",), 0, 0, 1, ("vector", 16)),
+    # one replica, long rows, 2-byte or 1-byte alignment: staged realigning copy
+    ((2000, 1301), "bf16", (3,), ("S0",), (2,), ("S0",), 0, 0, 0, ("staged", 2)),
+    ((2000, 1301), "bf16", (3,), ("S0",), (2,), ("S0",), 3, 3, 0, ("staged", 1)),
+    # one replica, 8-byte alignment: element kernel
+    ((6971, 7418), "fp32", (49,), ("S1",), (10,), ("S1",), 0, 0, 0, ("vector", 8)),
+    # short rows (< 512 bytes): element kernel
+    ((1000, 37), "bf16", (3,), ("S1",), (7,), ("S0",), 0, 0, 0, ("vector", 2)),
+    # fan-out, small or not in wide rows: register realigning kernel
+    ((2000, 1301), "bf16", (3,), ("S0",), (2,), ("R",), 3, 3, 0, ("realign", 1)),
+    # fan-out of 52.8 MB in 16 MB runs: bulk stores, unless the replicas differ mod 16
+    ((4400, 6001), "bf16", (3,), ("S0",), (2,), ("R",), 0, 6, 0, ("staged_bulk", 2)),
+    ((4400, 6001), "bf16", (3,), ("S0",), (2,), ("R",), 0, 5, 0, ("staged", 1)),
+])
+def test_plan_path_dispatch_rule(gshape, dtype, sm, sp, dm, dp, smis, dmis, kernel, want):
+    p = rs.reshard_plan_create(gshape, dtype, sm, sp, dm, dp)
+    src = _fake_ptrs(p, 0, p.n_src, lambda r: smis)
+    # dmis == 5: replica r sits 5 * r bytes past its alignment (incongruent replicas)
+    dst = _fake_ptrs(p, 1, p.n_dst, (lambda r: 5 * r) if dmis == 5 else (lambda r: dmis))
+    assert rs.reshard_plan_path(p, src, dst, kernel) == want
+
+
+def test_plan_path_argument_checks():
+    p = rs.reshard_plan_create((8, 8), "bf16", (2,), ("S0",), (4,), ("S1",))
+    src = _fake_ptrs(p, 0, 2, lambda r: 0)
+    dst = _fake_ptrs(p, 1, 4, lambda r: 0)
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_plan_path(p, src, dst, 7)
+    assert e.value.status == 1
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_plan_path(p, [None, src[1]], dst)
+    assert e.value.status == 1
+    empty = rs.reshard_plan_create((0, 7), "bf16", (2,), ("S0",), (3,), ("S1",))
+    assert rs.reshard_plan_path(empty, [None, None], [None] * 3) == ("none", 1)
+    out = ctypes.c_int32(-1)
+    assert rs._lib.reshard_plan_path(p, rs._ptr_array(src), rs._ptr_array(dst), 0, None,
+                                     ctypes.byref(out)) == 0
+    assert out.value == rs.reshard_plan_path(p, src, dst)[1] == 4  # 4-byte rows

@@ -62,7 +62,7 @@ def _upload(arrs, misalign=0):
 
 
 def run_and_compare(oracle, spec, kernel=rs.KERNEL_FANOUT, misalign=0, stream=None,
-                    path="reshard", dst_misalign=None):
+                    path="reshard", dst_misalign=None, expect_path=None):
     _cuda()
     glob = global_tensor(spec)
     srcs = [helpers.to_bytes(s) for s in helpers.scatter_with_oracle(
@@ -75,6 +75,8 @@ def run_and_compare(oracle, spec, kernel=rs.KERNEL_FANOUT, misalign=0, stream=No
     sptr = [g.ptr for g in dsrc]
     dptr = [g.ptr for g in ddst]
     scratch = None
+    if expect_path is not None:
+        assert rs.reshard_plan_path(plan, sptr, dptr, kernel)[0] == expect_path
     if path == "reshard":
         rs.reshard_execute_ex(plan, sptr, dptr, kernel, stream)
     else:
@@ -522,6 +524,53 @@ def test_transpose_blocks(oracle, i, misalign):
     assert blocks, "layout expected to use transpose blocks"
     run_and_compare(oracle, spec, misalign=misalign)
     run_and_compare(oracle, spec, misalign=misalign, dst_misalign=lambda r: (r * 5) % 16)
+
+
+# ---------------------------------------------------------------------- staged realigning copy
+# One case per way the TMA-staged realigning kernel stages and stores a chunk;
+# each asserts the path the execution takes, then checks every byte.
+STAGED_CASES = [
+    # runs, one replica
+    ("runs", _spec((2000, 1301), "bf16", (3,), ("S0",), (2,), ("S0",), seed=11), "staged"),
+    # rows that follow one another in the source: one bulk copy per chunk
+    ("contiguous_rows", _spec((3000, 1203), "bf16", (4,), ("S1",), (3,), ("S0",), seed=12),
+     "staged"),
+    # short rows apart in the source: 16-byte cp.async copies into row slots
+    ("short_rows", _spec((2400, 1203), "bf16", (3,), ("S0",), (2,), ("S1",), seed=13), "staged"),
+    # rows of 5 KB apart in the source: one bulk copy per row slot
+    ("long_rows", _spec((800, 5001), "bf16", (3,), ("S0",), (2,), ("S1",), seed=14), "staged"),
+    # rows of 30 KB: pieces of a row per chunk
+    ("row_pieces", _spec((300, 30001), "bf16", (3,), ("S0",), (2,), ("S1",), seed=15), "staged"),
+    # 3-D tiles with planes
+    ("planes", _spec((6, 500, 701), "bf16", (2,), ("S2",), (3,), ("S1",), seed=16), "staged"),
+]
+
+
+@pytest.mark.parametrize("misalign", [0, 3])
+@pytest.mark.parametrize("i", range(len(STAGED_CASES)))
+def test_staged_realign_paths(oracle, i, misalign):
+    name, spec, want = STAGED_CASES[i]
+    run_and_compare(oracle, spec, misalign=misalign, expect_path=want)
+
+
+# Two replicas of a 52.8 MB bf16 tensor in 16 MB runs: bulk stores from the
+# output stage when the replicas share their address mod 16 (aligned or not),
+# per-replica realignment in registers when they do not.
+BULK_SPEC = _spec((4400, 6001), "bf16", (3,), ("S0",), (2,), ("R",), seed=17)
+
+
+@pytest.mark.parametrize("dst_mis,want", [
+    (lambda r: 0, "staged_bulk"),
+    (lambda r: 6, "staged_bulk"),
+    (lambda r: (r * 5) % 16, "staged"),
+], ids=["aligned", "congruent_misaligned", "incongruent"])
+def test_staged_realign_fanout(oracle, dst_mis, want):
+    run_and_compare(oracle, BULK_SPEC, misalign=0, dst_misalign=dst_mis, expect_path=want)
+
+
+def test_small_misaligned_fanout_uses_register_realign(oracle):
+    spec = _spec((2000, 1301), "bf16", (3,), ("S0",), (2,), ("R",), seed=18)
+    run_and_compare(oracle, spec, misalign=3, expect_path="realign")
 
 
 # ---------------------------------------------------------------------- concurrency
