@@ -125,6 +125,13 @@ def _load():
         "reshard_batch_execute": ([vp, ctypes.POINTER(vpp), ctypes.POINTER(vpp), vp],
                                   ctypes.c_int),
         "reshard_batch_destroy": ([vp], ctypes.c_int),
+        "reshard_refit_create": ([ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                  ctypes.c_uint32, vpp], ctypes.c_int),
+        "reshard_refit_info": ([vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_uint64)],
+                               ctypes.c_int),
+        "reshard_refit_execute": ([vp, ctypes.POINTER(vpp), ctypes.POINTER(vpp), vp, ctypes.c_size_t,
+                                   vp], ctypes.c_int),
+        "reshard_refit_destroy": ([vp], ctypes.c_int),
         "reshard_plan_upload": ([vp], ctypes.c_int),
         "reshard_execute": ([vp, vpp, vpp, vp], ctypes.c_int),
         "reshard_execute_ex": ([vp, vpp, vpp, ctypes.c_int32, vp], ctypes.c_int),
@@ -346,6 +353,76 @@ def reshard_batch_destroy(batch: Batch):
     st = _lib.reshard_batch_destroy(batch)
     batch.handle = None
     _check(st, "reshard_batch_destroy")
+
+
+ROUTE_AUTO, ROUTE_RESHARD, ROUTE_GATHER_BROADCAST = 0, 1, 2
+REFIT_BATCH = 1
+
+
+class Refit:
+    """Owning wrapper of a reshard_refit_t (keeps its plans alive)."""
+
+    def __init__(self, handle, plans):
+        self.handle = handle
+        self.plans = list(plans)
+
+    @property
+    def _as_parameter_(self):
+        if not self.handle:
+            raise ReshardError(6, "refit", "refit already destroyed")
+        return ctypes.c_void_p(self.handle)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            try:
+                _lib.reshard_refit_destroy(ctypes.c_void_p(h))
+            except Exception:  # noqa: BLE001 - interpreter shutdown
+                pass
+            self.handle = None
+
+
+def _nested(ptr_lists):
+    arrs = [_ptr_array(x) for x in ptr_lists]
+    out = (ctypes.POINTER(ctypes.c_void_p) * len(arrs))(
+        *[ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)) for a in arrs])
+    return out, arrs
+
+
+def reshard_refit_create(plans, routes=None, batch: bool = False) -> Refit:
+    """One refit over plans; routes[i] in ROUTE_* (None: AUTO for every plan)."""
+    arr = (ctypes.c_void_p * len(plans))(*[p.handle for p in plans])
+    ra = None if routes is None else (ctypes.c_int32 * len(plans))(*[int(r) for r in routes])
+    h = ctypes.c_void_p()
+    _check(_lib.reshard_refit_create(arr, ra, len(plans), REFIT_BATCH if batch else 0,
+                                     ctypes.byref(h)), "reshard_refit_create")
+    return Refit(h.value, plans)
+
+
+def reshard_refit_info(refit: Refit):
+    """(resolved routes, scratch bytes needed)."""
+    routes = (ctypes.c_int32 * len(refit.plans))()
+    sb = ctypes.c_uint64()
+    _check(_lib.reshard_refit_info(refit, routes, ctypes.byref(sb)), "reshard_refit_info")
+    return [int(r) for r in routes], int(sb.value)
+
+
+def reshard_refit_execute(refit: Refit, src_ptrs_per_plan, dst_ptrs_per_plan, scratch=None,
+                          scratch_bytes: int = 0, stream=None):
+    sa, keep_s = _nested(src_ptrs_per_plan)
+    da, keep_d = _nested(dst_ptrs_per_plan)
+    if scratch is not None and not scratch_bytes and hasattr(scratch, "numel"):
+        scratch_bytes = scratch.numel() * scratch.element_size()
+    _check(_lib.reshard_refit_execute(refit, sa, da, _ptr(scratch), int(scratch_bytes),
+                                      _stream(stream)), "reshard_refit_execute")
+
+
+def reshard_refit_destroy(refit: Refit):
+    if not refit.handle:
+        raise ReshardError(6, "reshard_refit_destroy", "refit already destroyed")
+    st = _lib.reshard_refit_destroy(refit)
+    refit.handle = None
+    _check(st, "reshard_refit_destroy")
 
 
 def reshard_plan_upload(plan: Plan):

@@ -100,6 +100,7 @@ typedef struct reshard_mesh {
 
 typedef struct reshard_plan_s* reshard_plan_t;
 typedef struct reshard_batch_s* reshard_batch_t;
+typedef struct reshard_refit_s* reshard_refit_t;
 
 /* Which copy kernel an execution uses. */
 typedef enum reshard_kernel {
@@ -403,6 +404,54 @@ reshard_status_t reshard_batch_execute(reshard_batch_t batch, const void* const*
 
 /* Release a batch (not its plans).  Errors: BAD_HANDLE. */
 reshard_status_t reshard_batch_destroy(reshard_batch_t batch);
+
+/*
+ * Whole-model refit with the pages' hybrid routing (news.bpdata.com, section
+ * "Integracio es hibrid megoldas a NeMo RL-ben": the feed-forward projections,
+ * about 95% of the parameters, go through the Reshard path; smaller special
+ * weights such as QKV projections through gather-and-broadcast).  A refit
+ * holds plans[nplans] (owned by the caller, checked at every execution) and a
+ * route for each; one reshard_refit_execute then runs the whole model on one
+ * stream: the reshard group first (one batch launch with RESHARD_REFIT_BATCH,
+ * else one launch per plan), then every gather-and-broadcast plan in turn
+ * through one shared scratch buffer (stream order makes the reuse safe).
+ *
+ * Routes: RESHARD_ROUTE_RESHARD, RESHARD_ROUTE_GATHER_BROADCAST, or
+ * RESHARD_ROUTE_AUTO, which on one GPU always resolves to the reshard (it moves
+ * G + D bytes in one launch against 2G + 2D in two); routes == NULL means AUTO
+ * for every plan.  The split therefore only changes where it is asked for.
+ */
+typedef enum reshard_route {
+  RESHARD_ROUTE_AUTO = 0,
+  RESHARD_ROUTE_RESHARD = 1,
+  RESHARD_ROUTE_GATHER_BROADCAST = 2
+} reshard_route_t;
+
+/* reshard_refit_create flag: batch the reshard group into one launch. */
+#define RESHARD_REFIT_BATCH 1u
+
+/* Errors: INVALID_ARG (no plans, unknown route or flag), BAD_HANDLE (a plan is
+ * not live), UNSUPPORTED (RESHARD_REFIT_BATCH and the reshard group exceeds one
+ * batch's buffer table), NO_MEMORY. */
+reshard_status_t reshard_refit_create(const reshard_plan_t* plans, const int32_t* routes,
+                                      int32_t nplans, uint32_t flags, reshard_refit_t* out_refit);
+
+/* Resolved routes (routes[nplans], may be NULL) and the scratch bytes that
+ * reshard_refit_execute needs (the largest global tensor on the
+ * gather-and-broadcast route; 0 when there is none).  Errors: BAD_HANDLE. */
+reshard_status_t reshard_refit_info(reshard_refit_t refit, int32_t* routes, uint64_t* scratch_bytes);
+
+/* src_ptrs[i] / dst_ptrs[i]: plan i's pointer arrays, as for reshard_execute.
+ * scratch: device buffer of scratch_bytes >= the reshard_refit_info figure (may
+ * be NULL when that is 0).  Errors: as reshard_execute and
+ * gather_broadcast_execute; BAD_HANDLE when the refit or one of its plans is
+ * gone.  On an error the calls already enqueued stay enqueued. */
+reshard_status_t reshard_refit_execute(reshard_refit_t refit, const void* const* const* src_ptrs,
+                                       void* const* const* dst_ptrs, void* scratch,
+                                       size_t scratch_bytes, void* stream);
+
+/* Release the refit (its batch too; the plans stay).  Errors: BAD_HANDLE. */
+reshard_status_t reshard_refit_destroy(reshard_refit_t refit);
 
 /*
  * Local box of one rank (news.bpdata.com, section "A megkozelites": the DTensor

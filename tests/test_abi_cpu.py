@@ -220,3 +220,51 @@ def test_plan_path_argument_checks():
     assert rs._lib.reshard_plan_path(p, rs._ptr_array(src), rs._ptr_array(dst), 0, None,
                                      ctypes.byref(out)) == 0
     assert out.value == rs.reshard_plan_path(p, src, dst)[1] == 4  # 4-byte rows
+
+
+def test_refit_routes_and_host_checks():
+    a = rs.reshard_plan_create((64, 64), "bf16", (2,), ("S0",), (4,), ("S1",))
+    b = rs.reshard_plan_create((300, 7), "fp32", (3,), ("S1",), (2,), ("S0",))
+    c = rs.reshard_plan_create((5,), "bf16", (1,), ("R",), (2,), ("R",))
+    refit = rs.reshard_refit_create([a, b, c], [rs.ROUTE_AUTO, rs.ROUTE_GATHER_BROADCAST,
+                                                rs.ROUTE_RESHARD])
+    routes, scratch = rs.reshard_refit_info(refit)
+    assert routes == [rs.ROUTE_RESHARD, rs.ROUTE_GATHER_BROADCAST, rs.ROUTE_RESHARD]
+    assert scratch == 300 * 7 * 4          # the gathered tensor's global bytes
+    assert rs.reshard_refit_info(rs.reshard_refit_create([a, c]))[1] == 0
+    srcs = [_fake_ptrs(p, 0, p.n_src, lambda r: 0) for p in (a, b, c)]
+    dsts = [_fake_ptrs(p, 1, p.n_dst, lambda r: 0) for p in (a, b, c)]
+    with pytest.raises(rs.ReshardError) as e:          # no scratch for the gathered tensor
+        rs.reshard_refit_execute(refit, srcs, dsts, None, 0)
+    assert e.value.status == 1
+    with pytest.raises(rs.ReshardError) as e:          # scratch too small
+        rs.reshard_refit_execute(refit, srcs, dsts, 0x10000, scratch - 1)
+    assert e.value.status == 1
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_refit_create([a], [7])
+    assert e.value.status == 1
+    with pytest.raises(rs.ReshardError) as e:
+        rs._check(rs._lib.reshard_refit_create((ctypes.c_void_p * 1)(a.handle), None, 1, 8,
+                                               ctypes.byref(ctypes.c_void_p())), "create")
+    assert e.value.status == 1
+    rs.reshard_plan_destroy(c)                          # a plan destroyed behind its back
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_refit_execute(refit, srcs, dsts, 0x10000, scratch)
+    assert e.value.status == 6
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_refit_create([a, c])
+    assert e.value.status == 6
+    rs.reshard_refit_destroy(refit)
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_refit_destroy(refit)
+    assert e.value.status == 6
+    assert rs._lib.reshard_refit_destroy(ctypes.c_void_p(0)) == 6
+
+
+def test_refit_batch_limit_is_reported():
+    big = [rs.reshard_plan_create((4096,), "fp32", (256,), ("S0",), (256,), ("S0",))
+           for _ in range(2)]
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_refit_create(big, batch=True)
+    assert e.value.status == 2
+    rs.reshard_refit_create(big, batch=False)           # one launch per plan instead

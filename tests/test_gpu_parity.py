@@ -573,6 +573,45 @@ def test_small_misaligned_fanout_uses_register_realign(oracle):
     run_and_compare(oracle, spec, misalign=3, expect_path="realign")
 
 
+# ---------------------------------------------------------------------- whole-model refit
+@pytest.mark.parametrize("batch", [False, True])
+@pytest.mark.parametrize("misalign", [0, 2])
+def test_refit_hybrid_routes(oracle, batch, misalign):
+    """The reduced MoE model in one reshard_refit_execute: expert weights on the reshard
+    route, attention and norm weights on gather-and-broadcast (the configuration's split),
+    one shared scratch; every byte checked."""
+    _cuda()
+    w = workload(5, reduced=True)
+    plans, sptrs, dptrs, wants, keep = [], [], [], [], []
+    for spec in w.tensors:
+        glob = global_tensor(spec)
+        srcs = [helpers.to_bytes(x) for x in helpers.scatter_with_oracle(
+            oracle, glob, spec.src_mesh, spec.src_placements)]
+        want = helpers.expected_dst(oracle, spec, srcs)
+        ds = _upload(srcs, misalign)
+        dd = [Guarded(x.size, misalign) for x in want]
+        plans.append(helpers.spec_plan(spec))
+        sptrs.append([g.ptr for g in ds])
+        dptrs.append([g.ptr for g in dd])
+        wants.append(want)
+        keep.append((ds, dd))
+    routes = [rs.ROUTE_GATHER_BROADCAST if spec.path == "gather_broadcast" else rs.ROUTE_AUTO
+              for spec in w.tensors]
+    assert rs.ROUTE_GATHER_BROADCAST in routes and rs.ROUTE_AUTO in routes
+    refit = rs.reshard_refit_create(plans, routes, batch=batch)
+    got_routes, need = rs.reshard_refit_info(refit)
+    assert got_routes == [rs.ROUTE_RESHARD if r == rs.ROUTE_AUTO else r for r in routes]
+    scratch = Guarded(need, misalign)
+    rs.reshard_refit_execute(refit, sptrs, dptrs, scratch.ptr, need)
+    torch.cuda.synchronize()
+    for spec, want, (ds, dd) in zip(w.tensors, wants, keep):
+        for g, x in zip(dd, want):
+            assert np.array_equal(g.payload().cpu().numpy(), x), spec.name
+            assert g.guards_intact()
+    assert scratch.guards_intact()
+    assert rs.reshard_device_status() == 0
+
+
 # ---------------------------------------------------------------------- concurrency
 def test_first_use_from_several_host_threads(oracle):
     """Eight host threads execute one fresh plan at once (each into its own buffers): the
