@@ -135,6 +135,8 @@ def _load():
         "reshard_plan_upload": ([vp], ctypes.c_int),
         "reshard_execute": ([vp, vpp, vpp, vp], ctypes.c_int),
         "reshard_execute_ex": ([vp, vpp, vpp, ctypes.c_int32, vp], ctypes.c_int),
+        "reshard_plan_exclude": ([vp, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
+                                  ctypes.POINTER(ctypes.c_int64), ctypes.c_int32, vpp], ctypes.c_int),
         "reshard_plan_path": ([vp, vpp, vpp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
                                ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
         "gather_broadcast_execute": ([vp, vpp, vpp, vp, ctypes.c_size_t, vp], ctypes.c_int),
@@ -278,6 +280,18 @@ def reshard_plan_create(global_shape, dtype, src_mesh, src_placements, dst_mesh,
                                   _placements(dst_placements), ctypes.byref(h))
     _check(st, "reshard_plan_create")
     return Plan(h.value, global_shape, dtype, src_mesh, src_placements, dst_mesh, dst_placements)
+
+
+def reshard_plan_exclude(plan: Plan, src_gone=(), dst_gone=()) -> Plan:
+    """A plan with plan's layouts in which exactly the listed source and destination ranks
+    are gone (never read / never written; their pointers may be None)."""
+    sa = (ctypes.c_int64 * max(1, len(src_gone)))(*[int(r) for r in src_gone])
+    da = (ctypes.c_int64 * max(1, len(dst_gone)))(*[int(r) for r in dst_gone])
+    h = ctypes.c_void_p()
+    _check(_lib.reshard_plan_exclude(plan, sa, len(src_gone), da, len(dst_gone),
+                                     ctypes.byref(h)), "reshard_plan_exclude")
+    return Plan(h.value, plan.global_shape, plan.dtype, plan.src_mesh, plan.src_placements,
+                plan.dst_mesh, plan.dst_placements)
 
 
 def reshard_plan_create_inplace(global_shape, dtype, src_mesh, src_placements, dst_mesh,

@@ -132,6 +132,9 @@ struct reshard_plan_s {
   // (-1: separate buffer) at byte offset alias_off[s]
   bool inplace = false;
   std::vector<int64_t> alias_dst, alias_off;
+  // ranks left out (a membership change): src_gone[s] / dst_gone[d] = 1; empty
+  // when none.  A gone source is never read, a gone destination never written.
+  std::vector<uint8_t> src_gone, dst_gone;
   // device binding (set once by upload_plan, under upload_mu)
   std::mutex upload_mu;
   int device = -1;

@@ -106,10 +106,11 @@ struct Class {
 };
 
 // ---------------------------------------------------------------- step 2: classes
-std::vector<Class> classes_of(int32_t nd, const Layout& L) {
+std::vector<Class> classes_of(int32_t nd, const Layout& L, const std::vector<uint8_t>& gone) {
   std::vector<Class> out;
   std::map<std::vector<int64_t>, size_t> index;
   for (int64_t r = 0; r < L.nranks; ++r) {
+    if (!gone.empty() && gone[size_t(r)]) continue;
     const Box& b = L.box[r];
     const int64_t vol = box_volume(nd, b);
     if (vol == 0) continue;
@@ -340,11 +341,16 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   for (int d = 0; d < nd; ++d) S.global_bytes *= P->gshape[d];
   S.n_src_ranks = M;
   S.n_dst_ranks = N;
-  for (int64_t r = 0; r < M; ++r) S.src_bytes += box_volume(nd, P->src.box[r]) * eb;
-  for (int64_t r = 0; r < N; ++r) S.dst_bytes += box_volume(nd, P->dst.box[r]) * eb;
+  auto present = [](const std::vector<uint8_t>& gone, int64_t r) {
+    return gone.empty() || !gone[size_t(r)];
+  };
+  for (int64_t r = 0; r < M; ++r)
+    if (present(P->src_gone, r)) S.src_bytes += box_volume(nd, P->src.box[r]) * eb;
+  for (int64_t r = 0; r < N; ++r)
+    if (present(P->dst_gone, r)) S.dst_bytes += box_volume(nd, P->dst.box[r]) * eb;
 
-  const std::vector<Class> sc = classes_of(nd, P->src);
-  const std::vector<Class> dc = classes_of(nd, P->dst);
+  const std::vector<Class> sc = classes_of(nd, P->src, P->src_gone);
+  const std::vector<Class> dc = classes_of(nd, P->dst, P->dst_gone);
   S.n_src_classes = int64_t(sc.size());
   S.n_dst_classes = int64_t(dc.size());
 
@@ -381,6 +387,16 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   }
   S.n_regions = int64_t(regions.size());
   for (const Region& g : regions) S.region_bytes += g.bytes;
+  if (!P->src_gone.empty()) {
+    // with source ranks gone, every destination class must still be covered
+    std::vector<int64_t> covered(dc.size(), 0);
+    for (const Region& g : regions) covered[g.d] += g.bytes;
+    for (size_t di = 0; di < dc.size(); ++di)
+      if (covered[di] != dc[di].volume * eb)
+        return fail(RESHARD_ERR_UNSUPPORTED,
+                    "no remaining source rank holds part of destination rank " +
+                        std::to_string(dc[di].ranks[0]));
+  }
 
   // ---- step 4: replica pick, largest region first onto the least-loaded replica
   {
@@ -625,7 +641,7 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   // slice: every destination rank copies its box out of the full tensor
   for (int64_t r = 0; r < N; ++r) {
     const Box& b = P->dst.box[size_t(r)];
-    if (box_volume(nd, b) == 0) continue;
+    if (box_volume(nd, b) == 0 || !present(P->dst_gone, r)) continue;
     int64_t dst[RESHARD_MAX_TENSOR_NDIM];
     row_major_strides(nd, b.shp, dst);
     int64_t s0 = 0;
@@ -781,10 +797,79 @@ reshard_status_t create_plan(const int64_t* global_shape, int32_t tensor_ndim,
   return RESHARD_OK;
 }
 
+// A plan with base's layouts (and in-place declaration) and exactly the given
+// ranks gone.
+reshard_status_t derive_plan(const reshard_plan_s* base, const int64_t* src_gone,
+                             int32_t n_src_gone, const int64_t* dst_gone, int32_t n_dst_gone,
+                             reshard_plan_t* out_plan) {
+  const auto t0 = std::chrono::steady_clock::now();
+  if (!out_plan) return fail(RESHARD_ERR_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  if (n_src_gone < 0 || n_dst_gone < 0 || (n_src_gone > 0 && !src_gone) ||
+      (n_dst_gone > 0 && !dst_gone))
+    return fail(RESHARD_ERR_INVALID_ARG, "bad rank list");
+  const int64_t M = base->src.nranks, N = base->dst.nranks;
+  reshard_plan_s* P = new (std::nothrow) reshard_plan_s();
+  if (!P) return fail(RESHARD_ERR_NO_MEMORY, "host allocation failed");
+  reshard_status_t st = RESHARD_OK;
+  try {
+    P->ndim = base->ndim;
+    P->elem_bytes = base->elem_bytes;
+    for (int d = 0; d < base->ndim; ++d) P->gshape[d] = base->gshape[d];
+    P->src = base->src;
+    P->dst = base->dst;
+    P->inplace = base->inplace;
+    P->alias_dst = base->alias_dst;
+    P->alias_off = base->alias_off;
+    if (n_src_gone > 0) P->src_gone.assign(size_t(M), 0);
+    if (n_dst_gone > 0) P->dst_gone.assign(size_t(N), 0);
+    for (int32_t i = 0; i < n_src_gone && st == RESHARD_OK; ++i) {
+      if (src_gone[i] < 0 || src_gone[i] >= M) st = fail(RESHARD_ERR_INVALID_ARG, "source rank out of range");
+      else P->src_gone[size_t(src_gone[i])] = 1;
+    }
+    for (int32_t i = 0; i < n_dst_gone && st == RESHARD_OK; ++i) {
+      if (dst_gone[i] < 0 || dst_gone[i] >= N) st = fail(RESHARD_ERR_INVALID_ARG, "destination rank out of range");
+      else P->dst_gone[size_t(dst_gone[i])] = 1;
+    }
+    // an in-place source whose own rank or host rank is gone is simply not in place
+    if (st == RESHARD_OK && P->inplace)
+      for (int64_t s = 0; s < M; ++s) {
+        const int64_t d = P->alias_dst[size_t(s)];
+        if (d >= 0 && ((!P->src_gone.empty() && P->src_gone[size_t(s)]) ||
+                       (!P->dst_gone.empty() && P->dst_gone[size_t(d)])))
+          P->alias_dst[size_t(s)] = -1;
+      }
+    if (st == RESHARD_OK) st = build_plan(P);
+  } catch (const std::bad_alloc&) {
+    st = fail(RESHARD_ERR_NO_MEMORY, "host allocation failed while planning");
+  }
+  if (st != RESHARD_OK) {
+    delete P;
+    return st;
+  }
+  P->magic = kPlanMagic;
+  P->stats.planner_ns = std::chrono::duration_cast<std::chrono::nanoseconds>(
+                            std::chrono::steady_clock::now() - t0).count();
+  {
+    std::lock_guard<std::mutex> lk(g_registry_mu);
+    registry().insert(P);
+  }
+  *out_plan = P;
+  return RESHARD_OK;
+}
+
 }  // namespace
 }  // namespace rs
 
 extern "C" {
+
+reshard_status_t reshard_plan_exclude(reshard_plan_t plan, const int64_t* src_gone,
+                                      int32_t n_src_gone, const int64_t* dst_gone,
+                                      int32_t n_dst_gone, reshard_plan_t* out_plan) {
+  if (out_plan) *out_plan = nullptr;
+  if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  return rs::derive_plan(plan, src_gone, n_src_gone, dst_gone, n_dst_gone, out_plan);
+}
 
 reshard_status_t reshard_plan_create(const int64_t* global_shape, int32_t tensor_ndim,
                                      reshard_dtype_t dtype, const reshard_mesh_t* src_mesh,
@@ -933,13 +1018,15 @@ reshard_status_t buffer_table(reshard_plan_t plan, const void* const* src_ptrs,
   if (!src_ptrs || !dst_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "null pointer array");
   bufs->resize(size_t(M + N + 1));
   for (int64_t r = 0; r < M; ++r) {
-    if (!src_ptrs[r] && rs::box_volume(plan->ndim, plan->src.box[size_t(r)]) > 0)
+    if (!src_ptrs[r] && rs::box_volume(plan->ndim, plan->src.box[size_t(r)]) > 0 &&
+        (plan->src_gone.empty() || !plan->src_gone[size_t(r)]))
       return fail(RESHARD_ERR_INVALID_ARG, "NULL source pointer for a non-empty shard (rank " +
                                                std::to_string(r) + ")");
     (*bufs)[size_t(r)] = static_cast<unsigned char*>(const_cast<void*>(src_ptrs[r]));
   }
   for (int64_t r = 0; r < N; ++r) {
-    if (!dst_ptrs[r] && rs::box_volume(plan->ndim, plan->dst.box[size_t(r)]) > 0)
+    if (!dst_ptrs[r] && rs::box_volume(plan->ndim, plan->dst.box[size_t(r)]) > 0 &&
+        (plan->dst_gone.empty() || !plan->dst_gone[size_t(r)]))
       return fail(RESHARD_ERR_INVALID_ARG, "NULL destination pointer for a non-empty shard (rank " +
                                                std::to_string(r) + ")");
     (*bufs)[size_t(M + r)] = static_cast<unsigned char*>(dst_ptrs[r]);

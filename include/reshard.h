@@ -511,6 +511,25 @@ reshard_status_t reshard_plan_path(reshard_plan_t plan, const void* const* src_p
  */
 int64_t reshard_tile_units(const reshard_tile_t* tile);
 
+/*
+ * Membership change (news.bpdata.com, section "Integracio es hibrid megoldas a
+ * NeMo RL-ben": when GPUs join or leave at run time the communication group is
+ * rebuilt, or shrunk/grown in place).  Derives a new plan from plan's layouts
+ * (and in-place declaration) in which exactly the listed ranks are gone; rank
+ * numbering is unchanged, so buffer tables keep M + N entries and a gone rank's
+ * pointer may be NULL.  A gone source rank is never read: the regions it
+ * served move to the remaining replicas of its box (rebalanced as at
+ * creation); a gone destination rank is never written.  The derived plan's own
+ * exclusions do not carry over: a rank that comes back is a call with a shorter
+ * list (an empty one gives the full plan again).  An in-place alias that
+ * involves a gone rank is dropped.  Errors: BAD_HANDLE, INVALID_ARG (rank out
+ * of range, NULL list with a positive count), UNSUPPORTED (some destination
+ * bytes have no remaining source rank), NO_MEMORY.
+ */
+reshard_status_t reshard_plan_exclude(reshard_plan_t plan, const int64_t* src_gone,
+                                      int32_t n_src_gone, const int64_t* dst_gone,
+                                      int32_t n_dst_gone, reshard_plan_t* out_plan);
+
 /* Release a plan and its device tables.  Errors: BAD_HANDLE. */
 reshard_status_t reshard_plan_destroy(reshard_plan_t plan);
 

@@ -573,6 +573,36 @@ def test_small_misaligned_fanout_uses_register_realign(oracle):
     run_and_compare(oracle, spec, misalign=3, expect_path="realign")
 
 
+# ---------------------------------------------------------------------- membership change
+@pytest.mark.parametrize("kernel", [rs.KERNEL_FANOUT, rs.KERNEL_BOXCOPY])
+@pytest.mark.parametrize("misalign", [0, 2])
+def test_excluded_ranks_get_null_buffers(oracle, kernel, misalign):
+    """A source replica and a destination rank leave: the derived plan reads the other
+    replica, leaves the gone destination alone (NULL pointers for both) and is exact."""
+    _cuda()
+    spec = workload(2, reduced=True).tensors[0]
+    src_gone, dst_gone = [1], [3]
+    glob = global_tensor(spec)
+    srcs = [helpers.to_bytes(x) for x in helpers.scatter_with_oracle(
+        oracle, glob, spec.src_mesh, spec.src_placements)]
+    want = helpers.expected_dst(oracle, spec, srcs)
+    ds = _upload(srcs, misalign)
+    dd = [Guarded(w.size, misalign) for w in want]
+    plan = rs.reshard_plan_exclude(helpers.spec_plan(spec), src_gone, dst_gone)
+    sptr = [None if r in src_gone else g.ptr for r, g in enumerate(ds)]
+    dptr = [None if r in dst_gone else g.ptr for r, g in enumerate(dd)]
+    rs.reshard_execute_ex(plan, sptr, dptr, kernel)
+    torch.cuda.synchronize()
+    for r, (g, w) in enumerate(zip(dd, want)):
+        got = g.payload().cpu().numpy()
+        if r in dst_gone:
+            assert (got == FILL_BYTE).all(), "a gone destination was written"
+        else:
+            assert np.array_equal(got, w), r
+        assert g.guards_intact()
+    assert rs.reshard_device_status() == 0
+
+
 # ---------------------------------------------------------------------- whole-model refit
 @pytest.mark.parametrize("batch", [False, True])
 @pytest.mark.parametrize("misalign", [0, 2])

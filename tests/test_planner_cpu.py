@@ -292,3 +292,111 @@ def test_inplace_execute_requires_aliased_pointers():
     rc = rs._lib.reshard_execute(plan, rs._ptr_array(srcs), rs._ptr_array(dsts), None)
     assert rc == 1 and "in-place" in rs.reshard_last_error()
     del ctypes
+
+
+# ---------------------------------------------------------------------- membership change
+def _check_excluded(oracle, spec, src_gone, dst_gone):
+    """Run the derived plan's programs on the CPU with zero-length buffers for the gone
+    ranks (any access to one fails the executor's bounds check); every remaining
+    destination must match the oracle and be written exactly once."""
+    glob = global_tensor(spec)
+    srcs = [helpers.to_bytes(s) for s in helpers.scatter_with_oracle(
+        oracle, glob, spec.src_mesh, spec.src_placements)]
+    want = helpers.expected_dst(oracle, spec, srcs)
+    plan = rs.reshard_plan_exclude(helpers.spec_plan(spec), src_gone, dst_gone)
+    M = spec.n_src
+    empty = np.zeros(0, dtype=np.uint8)
+    for program in (rs.PROGRAM_FANOUT, rs.PROGRAM_BOXCOPY):
+        bufs = ([empty if s in src_gone else srcs[s].copy() for s in range(M)] +
+                [empty if r in dst_gone else np.full(w.size, 0xA5, dtype=np.uint8)
+                 for r, w in enumerate(want)] + [empty])
+        writes = helpers.run_program_cpu(plan, program, bufs)
+        for r, w in enumerate(want):
+            if r in dst_gone:
+                continue
+            assert np.array_equal(bufs[M + r], w), (spec.name, program, r)
+            assert (writes[M + r] == 1).all()
+    # gather-and-broadcast: the slice of every remaining destination is exact
+    bufs = ([empty if s in src_gone else srcs[s].copy() for s in range(M)] +
+            [empty if r in dst_gone else np.zeros(w.size, dtype=np.uint8)
+             for r, w in enumerate(want)] + [np.zeros(spec.global_bytes, dtype=np.uint8)])
+    helpers.run_program_cpu(plan, rs.PROGRAM_GATHER, bufs)
+    helpers.run_program_cpu(plan, rs.PROGRAM_SLICE, bufs)
+    for r, w in enumerate(want):
+        if r not in dst_gone:
+            assert np.array_equal(bufs[M + r], w), (spec.name, "gather-broadcast", r)
+    return plan
+
+
+def _shard_bytes(plan, side, ranks, spec):
+    return sum(math.prod(rs.reshard_plan_local_shape(plan, side, r)[0]) for r in ranks) * \
+        spec.elem_bytes
+
+
+def test_exclude_source_replicas_rebalances(oracle):
+    # FFN up (reduced): every source box has two replicas (DP2)
+    spec = workload(2, reduced=True).tensors[0]
+    base = helpers.spec_plan(spec)
+    plan = _check_excluded(oracle, spec, src_gone=[0, 5], dst_gone=[])
+    s0, s1 = rs.reshard_plan_stats(base), rs.reshard_plan_stats(plan)
+    assert s1["fanout_read_bytes"] == s0["fanout_read_bytes"]     # still read once
+    assert s1["src_bytes"] == s0["src_bytes"] - _shard_bytes(base, 0, [0, 5], spec)
+    tiles, _, _, _ = rs.reshard_plan_program(plan, rs.PROGRAM_FANOUT)
+    assert {t["src_buf"] for t in tiles}.isdisjoint({0, 5})
+
+
+def test_exclude_destination_ranks(oracle):
+    spec = workload(2, reduced=True).tensors[0]
+    base = helpers.spec_plan(spec)
+    plan = _check_excluded(oracle, spec, src_gone=[], dst_gone=[1, 6])
+    s0, s1 = rs.reshard_plan_stats(base), rs.reshard_plan_stats(plan)
+    assert s1["dst_bytes"] == s0["dst_bytes"] - _shard_bytes(base, 1, [1, 6], spec)
+    assert s1["fanout_write_bytes"] == s1["dst_bytes"]
+
+
+def test_exclude_both_sides_random(oracle):
+    rng = random.Random(77)
+    for i in range(12):
+        spec = _case((rng.randint(1, 40), rng.randint(1, 40)), "bf16", (2, 2),
+                     ("R", rng.choice(["S0", "S1"])), (3,), (rng.choice(["R", "S0", "S1"]),),
+                     seed=900 + i)
+        src_gone = [rng.choice([0, 1])] if rng.random() < 0.7 else []   # one replica of a pair
+        dst_gone = [rng.randrange(3)] if rng.random() < 0.5 else []
+        _check_excluded(oracle, spec, src_gone, dst_gone)
+
+
+def test_exclude_without_a_remaining_source_is_unsupported():
+    p = rs.reshard_plan_create((8, 8), "bf16", (2,), ("S0",), (4,), ("S1",))
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_plan_exclude(p, [1])
+    assert e.value.status == 2
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_plan_exclude(p, [2])
+    assert e.value.status == 1
+    with pytest.raises(rs.ReshardError) as e:
+        rs.reshard_plan_exclude(p, [], [4])
+    assert e.value.status == 1
+
+
+def test_rank_rejoining_restores_the_plan():
+    spec = workload(2, reduced=True).tensors[0]
+    base = helpers.spec_plan(spec)
+    gone = rs.reshard_plan_exclude(base, [0], [2])
+    back = rs.reshard_plan_exclude(gone, [], [])
+    for program in range(4):
+        a, pa, _, _ = rs.reshard_plan_program(base, program)
+        b, pb, _, _ = rs.reshard_plan_program(back, program)
+        assert [dict(t) for t in a] == [dict(t) for t in b] and list(pa) == list(pb)
+    assert rs.reshard_plan_stats(back)["dst_bytes"] == rs.reshard_plan_stats(base)["dst_bytes"]
+
+
+def test_exclude_drops_aliases_of_gone_ranks(oracle):
+    spec = workload(3, reduced=True).tensors[0]
+    alias = helpers.pick_aliases(oracle, spec)
+    s = next(i for i, d in enumerate(alias) if d >= 0)
+    base = rs.reshard_plan_create_inplace(spec.global_shape, spec.dtype, spec.src_mesh,
+                                          spec.src_placements, spec.dst_mesh,
+                                          spec.dst_placements, alias)
+    plan = rs.reshard_plan_exclude(base, [], [alias[s]])
+    assert rs.reshard_plan_alias(plan, s)[0] == -1
+    assert rs.reshard_plan_alias(base, s)[0] == alias[s]
