@@ -19,6 +19,14 @@ constexpr int64_t kRunSplitBytes = 64 * 1024;
 constexpr int64_t kUnitBytes = 4096;
 // Largest single-row tile (longer runs are cut into several tiles).
 constexpr int64_t kMaxRunBytes = int64_t(1) << 30;
+// A multi-row fan-out tile that fills a column band of wider destination rows
+// and goes to at least kGatherBlockFanout replicas is cut into blocks of about
+// kGatherBlockBytes of rows, so that after the sort by destination offset the
+// blocks of neighbouring bands interleave and each CTA writes whole stretches
+// of destination rows to every replica (measured: it pays where writes
+// dominate, and costs more tiles and smaller chunks elsewhere).
+constexpr int64_t kGatherBlockBytes = 16 * 1024;
+constexpr int64_t kGatherBlockFanout = 8;
 // Largest destination group one tile fans out to (larger groups are split).
 constexpr int kMaxGroup = 256;
 

@@ -148,7 +148,7 @@ void row_major_strides(int32_t nd, const int64_t* shp, int64_t* st) {
 // element src_base / dst_base of buffers with strides sst / dst (elements).
 void emit_box(Program& P, uint16_t src_buf, uint16_t group, int32_t nd, const int64_t* e,
               int64_t src_base, const int64_t* sst, int64_t dst_base, const int64_t* dstr,
-              int64_t eb) {
+              int64_t eb, int64_t fanout = 1) {
   std::vector<Dim> dims;
   for (int d = 0; d < nd; ++d) {
     if (e[d] == 0) return;
@@ -194,10 +194,16 @@ void emit_box(Program& P, uint16_t src_buf, uint16_t group, int32_t nd, const in
     // keep nrows * nplanes of one tile below 2^30: slice planes, then rows
     const int64_t kMaxRows = int64_t(1) << 30;
     const int64_t pstep = std::max<int64_t>(1, kMaxRows / nrows);
+    // rows that are a column band of wider destination rows: cut into blocks
+    int64_t rstep = kMaxRows;
+    if (kGatherBlockBytes > 0 && fanout >= kGatherBlockFanout && nplanes == 1 &&
+        drs * eb > row_bytes)
+      rstep = std::max<int64_t>(int64_t(rows_per_unit(uint32_t(row_bytes))),
+                                (kGatherBlockBytes + row_bytes - 1) / row_bytes);
     for (int64_t p0 = 0; p0 < nplanes; p0 += pstep) {
       const int64_t np = std::min(nplanes - p0, pstep);
-      for (int64_t r0 = 0; r0 < nrows; r0 += kMaxRows) {
-        const int64_t nr = std::min(nrows - r0, kMaxRows);
+      for (int64_t r0 = 0; r0 < nrows; r0 += rstep) {
+        const int64_t nr = std::min(nrows - r0, rstep);
         reshard_tile_t t = {};
         t.src_off = (sb + p0 * sps + r0 * srs) * eb;
         t.dst_off = (db + p0 * dps + r0 * drs) * eb;
@@ -613,7 +619,8 @@ reshard_status_t build_plan(reshard_plan_s* P) {
     }
     if (!consumed[ri])
       for (uint16_t grp : fan_groups(targets))
-        emit_box(PF, uint16_t(g.replica), grp, nd, g.ext, s0, sst, d0, dst, eb);
+        emit_box(PF, uint16_t(g.replica), grp, nd, g.ext, s0, sst, d0, dst, eb,
+                 int64_t(PF.goff[grp + 1] - PF.goff[grp]));
     for (int64_t r : targets)
       emit_box(PB, uint16_t(g.replica), uint16_t(r), nd, g.ext, s0, sst, d0, dst, eb);
   }
