@@ -604,7 +604,7 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
   const int planes = prog.has_planes ? 1 : 0;
   const int kidx = d.kidx;
   int bps = 1;
-  if (kidx != kStagedRealign) {
+  if (kidx >= 0) {
     reshard_status_t st = occupancy(dev, kidx, planes, &bps);
     if (st != RESHARD_OK) return st;
   }

@@ -68,44 +68,6 @@ struct Config {
   static constexpr uint32_t kMaxRows = Walker::kMaxRows;
 };
 
-struct FastDiv32 {
-  uint32_t m, l;
-  __device__ __forceinline__ explicit FastDiv32(uint32_t div) {
-    l = 0;
-    while ((uint64_t(1) << l) < div) ++l;
-    m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << l) - div)) / div + 1);
-  }
-  __device__ __forceinline__ uint32_t div(uint32_t n) const {
-    return uint32_t((uint64_t(__umulhi(n, m)) + n) >> l);
-  }
-};
-
-__device__ __forceinline__ uint32_t word_at(const uint4& v, uint32_t i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-// Bytes [lo, hi) of the 16-byte granule v to the 16-byte aligned address g,
-// in the widest naturally aligned stores that fit.
-__device__ __forceinline__ void store_partial16(unsigned char* g, const uint4& v, uint32_t lo,
-                                                uint32_t hi) {
-  while (lo < hi) {
-    const uint32_t w = word_at(v, lo >> 2);
-    if ((lo & 7u) == 0 && lo + 8 <= hi) {
-      *reinterpret_cast<uint2*>(g + lo) = make_uint2(w, word_at(v, (lo >> 2) + 1));
-      lo += 8;
-    } else if ((lo & 3u) == 0 && lo + 4 <= hi) {
-      *reinterpret_cast<uint32_t*>(g + lo) = w;
-      lo += 4;
-    } else if ((lo & 1u) == 0 && lo + 2 <= hi) {
-      *reinterpret_cast<uint16_t*>(g + lo) = uint16_t(w >> (8u * (lo & 3u)));
-      lo += 2;
-    } else {
-      g[lo] = uint8_t(w >> (8u * (lo & 3u)));
-      lo += 1;
-    }
-  }
-}
-
 // Destination granule k of a row whose first destination byte sits dmis bytes
 // into its granule and whose first source byte is staged at stage + spos.
 // Byte j of the granule is row byte 16k + j - dmis, staged at
@@ -119,14 +81,6 @@ __device__ __forceinline__ uint4 granule(const unsigned char* stage, uint32_t sp
   if (o == 0) return A;
   const uint4 B = *reinterpret_cast<const uint4*>(a + 16);
   return funnel16(A, B, o >> 2, 0x3210u + 0x1111u * (o & 3u));
-}
-
-// The destination bytes [lo, hi) that granule k of a row of n bytes covers,
-// G = the row's granule count.
-__device__ __forceinline__ void granule_span(uint32_t dmis, uint32_t n, uint32_t G, uint32_t k,
-                                             uint32_t* lo, uint32_t* hi) {
-  *lo = k == 0 ? dmis : 0u;
-  *hi = k + 1 == G ? ((dmis + n - 1u) & 15u) + 1u : 16u;
 }
 
 // Granule k (bytes v) of a row to one replica: dst + doff is the row's first
