@@ -3,12 +3,14 @@
 //
 // Used for fan-out programs in which every tile offset, stride, row length and
 // buffer address is a multiple of 16 bytes.  Each CTA runs a two-warp pipeline
-// over its equal share of the program's work units (the same partition as the
-// vector kernel in kernels.cu):
-//   warp 0 (producer) copies the next chunk of source bytes -- a piece of a
-//     contiguous run, a few whole rows, or a piece of a long row -- into a
-//     ring of shared-memory stages with cp.async.bulk; completion is counted in
-//     bytes on the stage's "full" mbarrier;
+// over pieces of consecutive work units that it takes from a per-launch work
+// queue as it goes, so that CTAs on faster SMs take more pieces and all finish
+// together (a static equal split left the slowest SMs 15-25% behind):
+//   warp 0 (producer) takes pieces and copies their chunks of source bytes --
+//     a piece of a contiguous run, a few whole rows, or a piece of a long row --
+//     into a ring of shared-memory stages with cp.async.bulk, with a descriptor
+//     of the chunk beside each stage; completion is counted in bytes on the
+//     stage's "full" mbarrier; a descriptor with no tile ends the CTA's work;
 //   warp 1 (consumer) waits for the stage and writes it to every destination
 //     replica of the tile with cp.async.bulk stores (rows that are contiguous
 //     in the destination go out as one store per replica), commits them as a
@@ -22,6 +24,7 @@
 // returns, so the context stays usable; reshard_device_status() reads it.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <string>
@@ -40,10 +43,38 @@ constexpr int kStagedThreads = 64;
 
 __device__ unsigned int g_device_status;
 
+// Work queue: pieces of consecutive work units are handed to CTAs in order as
+// they ask, so CTAs that run fast take more pieces and all finish
+// together.  Every launch takes its own slot {next piece, CTAs finished}; the
+// last CTA of the launch puts the slot back to zero.
+constexpr int kQueueSlots = 1024;
+__device__ unsigned int g_queue[kQueueSlots][2];
+// Units per piece: about kPieceBytes of the program's bytes, and few enough
+// that every CTA can get about kPiecesPerCta pieces (small programs still use
+// the whole grid).  Measured: 32 KiB pieces beat 8-unit and 64 KiB ones over
+// the workloads taken together.
+constexpr int64_t kPieceBytes = 32 * 1024;
+constexpr int64_t kPiecesPerCta = 8;
+
+// One chunk, handed from the producer to the consumer together with its stage.
+struct StageDesc {
+  int32_t ti;  // tile index; -1: no more chunks
+  uint32_t kind, bytes;
+  int64_t a, b;
+};
+
+__device__ __forceinline__ uint32_t grab_piece(unsigned int* queue, int lane) {
+  uint32_t piece = 0;
+  if (lane == 0) piece = atomicAdd(&queue[0], 1u);
+  return __shfl_sync(0xffffffffu, piece, 0);
+}
+
 __global__ void __launch_bounds__(kStagedThreads)
-    fanout_staged_kernel(const __grid_constant__ KernelParams p, unsigned int* status) {
+    fanout_staged_kernel(const __grid_constant__ KernelParams p, unsigned int* status,
+                         unsigned int* queue, int64_t piece_units) {
   extern __shared__ __align__(1024) unsigned char stage_mem[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+  __shared__ StageDesc desc[kStages];
   __shared__ unsigned char* dst_base[kMaxGroup];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -55,50 +86,76 @@ __global__ void __launch_bounds__(kStagedThreads)
   }
   __syncthreads();
 
-  ChunkWalker<kStageBytes, 0> w;
-  w.start(&p);
-  Chunk c;
   uint32_t n = 0;
   if (warp == 0) {
-    // producer: source -> stage (n % kStages)
-    while (w.next(&c)) {
+    // producer: pieces from the queue -> chunks -> stage (n % kStages)
+    ChunkWalker<kStageBytes, 0> w;
+    Chunk c;
+    bool ok = true;
+    const int64_t total = p.total_units;
+    const int64_t npieces = (total + piece_units - 1) / piece_units;
+    uint32_t piece = grab_piece(queue, lane);
+    while (ok && int64_t(piece) < npieces) {
+      const uint32_t next_piece = grab_piece(queue, lane);  // asked early, used later
+      const int64_t u0 = int64_t(piece) * piece_units;
+      w.start_range(&p, u0, min(u0 + piece_units, total));
+      while (w.next(&c)) {
+        const int s = int(n % kStages);
+        if (n >= uint32_t(kStages) &&
+            !mbar_wait(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls)) {
+          if (lane == 0) atomicExch(status, kStatusProducerWait);
+          ok = false;
+          break;
+        }
+        unsigned char* buf = stage_mem + size_t(s) * kStageBytes;
+        const reshard_tile_t& t = w.t;
+        const unsigned char* src = p.bufs[t.src_buf];
+        if (lane == 0) {
+          desc[s] = StageDesc{c.ti, c.kind, c.bytes, c.a, c.b};
+          mbar_arrive_expect(&full[s], c.bytes);
+        }
+        __syncwarp();
+        if (c.kind == 0) {
+          if (lane == 0) bulk_load(buf, src + t.src_off + c.a, c.bytes, &full[s]);
+        } else if (c.kind == 1) {
+          for (int64_t r = c.a + lane; r < c.b; r += 32)
+            bulk_load(buf + (r - c.a) * t.row_bytes, src + src_row(t, r), t.row_bytes, &full[s]);
+        } else {
+          if (lane == 0) bulk_load(buf, src + src_row(t, c.a) + c.b, c.bytes, &full[s]);
+        }
+        ++n;
+      }
+      piece = next_piece;
+    }
+    // end marker: a stage whose descriptor says "no more chunks", with no bytes
+    if (ok) {
       const int s = int(n % kStages);
-      if (n >= uint32_t(kStages) &&
-          !mbar_wait(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls)) {
+      if (n >= uint32_t(kStages) && !mbar_wait(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls)) {
         if (lane == 0) atomicExch(status, kStatusProducerWait);
-        return;  // nothing of ours is in flight that this stage still needs
+      } else if (lane == 0) {
+        desc[s].ti = -1;
+        mbar_arrive(&full[s]);
       }
-      unsigned char* buf = stage_mem + size_t(s) * kStageBytes;
-      const reshard_tile_t& t = w.t;
-      const unsigned char* src = p.bufs[t.src_buf];
-      if (lane == 0) mbar_arrive_expect(&full[s], c.bytes);
-      __syncwarp();
-      if (c.kind == 0) {
-        if (lane == 0) bulk_load(buf, src + t.src_off + c.a, c.bytes, &full[s]);
-      } else if (c.kind == 1) {
-        for (int64_t r = c.a + lane; r < c.b; r += 32)
-          bulk_load(buf + (r - c.a) * t.row_bytes, src + src_row(t, r), t.row_bytes, &full[s]);
-      } else {
-        if (lane == 0) bulk_load(buf, src + src_row(t, c.a) + c.b, c.bytes, &full[s]);
-      }
-      ++n;
     }
   } else {
     // consumer: stage -> every destination replica
     int cur_tile = -1, R = 0;
-    while (w.next(&c)) {
+    reshard_tile_t t = {};
+    while (true) {
       const int s = int(n % kStages);
-      const reshard_tile_t& t = w.t;
+      if (!mbar_wait(&full[s], (n / kStages) & 1u, kWaitPolls)) {
+        if (lane == 0) atomicExch(status, kStatusConsumerWait);
+        break;
+      }
+      const StageDesc c = desc[s];
+      if (c.ti < 0) break;
       if (c.ti != cur_tile) {
+        t = p.tiles[c.ti];
         const uint32_t g0 = p.goff[t.dst_group];
         R = int(p.goff[t.dst_group + 1] - g0);
         for (int i = lane; i < R; i += 32) dst_base[i] = p.bufs[p.gbuf[g0 + i]];
         __syncwarp();
         cur_tile = c.ti;
-      }
-      if (!mbar_wait(&full[s], (n / kStages) & 1u, kWaitPolls)) {
-        if (lane == 0) atomicExch(status, kStatusConsumerWait);
-        break;
       }
       const unsigned char* buf = stage_mem + size_t(s) * kStageBytes;
       if (c.kind == 0) {
@@ -126,6 +183,16 @@ __global__ void __launch_bounds__(kStagedThreads)
     }
     bulk_wait_all();
   }
+  // both roles are done (every wait above is bounded): count the CTA out, and
+  // the last one puts the launch's queue slot back to zero
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&queue[1], 1u) == gridDim.x - 1) {
+      atomicExch(&queue[0], 0u);
+      atomicExch(&queue[1], 0u);
+    }
+  }
 }
 
 // A wait that nothing will ever answer: exercises the bounded-wait path.
@@ -143,8 +210,10 @@ constexpr int kMaxDevices = 256;
 struct DeviceState {
   bool ready = false;
   unsigned int* status = nullptr;  // device address of g_device_status
+  unsigned int* queue = nullptr;   // device address of g_queue
   int blocks_per_sm = 0;
 };
+std::atomic<uint32_t> g_queue_slot{0};
 std::mutex g_dev_mu;
 DeviceState g_dev[kMaxDevices];
 
@@ -171,6 +240,11 @@ reshard_status_t device_state(DeviceState* out) {
         &n, reinterpret_cast<const void*>(fanout_staged_kernel), kStagedThreads, smem);
     if (ce != cudaSuccess)
       return fail(RESHARD_ERR_CUDA, std::string("occupancy query: ") + cudaGetErrorString(ce));
+    void* qaddr = nullptr;
+    ce = cudaGetSymbolAddress(&qaddr, g_queue);
+    if (ce != cudaSuccess)
+      return fail(RESHARD_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(ce));
+    d.queue = static_cast<unsigned int*>(qaddr);
     d.status = static_cast<unsigned int*>(addr);
     d.blocks_per_sm = n > 0 ? n : 1;
     d.ready = true;
@@ -190,7 +264,7 @@ reshard_status_t device_status_word(unsigned int** status) {
 }
 
 reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelParams& kp,
-                                      void* stream) {
+                                      int64_t plan_tile_bytes, void* stream) {
   DeviceState d;
   reshard_status_t st = device_state(&d);
   if (st != RESHARD_OK) return st;
@@ -198,7 +272,14 @@ reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelPa
   const unsigned grid = unsigned(kp.total_units < max_grid ? kp.total_units : max_grid);
   KernelParams params = kp;
   unsigned int* status = d.status;
-  void* args[] = {&params, &status};
+  // a slot of its own (launches in flight at once never come near kQueueSlots)
+  unsigned int* queue = d.queue + 2 * (g_queue_slot.fetch_add(1) % uint32_t(kQueueSlots));
+  const int64_t units = kp.total_units > 0 ? kp.total_units : 1;
+  const int64_t unit_bytes = plan_tile_bytes / units > 0 ? plan_tile_bytes / units : 1;
+  int64_t piece_units = kp.total_units / (int64_t(grid) * kPiecesPerCta);
+  const int64_t want_units = (kPieceBytes + unit_bytes - 1) / unit_bytes;
+  piece_units = piece_units < 1 ? 1 : piece_units > want_units ? want_units : piece_units;
+  void* args[] = {&params, &status, &queue, &piece_units};
   cudaError_t ce = cudaLaunchKernel(reinterpret_cast<const void*>(fanout_staged_kernel),
                                     dim3(grid), dim3(kStagedThreads), args,
                                     kStages * kStageBytes, static_cast<cudaStream_t>(stream));

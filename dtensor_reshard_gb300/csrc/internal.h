@@ -184,7 +184,7 @@ struct Dispatch {
 Dispatch decide(const Program& prog, unsigned char* const* bufs, int nbufs, bool allow_tma_fanout);
 // TMA-staged fan-out (bulk_fanout.cu) for a 16-byte-aligned program.
 reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelParams& kp,
-                                      void* stream);
+                                      int64_t plan_tile_bytes, void* stream);
 // TMA-staged realigning copy (realign_staged.cu) for a program that is not
 // 16-byte aligned, on a grid of num_sms x its resident CTAs per SM.
 reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, void* stream);

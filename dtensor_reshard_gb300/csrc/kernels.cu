@@ -555,7 +555,7 @@ static reshard_status_t launch_tiles(const reshard_plan_s* plan, const Program& 
   kp.pad = 0;
 
   // A fully 16-byte-aligned fan-out goes through the TMA-staged pipeline.
-  if (d.path == RESHARD_PATH_TMA_FANOUT) return launch_fanout_staged(plan, kp, stream);
+  if (d.path == RESHARD_PATH_TMA_FANOUT) return launch_fanout_staged(plan, kp, prog.tile_bytes, stream);
   if (d.kidx == kStagedRealign) return launch_realign_staged(plan->num_sms, kp, stream);
 
   const int planes = prog.has_planes ? 1 : 0;

@@ -167,13 +167,14 @@ struct ChunkWalker {
   // Most rows in one chunk when PAD > 0 (a row table entry each).
   static constexpr uint32_t kMaxRows = STAGE / ((1u + PAD + 15u) & ~15u);
 
-  const KernelParams* p;
-  int64_t u0, u1;
-  int ti;
+  const KernelParams* p = nullptr;
+  int64_t u0 = 0, u1 = 0;
+  int ti = 0;
   int64_t pos, end;
   uint32_t kind, per;  // per: rows per chunk (kind 1) or pieces per row (kind 2)
   reshard_tile_t t;
   bool live;
+  bool live_once = false;  // start_range has run before (ti is meaningful)
 
   __device__ __forceinline__ static uint32_t slot(uint32_t row_bytes) {
     return PAD == 0 ? row_bytes : (row_bytes + PAD + 15u) & ~15u;
@@ -231,6 +232,26 @@ struct ChunkWalker {
     live = u0 < u1;
     if (!live) return;
     int lo = 0, hi = kp->ntiles - 1;  // largest tile with prefix <= u0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (kp->prefix[mid] <= u0) lo = mid;
+      else hi = mid - 1;
+    }
+    ti = lo;
+    enter_tile();
+  }
+  // Walk units [a, b) instead of the CTA's equal share (a piece handed out at
+  // run time); the tile search starts at the current tile when the piece lies
+  // ahead of it, as pieces of one CTA do.
+  __device__ void start_range(const KernelParams* kp, int64_t a, int64_t b) {
+    const bool ahead = live_once && p == kp && a >= kp->prefix[ti];
+    p = kp;
+    u0 = a;
+    u1 = b;
+    live = u0 < u1;
+    live_once = true;
+    if (!live) return;
+    int lo = ahead ? ti : 0, hi = kp->ntiles - 1;  // largest tile with prefix <= u0
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (kp->prefix[mid] <= u0) lo = mid;
