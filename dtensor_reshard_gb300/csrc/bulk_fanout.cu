@@ -24,6 +24,7 @@
 // returns, so the context stays usable; reshard_device_status() reads it.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -55,19 +56,6 @@ __device__ unsigned int g_queue[kQueueSlots][2];
 // the workloads taken together.
 constexpr int64_t kPieceBytes = 32 * 1024;
 constexpr int64_t kPiecesPerCta = 8;
-
-// One chunk, handed from the producer to the consumer together with its stage.
-struct StageDesc {
-  int32_t ti;  // tile index; -1: no more chunks
-  uint32_t kind, bytes;
-  int64_t a, b;
-};
-
-__device__ __forceinline__ uint32_t grab_piece(unsigned int* queue, int lane) {
-  uint32_t piece = 0;
-  if (lane == 0) piece = atomicAdd(&queue[0], 1u);
-  return __shfl_sync(0xffffffffu, piece, 0);
-}
 
 __global__ void __launch_bounds__(kStagedThreads)
     fanout_staged_kernel(const __grid_constant__ KernelParams p, unsigned int* status,
@@ -186,13 +174,7 @@ __global__ void __launch_bounds__(kStagedThreads)
   // both roles are done (every wait above is bounded): count the CTA out, and
   // the last one puts the launch's queue slot back to zero
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(&queue[1], 1u) == gridDim.x - 1) {
-      atomicExch(&queue[0], 0u);
-      atomicExch(&queue[1], 0u);
-    }
-  }
+  finish_queue(queue);
 }
 
 // A wait that nothing will ever answer: exercises the bounded-wait path.
@@ -255,6 +237,28 @@ reshard_status_t device_state(DeviceState* out) {
 
 }  // namespace
 
+reshard_status_t work_queue_slot(unsigned int** slot) {
+  DeviceState d;
+  reshard_status_t st = device_state(&d);
+  if (st != RESHARD_OK) return st;
+  // a slot of its own (launches in flight at once never come near kQueueSlots)
+  *slot = d.queue + 2 * (g_queue_slot.fetch_add(1) % uint32_t(kQueueSlots));
+  return RESHARD_OK;
+}
+
+int64_t work_queue_piece_units(int64_t total_units, int64_t tile_bytes, int64_t grid,
+                               int64_t min_piece_bytes) {
+  const int64_t units = total_units > 0 ? total_units : 1;
+  const int64_t cta = grid > 0 ? grid : 1;
+  const int64_t unit_bytes = tile_bytes / units > 0 ? tile_bytes / units : 1;
+  const int64_t most = (kPieceBytes + unit_bytes - 1) / unit_bytes;
+  // no smaller than min_piece_bytes while every CTA still gets a piece
+  const int64_t least = std::min((min_piece_bytes + unit_bytes - 1) / unit_bytes,
+                                 std::max<int64_t>(1, units / cta));
+  const int64_t piece_units = std::max(units / (cta * kPiecesPerCta), least);
+  return std::max<int64_t>(1, std::min(piece_units, most));
+}
+
 reshard_status_t device_status_word(unsigned int** status) {
   DeviceState d;
   reshard_status_t st = device_state(&d);
@@ -272,13 +276,10 @@ reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelPa
   const unsigned grid = unsigned(kp.total_units < max_grid ? kp.total_units : max_grid);
   KernelParams params = kp;
   unsigned int* status = d.status;
-  // a slot of its own (launches in flight at once never come near kQueueSlots)
-  unsigned int* queue = d.queue + 2 * (g_queue_slot.fetch_add(1) % uint32_t(kQueueSlots));
-  const int64_t units = kp.total_units > 0 ? kp.total_units : 1;
-  const int64_t unit_bytes = plan_tile_bytes / units > 0 ? plan_tile_bytes / units : 1;
-  int64_t piece_units = kp.total_units / (int64_t(grid) * kPiecesPerCta);
-  const int64_t want_units = (kPieceBytes + unit_bytes - 1) / unit_bytes;
-  piece_units = piece_units < 1 ? 1 : piece_units > want_units ? want_units : piece_units;
+  unsigned int* queue = nullptr;
+  st = work_queue_slot(&queue);
+  if (st != RESHARD_OK) return st;
+  int64_t piece_units = work_queue_piece_units(kp.total_units, plan_tile_bytes, grid, 0);
   void* args[] = {&params, &status, &queue, &piece_units};
   cudaError_t ce = cudaLaunchKernel(reinterpret_cast<const void*>(fanout_staged_kernel),
                                     dim3(grid), dim3(kStagedThreads), args,

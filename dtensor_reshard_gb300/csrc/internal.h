@@ -187,7 +187,16 @@ reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelPa
                                       int64_t plan_tile_bytes, void* stream);
 // TMA-staged realigning copy (realign_staged.cu) for a program that is not
 // 16-byte aligned, on a grid of num_sms x its resident CTAs per SM.
-reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, void* stream);
+reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, int64_t tile_bytes,
+                                       void* stream);
+// A work-queue slot {next piece, CTAs finished} of the current device for one
+// launch; the launch's last CTA puts it back to zero (bulk_fanout.cu).
+reshard_status_t work_queue_slot(unsigned int** slot);
+// Work units per queue piece for a program of total_units units and tile_bytes
+// bytes on a grid of `grid` CTAs: about 32 KiB, at least 8 per CTA, but no less
+// than min_piece_bytes while every CTA still gets one (bulk_fanout.cu).
+int64_t work_queue_piece_units(int64_t total_units, int64_t tile_bytes, int64_t grid,
+                               int64_t min_piece_bytes);
 // Device address of the status word that bounded waits report into (bulk_fanout.cu).
 reshard_status_t device_status_word(unsigned int** status);
 // Transpose blocks of a program (transpose.cu); no-op when it has none.

@@ -1,8 +1,10 @@
 // realign_staged.cu -- TMA-staged copy for programs whose offsets, strides, row
 // lengths or buffers are not all 16-byte aligned (sm_103a).
 //
-// Each CTA runs three roles over its equal share of the program's work units
-// (the split of the vector kernel), in chunks of one tile each:
+// Each CTA runs three roles over pieces of consecutive work units that it takes
+// from a per-launch work queue as it goes (CTAs on faster SMs take more), in
+// chunks of one tile each; the producer hands every chunk to the other roles
+// through a descriptor beside its stage:
 //   warp 0, the producer, copies the aligned 16-byte granules that hold the
 //     chunk's source bytes into an input stage -- one cp.async.bulk copy for a
 //     piece of a run, of a long row, or of rows that follow one another in the
@@ -103,7 +105,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
 // BULK requires every destination buffer at the same address mod 16.
 template <bool BULK>
 __global__ void __launch_bounds__(Config<BULK>::kThreads)
-    realign_staged_kernel(const __grid_constant__ KernelParams p, unsigned int* status) {
+    realign_staged_kernel(const __grid_constant__ KernelParams p, unsigned int* status,
+                          unsigned int* queue, int64_t piece_units) {
   using C = Config<BULK>;
   using Walker = typename C::Walker;
   constexpr uint32_t kStageBytes = C::kStageBytes;
@@ -116,6 +119,7 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
   __shared__ int64_t row_doff[kStages][kMaxRows];
   __shared__ uint16_t row_spos[kStages][kMaxRows];
   __shared__ unsigned char* dst_ptr[kStages][kMaxGroup];
+  __shared__ StageDesc desc[kStages];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // bulk: the store warp writes whole granules from the output stages and
   // releases the input stages; otherwise the consumers write everything and
@@ -137,21 +141,30 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
 
   unsigned char* const in_mem = stage_mem;
   unsigned char* const out_mem = stage_mem + size_t(kStages) * kStageBytes;
-  Walker w;
-  w.start(&p);
-  Chunk c;
   uint32_t n = 0;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    Walker w;
+    Chunk c;
     int stage_tile[kStages];
     for (int s = 0; s < kStages; ++s) stage_tile[s] = -1;
+    bool ok = true;
+    const int64_t total = p.total_units;
+    const int64_t npieces = (total + piece_units - 1) / piece_units;
+    uint32_t piece = grab_piece(queue, lane);
+    while (ok && int64_t(piece) < npieces) {
+    const uint32_t next_piece = grab_piece(queue, lane);  // asked early, used later
+    const int64_t u0 = int64_t(piece) * piece_units;
+    w.start_range(&p, u0, min(u0 + piece_units, total));
     while (w.next(&c)) {
       const int s = int(n % kStages);
       if (n >= uint32_t(kStages) && !warp_wait(&empty[s], ((n / kStages) - 1) & 1u)) {
         if (lane == 0) atomicExch(status, kStatusProducerWait);
+        ok = false;
         break;
       }
       const reshard_tile_t& t = w.t;
+      if (lane == 0) desc[s] = StageDesc{c.ti, c.kind, c.bytes, c.a, c.b};
       if (stage_tile[s] != c.ti) {
         // the stage's destination pointers (the stage's last readers are done)
         const uint32_t g0 = p.goff[t.dst_group];
@@ -223,6 +236,21 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
       }
       ++n;
     }
+    piece = next_piece;
+    }
+    // end marker: a stage whose descriptor says "no more chunks", with no bytes
+    if (ok) {
+      const int s = int(n % kStages);
+      if (n >= uint32_t(kStages) && !warp_wait(&empty[s], ((n / kStages) - 1) & 1u)) {
+        if (lane == 0) atomicExch(status, kStatusProducerWait);
+      } else {
+        if (lane == 0) {
+          desc[s].ti = -1;
+          mbar_arrive(&full[s]);
+        }
+        ++n;
+      }
+    }
     // wait (boundedly) for the copies still landing in the stages
     const uint32_t issued = n;
     for (uint32_t m = issued > uint32_t(kStages) ? issued - kStages : 0u; m < issued; ++m)
@@ -230,7 +258,9 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
   } else if (warp < kStoreWarp) {
     // ------------------------------------------------------------ consumers
     const uint32_t ct = threadIdx.x - 32;
-    while (w.next(&c)) {
+    int cur_tile = -1;
+    reshard_tile_t t = {};
+    while (true) {
       const int s = int(n % kStages), o = int(n % kOutStages);
       if (!warp_wait(&full[s], (n / kStages) & 1u) ||
           (bulk && n >= uint32_t(kOutStages) &&
@@ -238,7 +268,16 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
         if (lane == 0) atomicExch(status, kStatusConsumerWait);
         break;
       }
-      const reshard_tile_t& t = w.t;
+      const StageDesc c = desc[s];
+      if (c.ti < 0) {
+        // pass the end on to the store warp through the output stage's barrier
+        if (bulk && lane == 0) mbar_arrive(&out_full[o]);
+        break;
+      }
+      if (c.ti != cur_tile) {
+        t = p.tiles[c.ti];
+        cur_tile = c.ti;
+      }
       const int R = int(p.goff[t.dst_group + 1] - p.goff[t.dst_group]);
       const uint32_t nr = c.kind == 1 ? uint32_t(c.b - c.a) : 1u;
       const uint32_t len = c.kind == 1 ? t.row_bytes : c.bytes;
@@ -301,13 +340,20 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
     }
   } else if (bulk) {
     // ------------------------------------------------------------ store warp
-    while (w.next(&c)) {
+    int cur_tile = -1;
+    reshard_tile_t t = {};
+    while (true) {
       const int s = int(n % kStages), o = int(n % kOutStages);
       if (!warp_wait(&out_full[o], (n / kOutStages) & 1u)) {
         if (lane == 0) atomicExch(status, kStatusConsumerWait);
         break;
       }
-      const reshard_tile_t& t = w.t;
+      const StageDesc c = desc[s];
+      if (c.ti < 0) break;
+      if (c.ti != cur_tile) {
+        t = p.tiles[c.ti];
+        cur_tile = c.ti;
+      }
       const uint32_t R = p.goff[t.dst_group + 1] - p.goff[t.dst_group];
       const uint32_t nr = c.kind == 1 ? uint32_t(c.b - c.a) : 1u;
       const uint32_t len = c.kind == 1 ? t.row_bytes : c.bytes;
@@ -335,6 +381,9 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
     }
     bulk_wait_all();
   }
+  // every role is done (all waits above are bounded): count the CTA out
+  __syncthreads();
+  finish_queue(queue);
 }
 
 std::mutex g_mu;
@@ -360,7 +409,8 @@ cudaError_t prepare(int* blocks_per_sm) {
 
 }  // namespace
 
-reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, void* stream) {
+reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, int64_t tile_bytes,
+                                       void* stream) {
   unsigned int* status = nullptr;
   reshard_status_t st = device_status_word(&status);
   if (st != RESHARD_OK) return st;
@@ -386,7 +436,13 @@ reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, void
   const int64_t max_grid = int64_t(num_sms) * bps;
   const unsigned grid = unsigned(kp.total_units < max_grid ? kp.total_units : max_grid);
   KernelParams params = kp;
-  void* args[] = {&params, &status};
+  unsigned int* queue = nullptr;
+  st = work_queue_slot(&queue);
+  if (st != RESHARD_OK) return st;
+  // pieces of at least 16 KiB: tiny ones cost more in grabs and short chunks
+  // than they gain in balance (measured on the small uneven-stress tensors)
+  int64_t piece_units = work_queue_piece_units(kp.total_units, tile_bytes, grid, 16 * 1024);
+  void* args[] = {&params, &status, &queue, &piece_units};
   if (bulk)
     ce = cudaLaunchKernel(reinterpret_cast<const void*>(realign_staged_kernel<true>), dim3(grid),
                           dim3(Config<true>::kThreads), args, Config<true>::kDynSmem,

@@ -153,6 +153,34 @@ struct Chunk {
   uint32_t bytes;  // bytes of the tile the chunk covers
 };
 
+// One chunk, handed from the producer to its consumers together with its stage
+// (when CTAs take their work from a queue rather than a fixed range).
+struct StageDesc {
+  int32_t ti;  // tile index; -1: no more chunks
+  uint32_t kind, bytes;
+  int64_t a, b;
+};
+
+// The next piece of a launch's work queue {next piece, CTAs finished}, one per
+// call of the warp (lane 0 asks, every lane gets the answer).
+__device__ __forceinline__ uint32_t grab_piece(unsigned int* queue, int lane) {
+  uint32_t piece = 0;
+  if (lane == 0) piece = atomicAdd(&queue[0], 1u);
+  return __shfl_sync(0xffffffffu, piece, 0);
+}
+
+// After every warp of the CTA is done: count the CTA out of the launch; the
+// last one puts the launch's queue slot back to zero for the next launch.
+__device__ __forceinline__ void finish_queue(unsigned int* queue) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&queue[1], 1u) == gridDim.x - 1) {
+      atomicExch(&queue[0], 0u);
+      atomicExch(&queue[1], 0u);
+    }
+  }
+}
+
 // Walks the chunks of this CTA's unit range (the same equal split of the
 // program's work units as the vector kernel); the producer and the consumers
 // each run their own copy and see the same sequence.  A stage holds STAGE
