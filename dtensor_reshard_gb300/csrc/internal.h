@@ -118,7 +118,7 @@ struct Program {
 // Narrow pieces (bytes per row) below this go through transpose blocks, and a
 // block holds at most this many bytes of wide rows in shared memory.
 constexpr int64_t kTransposeMaxWidth = 64;
-constexpr int64_t kTransposeBlockBytes = 24 * 1024;
+constexpr int64_t kTransposeBlockBytes = 20 * 1024;
 // Blocks a transpose group aims for (smaller blocks when the group is small).
 constexpr int64_t kTransposeMinBlocks = 512;
 // Most segments one transpose group may have (the kernel stages them in shared memory).

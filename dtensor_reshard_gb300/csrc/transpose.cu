@@ -182,7 +182,7 @@ __device__ __forceinline__ void scatter_write(const SegInfo* si, int K, const un
   }
 }
 
-__global__ void __launch_bounds__(kTThreads, 3)
+__global__ void __launch_bounds__(kTThreads, 4)
     reshard_transpose_kernel(const __grid_constant__ TransposeParams p) {
   extern __shared__ __align__(16) unsigned char dyn[];
   unsigned char* img = dyn;                // wide rows, shifted by the wide address mod 16
