@@ -24,6 +24,7 @@
 #include <string>
 
 #include "internal.h"
+#include "staging.cuh"
 
 namespace rs {
 namespace {
@@ -172,8 +173,12 @@ __device__ __forceinline__ void scatter_write(const SegInfo* si, int K, const un
       const uint4 v = *reinterpret_cast<const uint4*>(src);
       for (uint32_t r = 0; r < s.rcnt; ++r) {
         unsigned char* base = ptrs[s.rbeg + r] + s.off;  // segment byte 0 of this replica
-        if (lo == 0 && hi == 16 && (reinterpret_cast<uintptr_t>(base) & 15u) == s.gmis) {
-          __stcs(reinterpret_cast<uint4*>(base - s.gmis + 16 * size_t(j)), v);
+        if ((reinterpret_cast<uintptr_t>(base) & 15u) == s.gmis) {
+          // aligned like replica 0: whole granules in one store, partial ones in the
+          // widest aligned stores that fit
+          unsigned char* g = base - s.gmis + 16 * size_t(j);
+          if (lo == 0 && hi == 16) __stcs(reinterpret_cast<uint4*>(g), v);
+          else staging::store_partial16(g, v, lo, hi);
         } else {
           for (uint32_t b = lo; b < hi; ++b) base[16 * j + b - s.gmis] = src[b];
         }
