@@ -123,6 +123,7 @@ reshard_status_t reshard_batch_create(const reshard_plan_t* plans, int32_t nplan
 
 reshard_status_t reshard_batch_execute(reshard_batch_t batch, const void* const* const* src_ptrs,
                                        void* const* const* dst_ptrs, void* stream) {
+  rs::TraceRange trace("reshard.batch_exec");
   if (!rs::batch_live(batch)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid batch handle");
   if (!src_ptrs || !dst_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "null pointer array");
   const size_t n = batch->plans.size();

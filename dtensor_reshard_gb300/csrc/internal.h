@@ -8,9 +8,20 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "reshard.h"
 
 namespace rs {
+
+// A named NVTX range over a host call (plan creation, execution enqueue), so
+// timelines show where the library's time goes; free when no tool is attached.
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
 
 // A multi-row tile whose rows are longer than this is split into one
 // single-row ("run") tile per row, so that work units stay small.

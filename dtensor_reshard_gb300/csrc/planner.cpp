@@ -751,6 +751,7 @@ reshard_status_t create_plan(const int64_t* global_shape, int32_t tensor_ndim,
                              const reshard_placement_t* dst_placements, const int64_t* alias,
                              reshard_plan_t* out_plan) {
   const auto t0 = std::chrono::steady_clock::now();
+  TraceRange trace("reshard.plan");
   if (!out_plan) return fail(RESHARD_ERR_INVALID_ARG, "out_plan is NULL");
   *out_plan = nullptr;
   if (tensor_ndim < 1 || tensor_ndim > RESHARD_MAX_TENSOR_NDIM)
@@ -810,6 +811,7 @@ reshard_status_t derive_plan(const reshard_plan_s* base, const int64_t* src_gone
                              int32_t n_src_gone, const int64_t* dst_gone, int32_t n_dst_gone,
                              reshard_plan_t* out_plan) {
   const auto t0 = std::chrono::steady_clock::now();
+  TraceRange trace("reshard.plan_exclude");
   if (!out_plan) return fail(RESHARD_ERR_INVALID_ARG, "out_plan is NULL");
   *out_plan = nullptr;
   if (n_src_gone < 0 || n_dst_gone < 0 || (n_src_gone > 0 && !src_gone) ||
@@ -1059,6 +1061,7 @@ extern "C" {
 
 reshard_status_t reshard_execute_ex(reshard_plan_t plan, const void* const* src_ptrs,
                                     void* const* dst_ptrs, int32_t kernel, void* stream) {
+  rs::TraceRange trace("reshard.exec");
   if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
   if (kernel != RESHARD_KERNEL_FANOUT && kernel != RESHARD_KERNEL_BOXCOPY)
     return fail(RESHARD_ERR_INVALID_ARG, "unknown kernel");
@@ -1099,6 +1102,7 @@ reshard_status_t reshard_execute(reshard_plan_t plan, const void* const* src_ptr
 reshard_status_t gather_broadcast_execute(reshard_plan_t plan, const void* const* src_ptrs,
                                           void* const* dst_ptrs, void* full_scratch,
                                           size_t scratch_bytes, void* stream) {
+  rs::TraceRange trace("gb.exec");
   if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
   if (plan->stats.global_bytes > 0) {
     if (!full_scratch) return fail(RESHARD_ERR_INVALID_ARG, "full_scratch is NULL");

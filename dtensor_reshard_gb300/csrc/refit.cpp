@@ -111,6 +111,7 @@ reshard_status_t reshard_refit_info(reshard_refit_t refit, int32_t* routes, uint
 reshard_status_t reshard_refit_execute(reshard_refit_t refit, const void* const* const* src_ptrs,
                                        void* const* const* dst_ptrs, void* scratch,
                                        size_t scratch_bytes, void* stream) {
+  rs::TraceRange trace("reshard.refit_exec");
   if (!rs::refit_live(refit)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid refit handle");
   if (!src_ptrs || !dst_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "null pointer array");
   if (!refit->gb_idx.empty() && refit->scratch_bytes > 0) {

@@ -103,6 +103,7 @@ using rs::fail;
 extern "C" reshard_status_t gather_broadcast_execute_static(reshard_plan_t plan,
                                                             const void* const* src_ptrs,
                                                             void* const* dst_ptrs, void* stream) {
+  rs::TraceRange trace("gb.exec_static");
   reshard_stats_t st;
   if (reshard_plan_stats(plan, &st) != RESHARD_OK)
     return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
