@@ -50,6 +50,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=("moe_refit", "hybridflow", "ffn_up", "uneven_stress"),
                     default="moe_refit")
+    ap.add_argument("--config", type=int, choices=(2, 3, 4, 5), default=None,
+                    help="workload by number: 2 FFN up, 3 HybridFlow, 4 uneven stress, 5 MoE "
+                         "(overrides --workload)")
     ap.add_argument("--tensors", default=None,
                     help="comma-separated tensor names to keep from the workload (profiling)")
     ap.add_argument("--kernel", choices=("fanout", "boxcopy"), default="fanout")
@@ -65,7 +68,10 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle sample")
     ap.add_argument("--report", default=None,
                     help="write a per-workload table (JSON lines) to this file")
-    return ap.parse_args(argv)
+    args = ap.parse_args(argv)
+    if args.config is not None:
+        args.workload = {2: "ffn_up", 3: "hybridflow", 4: "uneven_stress", 5: "moe_refit"}[args.config]
+    return args
 
 
 def dist_env():
