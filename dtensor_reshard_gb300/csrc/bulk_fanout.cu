@@ -53,13 +53,21 @@ __device__ unsigned int g_queue[kQueueSlots][2];
 // Units per piece: about kPieceBytes of the program's bytes, and few enough
 // that every CTA can get about kPiecesPerCta pieces (small programs still use
 // the whole grid).  Measured: 32 KiB pieces beat 8-unit and 64 KiB ones over
-// the workloads taken together.
+// the workloads taken together.  The last kTailRounds pieces per CTA are cut
+// kTailDiv times smaller: a CTA holds up to two pieces (the one it works on
+// and the one it has already asked for), so big last pieces leave some SMs
+// busy for two piece-times after the others ran out of work.  A tail piece
+// still moves at least kTailPieceTraffic bytes (read plus written): shorter
+// ones were measured slower on one-to-one copies.
 constexpr int64_t kPieceBytes = 32 * 1024;
 constexpr int64_t kPiecesPerCta = 8;
+constexpr int64_t kTailRounds = 2;
+constexpr int64_t kTailDiv = 4;
+constexpr int64_t kTailPieceTraffic = 40 * 1024;
 
 __global__ void __launch_bounds__(kStagedThreads)
     fanout_staged_kernel(const __grid_constant__ KernelParams p, unsigned int* status,
-                         unsigned int* queue, int64_t piece_units) {
+                         unsigned int* queue, const PieceSchedule sched) {
   extern __shared__ __align__(1024) unsigned char stage_mem[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ StageDesc desc[kStages];
@@ -80,13 +88,13 @@ __global__ void __launch_bounds__(kStagedThreads)
     ChunkWalker<kStageBytes, 0> w;
     Chunk c;
     bool ok = true;
-    const int64_t total = p.total_units;
-    const int64_t npieces = (total + piece_units - 1) / piece_units;
+    const int64_t npieces = sched.count();
     uint32_t piece = grab_piece(queue, lane);
     while (ok && int64_t(piece) < npieces) {
       const uint32_t next_piece = grab_piece(queue, lane);  // asked early, used later
-      const int64_t u0 = int64_t(piece) * piece_units;
-      w.start_range(&p, u0, min(u0 + piece_units, total));
+      int64_t u0, u1;
+      sched.range(piece, &u0, &u1);
+      w.start_range(&p, u0, u1);
       while (w.next(&c)) {
         const int s = int(n % kStages);
         if (n >= uint32_t(kStages) &&
@@ -246,8 +254,8 @@ reshard_status_t work_queue_slot(unsigned int** slot) {
   return RESHARD_OK;
 }
 
-int64_t work_queue_piece_units(int64_t total_units, int64_t tile_bytes, int64_t grid,
-                               int64_t min_piece_bytes) {
+PieceSchedule work_queue_schedule(int64_t total_units, int64_t tile_bytes, int64_t write_bytes,
+                                  int64_t grid, int64_t min_piece_bytes) {
   const int64_t units = total_units > 0 ? total_units : 1;
   const int64_t cta = grid > 0 ? grid : 1;
   const int64_t unit_bytes = tile_bytes / units > 0 ? tile_bytes / units : 1;
@@ -256,7 +264,16 @@ int64_t work_queue_piece_units(int64_t total_units, int64_t tile_bytes, int64_t 
   const int64_t least = std::min((min_piece_bytes + unit_bytes - 1) / unit_bytes,
                                  std::max<int64_t>(1, units / cta));
   const int64_t piece_units = std::max(units / (cta * kPiecesPerCta), least);
-  return std::max<int64_t>(1, std::min(piece_units, most));
+  PieceSchedule s;
+  s.total = total_units > 0 ? total_units : 0;
+  s.big = std::max<int64_t>(1, std::min(piece_units, most));
+  const int64_t unit_traffic = std::max<int64_t>(1, (tile_bytes + write_bytes) / units);
+  s.small = std::max({std::min(s.big, least), s.big / kTailDiv,
+                      (kTailPieceTraffic + unit_traffic - 1) / unit_traffic, int64_t(1)});
+  s.small = std::min(s.small, s.big);
+  const int64_t tail = kTailRounds * cta * s.big;
+  s.split = s.total > tail ? (s.total - tail) / s.big * s.big : 0;
+  return s;
 }
 
 reshard_status_t device_status_word(unsigned int** status) {
@@ -268,7 +285,7 @@ reshard_status_t device_status_word(unsigned int** status) {
 }
 
 reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelParams& kp,
-                                      int64_t plan_tile_bytes, void* stream) {
+                                      const Program& prog, void* stream) {
   DeviceState d;
   reshard_status_t st = device_state(&d);
   if (st != RESHARD_OK) return st;
@@ -279,8 +296,9 @@ reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelPa
   unsigned int* queue = nullptr;
   st = work_queue_slot(&queue);
   if (st != RESHARD_OK) return st;
-  int64_t piece_units = work_queue_piece_units(kp.total_units, plan_tile_bytes, grid, 0);
-  void* args[] = {&params, &status, &queue, &piece_units};
+  PieceSchedule sched = work_queue_schedule(kp.total_units, prog.tile_bytes, prog.write_bytes,
+                                            grid, 0);
+  void* args[] = {&params, &status, &queue, &sched};
   cudaError_t ce = cudaLaunchKernel(reinterpret_cast<const void*>(fanout_staged_kernel),
                                     dim3(grid), dim3(kStagedThreads), args,
                                     kStages * kStageBytes, static_cast<cudaStream_t>(stream));

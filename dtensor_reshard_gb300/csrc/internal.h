@@ -116,6 +116,7 @@ struct Program {
   bool staged = false;      // eligible for the TMA-staged fan-out kernel when 16-byte aligned
   int max_fanout = 0;       // largest destination group
   int64_t tile_bytes = 0;   // source bytes of all tiles
+  int64_t write_bytes = 0;  // bytes written: each tile's bytes times its replicas
   int64_t long_row_bytes = 0;  // ... of those in rows of at least 512 bytes (runs included)
   int64_t wide_row_bytes = 0;  // ... of those in rows of at least 8 KiB (runs included)
   int64_t total_units() const { return prefix.empty() ? 0 : prefix.back(); }
@@ -195,19 +196,41 @@ struct Dispatch {
 Dispatch decide(const Program& prog, unsigned char* const* bufs, int nbufs, bool allow_tma_fanout);
 // TMA-staged fan-out (bulk_fanout.cu) for a 16-byte-aligned program.
 reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelParams& kp,
-                                      int64_t plan_tile_bytes, void* stream);
+                                      const Program& prog, void* stream);
 // TMA-staged realigning copy (realign_staged.cu) for a program that is not
 // 16-byte aligned, on a grid of num_sms x its resident CTAs per SM.
-reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, int64_t tile_bytes,
+reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, const Program& prog,
                                        void* stream);
 // A work-queue slot {next piece, CTAs finished} of the current device for one
 // launch; the launch's last CTA puts it back to zero (bulk_fanout.cu).
 reshard_status_t work_queue_slot(unsigned int** slot);
-// Work units per queue piece for a program of total_units units and tile_bytes
-// bytes on a grid of `grid` CTAs: about 32 KiB, at least 8 per CTA, but no less
-// than min_piece_bytes while every CTA still gets one (bulk_fanout.cu).
-int64_t work_queue_piece_units(int64_t total_units, int64_t tile_bytes, int64_t grid,
-                               int64_t min_piece_bytes);
+// The pieces a work queue hands out, in order: pieces of `big` units up to unit
+// `split` (a multiple of big), then pieces of `small` units up to `total`, so
+// that the last pieces taken are short and the CTAs of a launch finish close
+// together.
+struct PieceSchedule {
+  int64_t total, big, split, small;
+  RS_HOST_DEVICE int64_t count() const { return split / big + (total - split + small - 1) / small; }
+  // Units [*u0, *u1) of piece i < count().
+  RS_HOST_DEVICE void range(int64_t i, int64_t* u0, int64_t* u1) const {
+    const int64_t nbig = split / big;
+    if (i < nbig) {
+      *u0 = i * big;
+      *u1 = *u0 + big;
+    } else {
+      *u0 = split + (i - nbig) * small;
+      *u1 = *u0 + small < total ? *u0 + small : total;
+    }
+  }
+};
+// The queue pieces for a program of total_units units that reads tile_bytes
+// and writes write_bytes, on a grid of `grid` CTAs: big pieces of about 32 KiB
+// read, at least 8 per CTA, but no less than min_piece_bytes while every CTA
+// still gets one; the last two rounds of the grid in pieces a quarter that
+// size, but of at least 40 KiB read plus written and still no less than
+// min_piece_bytes (bulk_fanout.cu).
+PieceSchedule work_queue_schedule(int64_t total_units, int64_t tile_bytes, int64_t write_bytes,
+                                  int64_t grid, int64_t min_piece_bytes);
 // Device address of the status word that bounded waits report into (bulk_fanout.cu).
 reshard_status_t device_status_word(unsigned int** status);
 // Transpose blocks of a program (transpose.cu); no-op when it has none.

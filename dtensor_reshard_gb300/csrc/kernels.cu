@@ -555,9 +555,9 @@ static reshard_status_t launch_tiles(const reshard_plan_s* plan, const Program& 
   kp.pad = 0;
 
   // A fully 16-byte-aligned fan-out goes through the TMA-staged pipeline.
-  if (d.path == RESHARD_PATH_TMA_FANOUT) return launch_fanout_staged(plan, kp, prog.tile_bytes, stream);
+  if (d.path == RESHARD_PATH_TMA_FANOUT) return launch_fanout_staged(plan, kp, prog, stream);
   if (d.kidx == kStagedRealign)
-    return launch_realign_staged(plan->num_sms, kp, prog.tile_bytes, stream);
+    return launch_realign_staged(plan->num_sms, kp, prog, stream);
 
   const int planes = prog.has_planes ? 1 : 0;
   const int kidx = d.kidx;
@@ -622,7 +622,7 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
   for (int i = nbufs; i < RESHARD_MAX_EXEC_BUFFERS; ++i) kp.bufs[i] = nullptr;
   kp.flags = d.flags;
   kp.pad = 0;
-  if (kidx == kStagedRealign) return launch_realign_staged(num_sms, kp, prog.tile_bytes, stream);
+  if (kidx == kStagedRealign) return launch_realign_staged(num_sms, kp, prog, stream);
 
   const int64_t max_grid = int64_t(num_sms) * bps;
   const unsigned grid = unsigned(total < max_grid ? total : max_grid);

@@ -271,6 +271,7 @@ void finish_program(Program& P) {
     if (t.nplanes > 1) P.has_planes = true;
     const int64_t bytes = int64_t(t.row_bytes) * t.nrows * t.nplanes;
     P.tile_bytes += bytes;
+    P.write_bytes += bytes * int64_t(P.goff[t.dst_group + 1] - P.goff[t.dst_group]);
     if (t.row_bytes >= 512) P.long_row_bytes += bytes;
     if (t.row_bytes >= 8192) P.wide_row_bytes += bytes;
   }

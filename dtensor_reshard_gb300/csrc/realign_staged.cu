@@ -106,7 +106,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
 template <bool BULK>
 __global__ void __launch_bounds__(Config<BULK>::kThreads)
     realign_staged_kernel(const __grid_constant__ KernelParams p, unsigned int* status,
-                          unsigned int* queue, int64_t piece_units) {
+                          unsigned int* queue, const PieceSchedule sched) {
   using C = Config<BULK>;
   using Walker = typename C::Walker;
   constexpr uint32_t kStageBytes = C::kStageBytes;
@@ -149,13 +149,13 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
     int stage_tile[kStages];
     for (int s = 0; s < kStages; ++s) stage_tile[s] = -1;
     bool ok = true;
-    const int64_t total = p.total_units;
-    const int64_t npieces = (total + piece_units - 1) / piece_units;
+    const int64_t npieces = sched.count();
     uint32_t piece = grab_piece(queue, lane);
     while (ok && int64_t(piece) < npieces) {
     const uint32_t next_piece = grab_piece(queue, lane);  // asked early, used later
-    const int64_t u0 = int64_t(piece) * piece_units;
-    w.start_range(&p, u0, min(u0 + piece_units, total));
+    int64_t u0, u1;
+    sched.range(piece, &u0, &u1);
+    w.start_range(&p, u0, u1);
     while (w.next(&c)) {
       const int s = int(n % kStages);
       if (n >= uint32_t(kStages) && !warp_wait(&empty[s], ((n / kStages) - 1) & 1u)) {
@@ -409,7 +409,7 @@ cudaError_t prepare(int* blocks_per_sm) {
 
 }  // namespace
 
-reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, int64_t tile_bytes,
+reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, const Program& prog,
                                        void* stream) {
   unsigned int* status = nullptr;
   reshard_status_t st = device_status_word(&status);
@@ -441,8 +441,9 @@ reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, int6
   if (st != RESHARD_OK) return st;
   // pieces of at least 16 KiB: tiny ones cost more in grabs and short chunks
   // than they gain in balance (measured on the small uneven-stress tensors)
-  int64_t piece_units = work_queue_piece_units(kp.total_units, tile_bytes, grid, 16 * 1024);
-  void* args[] = {&params, &status, &queue, &piece_units};
+  PieceSchedule sched = work_queue_schedule(kp.total_units, prog.tile_bytes, prog.write_bytes, grid,
+                                            16 * 1024);
+  void* args[] = {&params, &status, &queue, &sched};
   if (bulk)
     ce = cudaLaunchKernel(reinterpret_cast<const void*>(realign_staged_kernel<true>), dim3(grid),
                           dim3(Config<true>::kThreads), args, Config<true>::kDynSmem,
