@@ -100,6 +100,7 @@ reshard_status_t reshard_batch_create(const reshard_plan_t* plans, int32_t nplan
       C.max_fanout = std::max(C.max_fanout, F.max_fanout);
       C.tile_bytes += F.tile_bytes;
       C.write_bytes += F.write_bytes;
+      C.talign_bits |= F.talign_bits;
       C.long_row_bytes += F.long_row_bytes;
       C.wide_row_bytes += F.wide_row_bytes;
       B->plans.push_back(p);

@@ -123,6 +123,9 @@ struct Program {
   // transpose blocks (narrow innermost pieces grouped by shared rows)
   std::vector<reshard_tblock_t> tblocks;
   std::vector<reshard_tseg_t> tsegs;
+  // OR of every block's row length and wide offset and every segment's width,
+  // column and narrow offset (with the buffers' addresses: the element width)
+  uint64_t talign_bits = 0;
   const reshard_tblock_t* d_tblocks = nullptr;
   const reshard_tseg_t* d_tsegs = nullptr;
 };

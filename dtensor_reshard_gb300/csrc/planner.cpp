@@ -667,6 +667,10 @@ reshard_status_t build_plan(reshard_plan_s* P) {
     S.fanout_write_bytes += R * tile_bytes(t);
   }
   for (const reshard_tblock_t& b : PF.tblocks) {
+    PF.talign_bits |= uint64_t(b.row_bytes) | uint64_t(b.wide_off);
+    for (uint32_t k = b.seg_begin; k < b.seg_begin + b.seg_count; ++k)
+      PF.talign_bits |= uint64_t(PF.tsegs[k].width) | PF.tsegs[k].col |
+                        uint64_t(PF.tsegs[k].narrow_off);
     const int64_t bytes = int64_t(b.row_bytes) * b.nrows;
     S.fanout_read_bytes += bytes;
     if (b.direction == 0) {

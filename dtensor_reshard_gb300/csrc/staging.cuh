@@ -19,7 +19,8 @@ constexpr uint32_t kWaitPolls = 1u << 22;
 enum : unsigned int {
   kStatusProducerWait = 1,  // producer gave up waiting for a free stage
   kStatusConsumerWait = 2,  // consumer gave up waiting for a loaded stage
-  kStatusSelfTest = 3       // the self-test's deliberately unanswered wait ran out
+  kStatusSelfTest = 3,      // the self-test's deliberately unanswered wait ran out
+  kStatusTransposeAlign = 4  // a transpose block did not allow its launch's element width
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

@@ -6,16 +6,22 @@
 // buffer (or destination group) that fills bytes [col, col + width) of every
 // wide row.  A CTA takes a contiguous share of the program's blocks and, per
 // block:
-//   gather  (narrow sources -> wide destination group): copies every segment
-//           into its columns of a shared-memory image of the rows, then writes
-//           the image with 16-byte stores to every replica;
-//   scatter (wide source -> narrow destination groups): loads the rows with
-//           16-byte loads, then writes every segment to its replicas.
+//   gather  (narrow sources -> wide destination group): every thread loads
+//           whole aligned 16-byte granules of the segments' dense ranges and
+//           puts their elements into their columns of a shared-memory image of
+//           the rows, then the image goes out with 16-byte stores to every
+//           replica;
+//   scatter (wide source -> narrow destination groups): the rows come in with
+//           16-byte loads, then every thread builds whole aligned 16-byte
+//           granules of the segments' dense ranges from the image and stores
+//           each to every replica of its segment.
 // The shared-memory image is shifted by the wide side's address mod 16, so its
-// 16-byte vectors line up with aligned global addresses.  Narrow-side copies
-// move elements of U bytes (the widest unit every address, width and column of
-// the block allows), walking each segment's dense range in order, so both
-// sides of every copy are coalesced.
+// 16-byte vectors line up with aligned global addresses.  Inside a granule the
+// elements are U bytes (the widest unit every address, width and column of the
+// block allows) and follow a segment's rows in order, so a thread finds the
+// image position of its first element with one division and steps from there;
+// the granules of all segments are numbered in one sequence, so every thread
+// has the same amount of work whatever the segments' sizes.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,13 +38,11 @@ namespace {
 constexpr int kTThreads = 256;
 constexpr int kTVecUnroll = 4;  // wide-side 16-byte loads in flight per thread
 constexpr int kImageBytes = int(kTransposeBlockBytes) + 64;
-// staging area for the narrow side: every segment's dense range in whole 16-byte
-// granules (at most one extra granule per segment)
-constexpr int kStageBytes = int(kTransposeBlockBytes) + 32 * int(kTransposeMaxSegs) + 64;
-constexpr int kDynSmem = kImageBytes + kStageBytes;
+constexpr int kDynSmem = kImageBytes;
 constexpr int kMaxReplicaPtrs = int(kTransposeMaxReplicaPtrs);
 
 struct TransposeParams {
+  unsigned int* status;
   const reshard_tblock_t* blocks;
   const reshard_tseg_t* segs;
   const uint32_t* goff;
@@ -90,108 +94,158 @@ __device__ __forceinline__ int find_granule(const SegInfo* si, int K, uint32_t g
   return lo;
 }
 
-// gather, phase 1a: every segment's dense source range -> staging, as whole aligned
-// 16-byte granules (granule j of segment k at staging byte 16 (gstart_k + j))
-__device__ __forceinline__ void gather_stage(const SegInfo* si, int K, uint32_t ngran,
-                                             unsigned char* stg) {
+// Element i (of 16 / U) of a 16-byte granule held as four words.
+template <int U>
+__device__ __forceinline__ typename UType<U>::T granule_elem(const uint4& v, int i) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (U == 8) {
+    return make_uint2(w[2 * i], w[2 * i + 1]);
+  } else if constexpr (U == 4) {
+    return w[i];
+  } else if constexpr (U == 2) {
+    return uint16_t(w[i >> 1] >> (16 * (i & 1)));
+  } else {
+    return uint8_t(w[i >> 2] >> (8 * (i & 3)));
+  }
+}
+template <int U>
+__device__ __forceinline__ void granule_put(uint32_t (&w)[4], int i, typename UType<U>::T e) {
+  if constexpr (U == 8) {
+    w[2 * i] = e.x;
+    w[2 * i + 1] = e.y;
+  } else if constexpr (U == 4) {
+    w[i] = e;
+  } else if constexpr (U == 2) {
+    w[i >> 1] |= uint32_t(e) << (16 * (i & 1));
+  } else {
+    w[i >> 2] |= uint32_t(e) << (8 * (i & 3));
+  }
+}
+
+// Where granule g (flattened over the segments' dense ranges) starts: its
+// segment, the bytes [lo, hi) of the granule that belong to it, and the
+// image address of its first element; the elements of a segment follow one
+// another along a row of `units` elements, then wrap to the next row.
+struct GranuleWalk {
+  const SegInfo* s;
+  uint32_t j, lo, hi, c;
+  uint32_t img_off;  // image byte of the first element (before the image shift)
+};
+template <int U>
+__device__ __forceinline__ GranuleWalk granule_walk(const SegInfo* si, int K, uint32_t g,
+                                                    uint32_t L) {
+  GranuleWalk w;
+  w.s = &si[find_granule(si, K, g)];
+  const SegInfo& s = *w.s;
+  w.j = g - s.gstart;
+  w.lo = w.j == 0 ? s.gmis : 0u;
+  w.hi = min(16u, s.gmis + s.nbytes - 16u * w.j);
+  const uint32_t e0 = (16u * w.j + w.lo - s.gmis) / U;
+  const uint32_t row = fastdiv(e0, s.m, s.l);
+  w.c = e0 - row * s.units;
+  w.img_off = s.col + row * L + w.c * U;
+  return w;
+}
+
+// gather: each thread loads whole aligned 16-byte granules of the segments'
+// dense source ranges (kTVecUnroll in flight) and puts their elements into
+// the image columns they belong to.
+template <int U>
+__device__ __forceinline__ void gather_direct(const SegInfo* si, int K, uint32_t ngran,
+                                              unsigned char* img, uint32_t mis, uint32_t L) {
+  using T = typename UType<U>::T;
+  constexpr int E = 16 / U;
 #pragma unroll 1
   for (uint32_t g0 = threadIdx.x; g0 < ngran; g0 += kTThreads * kTVecUnroll) {
     uint4 v[kTVecUnroll];
 #pragma unroll
-    for (int j = 0; j < kTVecUnroll; ++j) {
-      const uint32_t g = g0 + j * kTThreads;
+    for (int q = 0; q < kTVecUnroll; ++q) {
+      const uint32_t g = g0 + q * kTThreads;
       if (g < ngran) {
         const SegInfo& s = si[find_granule(si, K, g)];
-        v[j] = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(g - s.gstart)));
+        v[q] = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(g - s.gstart)));
       }
     }
 #pragma unroll
-    for (int j = 0; j < kTVecUnroll; ++j) {
-      const uint32_t g = g0 + j * kTThreads;
-      if (g < ngran) *reinterpret_cast<uint4*>(stg + 16 * size_t(g)) = v[j];
-    }
-  }
-}
-
-// gather, phase 1b: staging -> columns of the image (shared memory only), one
-// warp per segment, lanes over its elements
-template <int U>
-__device__ __forceinline__ void gather_place(const SegInfo* si, int K, uint32_t nr,
-                                             const unsigned char* stg, unsigned char* img,
-                                             uint32_t mis, uint32_t L) {
-  using T = typename UType<U>::T;
-  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
-  for (int k = warp; k < K; k += kTThreads / 32) {
-    const SegInfo& s = si[k];
-    const uint32_t n = s.units * nr;
-    const unsigned char* from = stg + 16 * s.gstart + s.gmis;
-    unsigned char* to = img + mis + s.col;
-#pragma unroll 4
-    for (uint32_t local = lane; local < n; local += 32) {
-      const uint32_t row = fastdiv(local, s.m, s.l);
-      const uint32_t c = local - row * s.units;
-      *reinterpret_cast<T*>(to + row * L + c * U) = *reinterpret_cast<const T*>(from + local * U);
-    }
-  }
-}
-
-// scatter, phase 2a: image columns -> staging, laid out so that every segment's
-// destination range (replica 0) falls on whole 16-byte granules; warp per segment
-template <int U>
-__device__ __forceinline__ void scatter_stage(const SegInfo* si, int K, uint32_t nr,
-                                              const unsigned char* img, uint32_t mis, uint32_t L,
-                                              unsigned char* stg) {
-  using T = typename UType<U>::T;
-  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
-  for (int k = warp; k < K; k += kTThreads / 32) {
-    const SegInfo& s = si[k];
-    const uint32_t n = s.units * nr;
-    const unsigned char* from = img + mis + s.col;
-    unsigned char* to = stg + 16 * s.gstart + s.gmis;
-#pragma unroll 4
-    for (uint32_t local = lane; local < n; local += 32) {
-      const uint32_t row = fastdiv(local, s.m, s.l);
-      const uint32_t c = local - row * s.units;
-      *reinterpret_cast<T*>(to + local * U) = *reinterpret_cast<const T*>(from + row * L + c * U);
-    }
-  }
-}
-
-// scatter, phase 2b: staging granules -> every replica of every segment, warp per
-// segment; whole granules of replicas aligned like replica 0 go out as 16-byte stores
-__device__ __forceinline__ void scatter_write(const SegInfo* si, int K, const unsigned char* stg,
-                                              unsigned char* const* ptrs) {
-  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
-  for (int k = warp; k < K; k += kTThreads / 32) {
-    const SegInfo& s = si[k];
-    const uint32_t end = s.gmis + s.nbytes;      // segment end, granule-relative bytes
-    const uint32_t ng = (end + 15u) >> 4;
-    for (uint32_t j = lane; j < ng; j += 32) {
-      const uint32_t lo = j == 0 ? s.gmis : 0u;
-      const uint32_t hi = min(16u, end - 16u * j);
-      const unsigned char* src = stg + 16 * size_t(s.gstart + j);
-      const uint4 v = *reinterpret_cast<const uint4*>(src);
-      for (uint32_t r = 0; r < s.rcnt; ++r) {
-        unsigned char* base = ptrs[s.rbeg + r] + s.off;  // segment byte 0 of this replica
-        if ((reinterpret_cast<uintptr_t>(base) & 15u) == s.gmis) {
-          // aligned like replica 0: whole granules in one store, partial ones in the
-          // widest aligned stores that fit
-          unsigned char* g = base - s.gmis + 16 * size_t(j);
-          if (lo == 0 && hi == 16) __stcs(reinterpret_cast<uint4*>(g), v);
-          else staging::store_partial16(g, v, lo, hi);
-        } else {
-          for (uint32_t b = lo; b < hi; ++b) base[16 * j + b - s.gmis] = src[b];
+    for (int q = 0; q < kTVecUnroll; ++q) {
+      const uint32_t g = g0 + q * kTThreads;
+      if (g < ngran) {
+        GranuleWalk w = granule_walk<U>(si, K, g, L);
+        const uint32_t units = w.s->units, wrap = L - units * U;
+        unsigned char* to = img + mis + w.img_off;
+        const int ilo = int(w.lo / U), ihi = int(w.hi / U);
+        uint32_t c = w.c;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          if (i >= ilo && i < ihi) {
+            *reinterpret_cast<T*>(to) = granule_elem<U>(v[q], i);
+            to += U;
+            if (++c == units) {
+              c = 0;
+              to += wrap;
+            }
+          }
         }
       }
     }
   }
 }
 
+// scatter: each thread builds whole 16-byte granules of the segments' dense
+// destination ranges (aligned like replica 0) from the image columns and
+// writes them to every replica of the segment.
+template <int U>
+__device__ __forceinline__ void scatter_direct(const SegInfo* si, int K, uint32_t ngran,
+                                               const unsigned char* img, uint32_t mis, uint32_t L,
+                                               unsigned char* const* ptrs) {
+  using T = typename UType<U>::T;
+  constexpr int E = 16 / U;
+#pragma unroll 1
+  for (uint32_t g = threadIdx.x; g < ngran; g += kTThreads) {
+    GranuleWalk w = granule_walk<U>(si, K, g, L);
+    const SegInfo& s = *w.s;
+    const uint32_t units = s.units, wrap = L - units * U;
+    const unsigned char* from = img + mis + w.img_off;
+    const int ilo = int(w.lo / U), ihi = int(w.hi / U);
+    uint32_t c = w.c;
+    uint32_t words[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      if (i >= ilo && i < ihi) {
+        granule_put<U>(words, i, *reinterpret_cast<const T*>(from));
+        from += U;
+        if (++c == units) {
+          c = 0;
+          from += wrap;
+        }
+      }
+    }
+    const uint4 v = make_uint4(words[0], words[1], words[2], words[3]);
+    for (uint32_t r = 0; r < s.rcnt; ++r) {
+      unsigned char* base = ptrs[s.rbeg + r] + s.off;  // segment byte 0 of this replica
+      if ((reinterpret_cast<uintptr_t>(base) & 15u) == s.gmis) {
+        // aligned like replica 0: a whole granule in one store, a partial one in the
+        // widest aligned stores that fit
+        unsigned char* gp = base - s.gmis + 16 * size_t(w.j);
+        if (w.lo == 0 && w.hi == 16) __stcs(reinterpret_cast<uint4*>(gp), v);
+        else staging::store_partial16(gp, v, w.lo, w.hi);
+      } else {
+        for (uint32_t b = w.lo; b < w.hi; ++b)
+          base[16 * w.j + b - s.gmis] = uint8_t(staging::word_at(v, b >> 2) >> (8u * (b & 3u)));
+      }
+    }
+  }
+}
+
+// U: the element width in bytes (1, 2, 4 or 8) that divides every block's row
+// length, columns, widths and narrow addresses (the host takes it from the
+// plan's offsets and the buffers' addresses); a block that does not allow it
+// is skipped and reported in the status word.
+template <int U>
 __global__ void __launch_bounds__(kTThreads, 4)
     reshard_transpose_kernel(const __grid_constant__ TransposeParams p) {
   extern __shared__ __align__(16) unsigned char dyn[];
-  unsigned char* img = dyn;                // wide rows, shifted by the wide address mod 16
-  unsigned char* stg = dyn + kImageBytes;  // narrow ranges in whole 16-byte granules
+  unsigned char* img = dyn;  // wide rows, shifted by the wide address mod 16
   __shared__ SegInfo si[kTransposeMaxSegs];
   __shared__ unsigned char* ptrs[kMaxReplicaPtrs];
   __shared__ unsigned int s_align;
@@ -218,7 +272,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
     __syncthreads();
     const uint32_t mis = gather ? uint32_t(reinterpret_cast<uintptr_t>(ptrs[0] + blk.wide_off) & 15u)
                                 : uint32_t(reinterpret_cast<uintptr_t>(wsrc) & 15u);
-    if (threadIdx.x == 0) s_align = L | 8u;
+    if (threadIdx.x == 0) s_align = L;
     __syncthreads();
     // per-segment set-up (one thread per segment), alignment of every narrow access
     for (uint32_t k = threadIdx.x; k < K; k += kTThreads) {
@@ -243,8 +297,10 @@ __global__ void __launch_bounds__(kTThreads, 4)
       atomicOr(&s_align, a);
     }
     __syncthreads();
-    const unsigned int al = s_align;
-    const uint32_t U = (al & 1u) ? 1u : (al & 2u) ? 2u : (al & 4u) ? 4u : 8u;
+    if ((s_align & uint32_t(U - 1)) != 0) {
+      if (threadIdx.x == 0) atomicExch(p.status, staging::kStatusTransposeAlign);
+      continue;  // uniform: every thread read the same s_align
+    }
     if (threadIdx.x < 32) {
       // staging granules and replica pointer slots, exclusive prefix in segment order:
       // each lane owns segments [4 lane, 4 lane + 4) (K <= 128), then a warp scan
@@ -295,14 +351,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
     const uint32_t ngran = s_ngran;
 
     if (gather) {
-      gather_stage(si, int(K), ngran, stg);
-      __syncthreads();
-      switch (U) {
-        case 1: gather_place<1>(si, int(K), nr, stg, img, mis, L); break;
-        case 2: gather_place<2>(si, int(K), nr, stg, img, mis, L); break;
-        case 4: gather_place<4>(si, int(K), nr, stg, img, mis, L); break;
-        default: gather_place<8>(si, int(K), nr, stg, img, mis, L); break;
-      }
+      gather_direct<U>(si, int(K), ngran, img, mis, L);
       __syncthreads();
       // image [mis, mis + n) -> each replica's [wide_off, wide_off + n)
       const uint32_t h = min((16u - mis) & 15u, n);
@@ -339,20 +388,17 @@ __global__ void __launch_bounds__(kTThreads, 4)
         }
       }
       __syncthreads();
-      switch (U) {
-        case 1: scatter_stage<1>(si, int(K), nr, img, mis, L, stg); break;
-        case 2: scatter_stage<2>(si, int(K), nr, img, mis, L, stg); break;
-        case 4: scatter_stage<4>(si, int(K), nr, img, mis, L, stg); break;
-        default: scatter_stage<8>(si, int(K), nr, img, mis, L, stg); break;
-      }
-      __syncthreads();
-      scatter_write(si, int(K), stg, ptrs);
+      scatter_direct<U>(si, int(K), ngran, img, mis, L, ptrs);
     }
   }
 }
 
 std::mutex g_t_mu;
-std::map<int, int> g_t_occ;  // device -> blocks per SM
+std::map<std::pair<int, int>, int> g_t_occ;  // (device, log2 U) -> blocks per SM
+
+using TransposeFn = void (*)(TransposeParams);
+const TransposeFn kTransposeKernels[4] = {reshard_transpose_kernel<1>, reshard_transpose_kernel<2>,
+                                          reshard_transpose_kernel<4>, reshard_transpose_kernel<8>};
 
 }  // namespace
 
@@ -364,25 +410,33 @@ reshard_status_t launch_transposes(const reshard_plan_s* plan, const Program& pr
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
+  // element width: the widest of 1, 2, 4, 8 bytes that divides every row length,
+  // column, width and offset of the blocks and every buffer's address
+  uint64_t bits = prog.talign_bits | 8u;
+  for (int i = 0; i < nbufs; ++i) bits |= uint64_t(reinterpret_cast<uintptr_t>(bufs[i]));
+  const int ulog = (bits & 1u) ? 0 : (bits & 2u) ? 1 : (bits & 4u) ? 2 : 3;
+  const void* fn = reinterpret_cast<const void*>(kTransposeKernels[ulog]);
   int bps = 0;
   {
     std::lock_guard<std::mutex> lk(g_t_mu);
-    auto it = g_t_occ.find(dev);
+    auto it = g_t_occ.find({dev, ulog});
     if (it == g_t_occ.end()) {
-      ce = cudaFuncSetAttribute(reinterpret_cast<const void*>(reshard_transpose_kernel),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+      ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
       if (ce == cudaSuccess)
-        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &bps, reinterpret_cast<const void*>(reshard_transpose_kernel), kTThreads, kDynSmem);
+        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, kTThreads, kDynSmem);
       if (ce != cudaSuccess)
         return fail(RESHARD_ERR_CUDA, std::string("transpose kernel set-up: ") + cudaGetErrorString(ce));
       bps = bps > 0 ? bps : 1;
-      g_t_occ[dev] = bps;
+      g_t_occ[{dev, ulog}] = bps;
     } else {
       bps = it->second;
     }
   }
+  unsigned int* status = nullptr;
+  reshard_status_t st = device_status_word(&status);
+  if (st != RESHARD_OK) return st;
   TransposeParams tp;
+  tp.status = status;
   tp.blocks = prog.d_tblocks;
   tp.segs = prog.d_tsegs;
   tp.goff = prog.d_goff;
@@ -395,8 +449,8 @@ reshard_status_t launch_transposes(const reshard_plan_s* plan, const Program& pr
   const int64_t max_grid = int64_t(plan->num_sms) * bps;
   const unsigned grid = unsigned(tp.nblocks < max_grid ? tp.nblocks : max_grid);
   void* args[] = {&tp};
-  ce = cudaLaunchKernel(reinterpret_cast<const void*>(reshard_transpose_kernel), dim3(grid),
-                        dim3(kTThreads), args, kDynSmem, static_cast<cudaStream_t>(stream));
+  ce = cudaLaunchKernel(fn, dim3(grid), dim3(kTThreads), args, kDynSmem,
+                        static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(ce));
   return RESHARD_OK;
