@@ -94,7 +94,7 @@ def load_peaks():
 def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for name in ("kernels.cu", "bulk_fanout.cu", "internal.h"):
+    for name in ("kernels.cu", "bulk_fanout.cu", "internal.h", "staging.cuh"):
         with open(os.path.join(ROOT, "dtensor_reshard_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
