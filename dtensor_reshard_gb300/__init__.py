@@ -125,6 +125,8 @@ def _load():
         "reshard_batch_execute": ([vp, ctypes.POINTER(vpp), ctypes.POINTER(vpp), vp],
                                   ctypes.c_int),
         "reshard_batch_destroy": ([vp], ctypes.c_int),
+        "reshard_batch_classes": ([vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+                                  ctypes.c_int),
         "reshard_refit_create": ([ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                   ctypes.c_uint32, vpp], ctypes.c_int),
         "reshard_refit_info": ([vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_uint64)],
@@ -359,6 +361,14 @@ def reshard_batch_execute(batch: Batch, src_ptrs_per_plan, dst_ptrs_per_plan, st
     da = (ctypes.POINTER(ctypes.c_void_p) * len(dsts))(
         *[ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)) for a in dsts])
     _check(_lib.reshard_batch_execute(batch, sa, da, _stream(stream)), "reshard_batch_execute")
+
+
+def reshard_batch_classes(batch: Batch):
+    """(number of launch classes, class of each plan or -1 for a plan with nothing to copy)."""
+    n = ctypes.c_int32()
+    per = (ctypes.c_int32 * len(batch.plans))()
+    _check(_lib.reshard_batch_classes(batch, ctypes.byref(n), per), "reshard_batch_classes")
+    return int(n.value), [int(x) for x in per]
 
 
 def reshard_batch_destroy(batch: Batch):

@@ -375,18 +375,22 @@ reshard_status_t gather_broadcast_execute_static(reshard_plan_t plan, const void
 
 /*
  * Whole-model batching: the fan-out reshards of several plans (e.g. every
- * feed-forward weight of a model) as ONE kernel launch.  The plans' copy
- * descriptors are concatenated over a combined buffer table, so the work is
- * spread evenly over the GPU with no launch boundary between tensors.  The
+ * feed-forward weight of a model) with the plans that take the TMA fan-out as
+ * ONE kernel launch: their copy descriptors are concatenated over a combined
+ * buffer table, and the kernel's work queue spreads the work evenly over the
+ * GPU with no launch boundary between tensors.  Every other plan runs on its
+ * own, as reshard_execute runs it (see reshard_batch_classes).  The
  * pages route the feed-forward projections (most of the parameters) through
  * the Reshard collective and the small irregular weights through
  * gather-and-broadcast (news.bpdata.com, section "Integracio es hibrid megoldas
  * a NeMo RL-ben"); a batch is the unit for the first group.
  *
  * reshard_batch_create: plans[nplans] stay owned by the caller and must outlive
- * the batch (executions check them).  The sum over plans of M + N must be below
- * RESHARD_MAX_EXEC_BUFFERS (else UNSUPPORTED: split the model into several
- * batches).  Errors: INVALID_ARG, BAD_HANDLE, UNSUPPORTED, NO_MEMORY.
+ * the batch (executions check them).  TMA fan-out plans that together have
+ * more ranks (M + N each) than one launch can address (RESHARD_MAX_EXEC_BUFFERS)
+ * go to several launches; a plan that alone has more (which no reshard_execute
+ * could run either) makes the call fail with UNSUPPORTED.
+ * Errors: INVALID_ARG, BAD_HANDLE, UNSUPPORTED, NO_MEMORY.
  */
 reshard_status_t reshard_batch_create(const reshard_plan_t* plans, int32_t nplans,
                                       reshard_batch_t* out_batch);
@@ -394,13 +398,23 @@ reshard_status_t reshard_batch_create(const reshard_plan_t* plans, int32_t nplan
 /*
  * Execute every plan of the batch: src_ptrs[i] and dst_ptrs[i] are plan i's
  * pointer arrays, exactly as for reshard_execute (in-place plans included).
- * When every copy can use 16-byte accesses with these buffers the batch is one
- * launch of the fan-out kernel (its descriptor tables are uploaded on first use,
- * like a plan's); otherwise each plan is executed in turn with its own kernel.
- * Errors: as reshard_execute.
+ * The merged TMA fan-out plans are one launch (its descriptor tables are
+ * uploaded on first use, like a plan's) when all their buffers are 16-byte
+ * aligned (torch allocations are); otherwise they too run one by one, each
+ * with its own kernel.  All pointer arrays are checked before anything is
+ * launched.  Errors: as reshard_execute.
  */
 reshard_status_t reshard_batch_execute(reshard_batch_t batch, const void* const* const* src_ptrs,
                                        void* const* const* dst_ptrs, void* stream);
+
+/*
+ * The launch classes of a batch, in the order they run on the stream: one
+ * for the merged TMA fan-out plans (more if their ranks overflow a launch's
+ * buffer table), one for each other plan.  *nclasses (may be NULL) receives
+ * their number, plan_class[nplans] (may be NULL) the class of each plan, -1
+ * for a plan with nothing to copy.  Errors: BAD_HANDLE.
+ */
+reshard_status_t reshard_batch_classes(reshard_batch_t batch, int32_t* nclasses, int32_t* plan_class);
 
 /* Release a batch (not its plans).  Errors: BAD_HANDLE. */
 reshard_status_t reshard_batch_destroy(reshard_batch_t batch);

@@ -162,12 +162,32 @@ def test_batch_host_checks():
     with pytest.raises(rs.ReshardError) as e:
         rs.reshard_batch_create([b])
     assert e.value.status == 6
-    # too many ranks for one launch
-    big = [rs.reshard_plan_create((4096,), "fp32", (256,), ("S0",), (256,), ("S0",))
-           for _ in range(2)]
+    # a plan with more ranks than one launch can address
+    big = rs.reshard_plan_create((8192,), "fp32", (512,), ("S0",), (512,), ("S0",))
     with pytest.raises(rs.ReshardError) as e:
-        rs.reshard_batch_create(big)
+        rs.reshard_batch_create([big])
     assert e.value.status == 2
+    # plans that only together exceed one launch's buffer table go to two launches
+    wide = [rs.reshard_plan_create((4800,), "fp32", (300,), ("S0",), (300,), ("S0",))
+            for _ in range(2)]
+    assert rs.reshard_batch_classes(rs.reshard_batch_create(wide)) == (2, [0, 1])
+
+
+def test_batch_classes():
+    """Plans go into launch classes by the kernel they take with aligned buffers."""
+    aligned = rs.reshard_plan_create((64, 64), "fp32", (2,), ("S0",), (4,), ("S0",))
+    aligned2 = rs.reshard_plan_create((128, 32), "bf16", (4,), ("S1",), (2,), ("S1",))
+    odd = rs.reshard_plan_create((7, 9), "bf16", (2,), ("S0",), (3,), ("S1",))
+    odd2 = rs.reshard_plan_create((5, 11), "bf16", (3,), ("S1",), (2,), ("S0",))
+    empty = rs.reshard_plan_create((0, 8), "fp32", (2,), ("S0",), (2,), ("S0",))
+    batch = rs.reshard_batch_create([aligned, odd, empty, aligned2, odd2])
+    n, per = rs.reshard_batch_classes(batch)
+    assert per[2] == -1                      # nothing to copy
+    assert per[0] == per[3] == 0             # 16-byte runs: one TMA fan-out launch
+    assert per[1] != per[0] and per[4] != per[0]
+    assert n == len({c for c in per if c >= 0})
+    # the same plans in one class each when batched alone
+    assert rs.reshard_batch_classes(rs.reshard_batch_create([odd])) == (1, [0])
 
 
 def _fake_ptrs(plan, side, n, mis):
@@ -262,9 +282,13 @@ def test_refit_routes_and_host_checks():
 
 
 def test_refit_batch_limit_is_reported():
-    big = [rs.reshard_plan_create((4096,), "fp32", (256,), ("S0",), (256,), ("S0",))
-           for _ in range(2)]
+    # plans that only together exceed one launch's buffer table: the batch splits them
+    wide = [rs.reshard_plan_create((4096,), "fp32", (256,), ("S0",), (256,), ("S0",))
+            for _ in range(2)]
+    rs.reshard_refit_create(wide, batch=True)
+    # a plan that alone exceeds it cannot be batched (nor executed)
+    big = [rs.reshard_plan_create((8192,), "fp32", (512,), ("S0",), (512,), ("S0",))]
     with pytest.raises(rs.ReshardError) as e:
         rs.reshard_refit_create(big, batch=True)
     assert e.value.status == 2
-    rs.reshard_refit_create(big, batch=False)           # one launch per plan instead
+    rs.reshard_refit_create(big, batch=False)

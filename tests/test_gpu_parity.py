@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import dtensor_reshard_gb300 as rs
-from inputs import TensorSpec, global_tensor, workload
+from inputs import TensorSpec, global_tensor, uneven_stress, workload
 from tests import helpers
 
 pytestmark = pytest.mark.gpu
@@ -415,6 +415,27 @@ def test_batch_of_plans(oracle, misalign):
         t for t in workload(5, reduced=True).tensors if t.path == "reshard")
     plans, sptrs, dptrs, want, keep = _batch_case(oracle, specs, misalign)
     batch = rs.reshard_batch_create(plans)
+    for _ in range(2):
+        rs.reshard_batch_execute(batch, sptrs, dptrs)
+    torch.cuda.synchronize()
+    for (ds, dd), w in zip(keep, want):
+        for g, x in zip(dd, w):
+            assert np.array_equal(g.payload().cpu().numpy(), x)
+            assert g.guards_intact()
+    assert rs.reshard_device_status() == 0
+
+
+@pytest.mark.parametrize("misalign", [0, 2, 3])
+def test_batch_of_mixed_classes(oracle, misalign):
+    """Uneven tensors of every copy path batched together: one launch per class of plans
+    that take the same kernel, classes whose buffers are less aligned than assumed run plan
+    by plan; every destination byte and guard band matches the oracle."""
+    specs = list(uneven_stress(n=24, seed=4242, max_dim=2000, max_numel=1 << 19,
+                               max_bytes=64 << 20, name="mix").tensors)
+    plans, sptrs, dptrs, want, keep = _batch_case(oracle, specs, misalign)
+    batch = rs.reshard_batch_create(plans)
+    n, per = rs.reshard_batch_classes(batch)
+    assert n >= 3 and n == len({c for c in per if c >= 0})
     for _ in range(2):
         rs.reshard_batch_execute(batch, sptrs, dptrs)
     torch.cuda.synchronize()
