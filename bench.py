@@ -56,8 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--tensors", default=None,
                     help="comma-separated tensor names to keep from the workload (profiling)")
     ap.add_argument("--kernel", choices=("fanout", "boxcopy"), default="fanout")
-    ap.add_argument("--batch", action="store_true",
-                    help="launch all reshard tensors as one batch (measured: no gain on GB300)")
+    ap.add_argument("--no-batch", action="store_true",
+                    help="launch the reshard tensors one by one instead of as one batch "
+                         "(the default when they all take the TMA fan-out)")
     ap.add_argument("--reshard-only", action="store_true",
                     help="leave out the gather-and-broadcast tensors (profiling captures)")
     ap.add_argument("--experts", type=int, default=256,
@@ -519,8 +520,16 @@ def ours_arm(args, rank, world, local):
 
     dom_jobs = [j for j in jobs if j.spec.path == "reshard"]
     batch = None
-    if args.batch and kernel == rs.KERNEL_FANOUT and len(dom_jobs) > 1:
+    batch_one_launch = False
+    if not args.no_batch and kernel == rs.KERNEL_FANOUT and len(dom_jobs) > 1:
+        # one batch when it makes one launch of all of them (every plan on the TMA
+        # fan-out); otherwise a batch would run most plans one by one anyway, after
+        # checking all their pointers first, so the step launches them in turn
         batch = rs.reshard_batch_create([j.plan for j in dom_jobs])
+        nclasses, per = rs.reshard_batch_classes(batch)
+        batch_one_launch = nclasses == 1 and all(c == 0 for c in per)
+        if not batch_one_launch:
+            batch = None
     ops = make_step(jobs, kernel, batch)
     ms_step, dom_ms, clocks = device_time(ops, stream, args.steps, args.warmup, dctx, gpu_uuid)
     ms_step_max = dctx.max(ms_step)
@@ -539,7 +548,9 @@ def ours_arm(args, rank, world, local):
     traffic = load_profile_traffic()
     traffic_val = None
     if traffic and traffic.get("workload") == w.name:
-        traffic_val = traffic.get("dram_bytes_per_launch")
+        # profiled per launch in both forms: the batch of the expert tensors, one tensor
+        traffic_val = traffic.get("batch_launch" if batch is not None else "tensor_launch",
+                                  {}).get("dram_bytes")
 
     # gather-and-broadcast comparison on the same tensors (reshard tensors only)
     gb_ms = None
@@ -558,9 +569,19 @@ def ours_arm(args, rank, world, local):
             cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                    "sample": desc, "seconds": round(secs, 2)}
 
+    if batch is not None:
+        # one launch per class of the batch (a class of one plan: that plan's launches)
+        _, per = rs.reshard_batch_classes(batch)
+        members = {}
+        for j, c in zip(dom_jobs, per):
+            if c >= 0:
+                members.setdefault(c, []).append(j)
+        dom_launches = sum(1 if len(m) > 1 else launches_of(m[0], kernel)
+                           for m in members.values())
+    else:
+        dom_launches = sum(launches_of(j, kernel) for j in dom_jobs)
     launches = args.steps * (sum(launches_of(j, kernel) for j in jobs if j.spec.path != "reshard")
-                             + (1 if batch is not None else
-                                sum(launches_of(j, kernel) for j in dom_jobs)))
+                             + dom_launches)
     st_tot = {k: sum(j.stats[k] for j in jobs) for k in (
         "global_bytes", "dst_bytes", "src_bytes", "fanout_read_bytes", "fanout_write_bytes",
         "boxcopy_read_bytes", "boxcopy_write_bytes", "gb_read_bytes", "gb_write_bytes")}
