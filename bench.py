@@ -341,6 +341,9 @@ def device_time(ops, stream, steps, warmup, dist_ctx, gpu_uuid):
     sampler.start()
     dist_ctx.barrier()
     torch.cuda.synchronize()
+    # busy the stream for ~0.1 ms so that the first timed launch is already queued when
+    # the start event completes (the interval holds device time, not host submission)
+    torch.cuda._sleep(200_000)
     start.record(stream)
     e = 0
     for _ in range(steps):
@@ -723,6 +726,9 @@ def report(args):
         for i in range(reps + 3):
             if flush:
                 l2_flush.fill_(i & 0xFF)
+            # keep the stream busy (~0.1 ms) while the host enqueues the start event and the
+            # launches, so the interval holds device time only, not the host's submission
+            torch.cuda._sleep(200_000)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
