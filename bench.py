@@ -42,6 +42,11 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # ------------------------------------------------------------------------------ setup
+def elem_types(w) -> str:
+    """The tensors' element types: the path copies their bits (its dtype is u8)."""
+    return ",".join(sorted({t.dtype for t in w.tensors}))
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,9 +492,9 @@ def reference_arm(args, rank, world):
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic",
-        "config": {"workload": w.name, "sample": desc},
+        "config": {"workload": w.name, "elements": elem_types(w), "sample": desc},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -594,10 +599,10 @@ def ours_arm(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic",
         "config": {
-            "workload": w.name, "tensors": len(jobs),
+            "workload": w.name, "tensors": len(jobs), "elements": elem_types(w),
             "reshard_kernel": args.kernel,
             "reshard_launch": "one batch launch for all reshard tensors" if batch is not None
                               else "one launch per tensor",
@@ -787,7 +792,7 @@ def report(args):
         b1 = sum(j.stats["boxcopy_read_bytes"] + j.stats["boxcopy_write_bytes"] for j in jobs)
         bg = sum(j.stats["gb_read_bytes"] + j.stats["gb_write_bytes"] for j in jobs)
         row = {
-            "workload": w.name, "tensors": len(jobs), "G": G, "D": D,
+            "workload": w.name, "tensors": len(jobs), "elements": elem_types(w), "G": G, "D": D,
             "l2_flush": flush,
             "fanout_ms": round(t2, 4), "boxcopy_ms": round(t1, 4),
             "fanout_batched_ms": round(t2b, 4) if t2b else None,
