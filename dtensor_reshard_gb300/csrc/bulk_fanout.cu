@@ -25,10 +25,12 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <cstdint>
+#include <map>
 #include <mutex>
 #include <string>
+#include <thread>
+#include <utility>
 
 #include "internal.h"
 #include "staging.cuh"
@@ -48,7 +50,11 @@ __device__ unsigned int g_device_status;
 // they ask, so CTAs that run fast take more pieces and all finish
 // together.  Every launch takes its own slot {next piece, CTAs finished}; the
 // last CTA of the launch puts the slot back to zero.
-constexpr int kQueueSlots = 1024;
+// Slots [0, kStreamSlots) belong to streams, one each; the rest go to launches
+// captured into CUDA graphs, one each, never handed out again (a graph may be
+// replayed on any stream, beside the eager launches of the stream it came from).
+constexpr int kQueueSlots = 4096;
+constexpr int kStreamSlots = 1024;
 __device__ unsigned int g_queue[kQueueSlots][2];
 // Units per piece: about kPieceBytes of the program's bytes, and few enough
 // that every CTA can get about kPiecesPerCta pieces (small programs still use
@@ -203,9 +209,17 @@ struct DeviceState {
   unsigned int* queue = nullptr;   // device address of g_queue
   int blocks_per_sm = 0;
 };
-std::atomic<uint32_t> g_queue_slot{0};
 std::mutex g_dev_mu;
+// per device: the slot of each stream (keyed by handle; the per-thread default
+// stream also by thread) and the next free slot of each kind
+struct SlotTable {
+  std::map<std::pair<uintptr_t, std::thread::id>, uint32_t> by_stream;
+  uint32_t next_stream = 0;
+  uint32_t next_captured = kStreamSlots;
+};
+std::mutex g_slot_mu;
 DeviceState g_dev[kMaxDevices];
+SlotTable g_slots[kMaxDevices];
 
 reshard_status_t device_state(DeviceState* out) {
   int dev = -1;
@@ -245,12 +259,43 @@ reshard_status_t device_state(DeviceState* out) {
 
 }  // namespace
 
-reshard_status_t work_queue_slot(unsigned int** slot) {
+reshard_status_t work_queue_slot(void* stream, unsigned int** slot) {
   DeviceState d;
   reshard_status_t st = device_state(&d);
   if (st != RESHARD_OK) return st;
-  // a slot of its own (launches in flight at once never come near kQueueSlots)
-  *slot = d.queue + 2 * (g_queue_slot.fetch_add(1) % uint32_t(kQueueSlots));
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess)
+    return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  ce = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs);
+  if (ce != cudaSuccess)
+    return fail(RESHARD_ERR_CUDA, std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(ce));
+  std::lock_guard<std::mutex> lk(g_slot_mu);
+  SlotTable& t = g_slots[dev];
+  uint32_t idx = 0;
+  if (cs != cudaStreamCaptureStatusNone) {
+    if (t.next_captured >= uint32_t(kQueueSlots))
+      return fail(RESHARD_ERR_UNSUPPORTED, "more than " + std::to_string(kQueueSlots - kStreamSlots) +
+                                               " work-queue launches captured into CUDA graphs "
+                                               "on this device");
+    idx = t.next_captured++;
+  } else {
+    const uintptr_t h = reinterpret_cast<uintptr_t>(stream);
+    const std::thread::id who = stream == static_cast<void*>(cudaStreamPerThread)
+                                    ? std::this_thread::get_id()
+                                    : std::thread::id();
+    auto it = t.by_stream.find({h, who});
+    if (it == t.by_stream.end()) {
+      if (t.next_stream >= uint32_t(kStreamSlots))
+        return fail(RESHARD_ERR_UNSUPPORTED, "work-queue launches on more than " +
+                                                 std::to_string(kStreamSlots) +
+                                                 " streams of this device");
+      it = t.by_stream.emplace(std::make_pair(h, who), t.next_stream++).first;
+    }
+    idx = it->second;
+  }
+  *slot = d.queue + 2 * idx;
   return RESHARD_OK;
 }
 
@@ -294,7 +339,7 @@ reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelPa
   KernelParams params = kp;
   unsigned int* status = d.status;
   unsigned int* queue = nullptr;
-  st = work_queue_slot(&queue);
+  st = work_queue_slot(stream, &queue);
   if (st != RESHARD_OK) return st;
   PieceSchedule sched = work_queue_schedule(kp.total_units, prog.tile_bytes, prog.write_bytes,
                                             grid, 0);

@@ -205,8 +205,11 @@ reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelPa
 reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, const Program& prog,
                                        void* stream);
 // A work-queue slot {next piece, CTAs finished} of the current device for one
-// launch; the launch's last CTA puts it back to zero (bulk_fanout.cu).
-reshard_status_t work_queue_slot(unsigned int** slot);
+// launch on `stream`; the launch's last CTA puts it back to zero.  Launches on one
+// stream run in turn and share the stream's slot; a launch being captured into a
+// CUDA graph gets a slot of its own for good (bulk_fanout.cu).  UNSUPPORTED when
+// a device's slots for streams or for captured launches run out.
+reshard_status_t work_queue_slot(void* stream, unsigned int** slot);
 // The pieces a work queue hands out, in order: pieces of `big` units up to unit
 // `split` (a multiple of big), then pieces of `small` units up to `total`, so
 // that the last pieces taken are short and the CTAs of a launch finish close

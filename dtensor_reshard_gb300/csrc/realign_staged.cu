@@ -437,7 +437,7 @@ reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, cons
   const unsigned grid = unsigned(kp.total_units < max_grid ? kp.total_units : max_grid);
   KernelParams params = kp;
   unsigned int* queue = nullptr;
-  st = work_queue_slot(&queue);
+  st = work_queue_slot(stream, &queue);
   if (st != RESHARD_OK) return st;
   // pieces of at least 16 KiB: tiny ones cost more in grabs and short chunks
   // than they gain in balance (measured on the small uneven-stress tensors)

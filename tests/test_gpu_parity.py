@@ -526,6 +526,70 @@ def test_cuda_graph_capture_and_replay(oracle):
     assert rs.reshard_device_status() == 0
 
 
+def test_streams_and_graph_replay_beside_eager_launches(oracle):
+    """Work-queue kernels on four streams at once, then a captured reshard replayed on one
+    stream while the stream it was captured on keeps launching (more launches than a round
+    of the device's work-queue slots): every destination byte is exact."""
+    dev = _cuda()
+    specs = [
+        _spec((256, 64, 96), "fp32", (2, 2), ("S0", "S2"), (4,), ("S1",), seed=10),  # TMA fan-out
+        _spec((2000, 1001), "bf16", (3,), ("S0",), (2,), ("S1",), seed=11),          # staged
+        _spec((1500, 777), "fp16", (2,), ("S1",), (3,), ("S0",), seed=12),           # staged
+        _spec((1000, 257), "fp16", (5,), ("S0",), (4,), ("R",), seed=13)]            # TMA fan-out
+    for spec in specs:
+        p = helpers.spec_plan(spec)
+        assert rs.reshard_plan_path(p, [1 << 20] * p.n_src, [1 << 24] * p.n_dst)[0] in (
+            "tma_fanout", "staged", "staged_bulk"), spec
+    cases = []
+    for spec in specs:
+        glob = global_tensor(TensorSpec(spec.name, spec.global_shape, spec.dtype, spec.src_mesh,
+                                        spec.src_placements, spec.dst_mesh, spec.dst_placements,
+                                        init=("bits",), seed=spec.seed))
+        boxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+        host = [helpers.slice_box(glob, o, sh) for o, sh in boxes]
+        want = helpers.expected_dst(oracle, spec, [helpers.to_bytes(h) for h in host])
+        srcs = [h.to(dev) for h in host]
+        dboxes = oracle.boxes(spec.global_shape, spec.dst_mesh, spec.dst_placements)
+        dsts = [torch.empty(sh, dtype=host[0].dtype, device=dev) for _, sh in dboxes]
+        plan = helpers.spec_plan(spec)
+        rs.reshard_plan_upload(plan)
+        cases.append((spec, plan, srcs, dsts, want))
+
+    def clear():
+        for _, _, _, dsts, _ in cases:
+            for d in dsts:
+                d.view(-1).view(torch.uint8).fill_(FILL_BYTE)
+        torch.cuda.synchronize()
+
+    def check(which):
+        torch.cuda.synchronize()
+        for i in which:
+            spec, _, _, dsts, want = cases[i]
+            for d, w in zip(dsts, want):
+                assert np.array_equal(helpers.to_bytes(d), w), spec.name
+        assert rs.reshard_device_status() == 0
+
+    clear()
+    streams = [torch.cuda.Stream() for _ in cases]
+    for _ in range(20):
+        for (spec, plan, srcs, dsts, _), st in zip(cases, streams):
+            rs.reshard_execute(plan, srcs, dsts, st)
+    check(range(len(cases)))
+
+    clear()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        rs.reshard_execute(cases[0][1], cases[0][2], cases[0][3], torch.cuda.current_stream())
+    eager, replay = torch.cuda.Stream(), torch.cuda.Stream()
+    _, plan1, srcs1, dsts1, _ = cases[3]
+    for k in range(1100):
+        rs.reshard_execute(plan1, srcs1, dsts1, eager)
+        if k % 50 == 0:
+            with torch.cuda.stream(replay):
+                graph.replay()
+    check([0, 3])
+
+
 # ---------------------------------------------------------------------- transpose blocks
 TRANSPOSE_CASES = [
     _spec((74, 65, 1721), "fp16", (61,), ("S2",), (3,), ("R",), seed=1),        # gather, R=3
