@@ -280,7 +280,9 @@ reshard_status_t reshard_plan_upload(reshard_plan_t plan);
  * execution has run on the device, executions can be recorded into a CUDA graph
  * by stream capture and replayed; the graph keeps the buffer addresses.
  * Errors: BAD_HANDLE, INVALID_ARG (null pointer for a non-empty shard),
- * UNSUPPORTED (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS), CUDA (launch failed).
+ * UNSUPPORTED (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS, or the device's work-queue
+ * slots are used up: one per stream for 1024 streams, one per launch captured
+ * into a CUDA graph for 3072 captured launches), CUDA (launch failed).
  */
 reshard_status_t reshard_execute(reshard_plan_t plan, const void* const* src_ptrs,
                                  void* const* dst_ptrs, void* stream);
