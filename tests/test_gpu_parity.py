@@ -292,6 +292,49 @@ def test_full_moe_refit(oracle, idx):
         _full_size_check(oracle, spec)
 
 
+def test_full_moe_refit_as_one_batch_launch(oracle):
+    """The bench's launch form at full size: the three expert tensors of the MoE refit as one
+    batch launch (one launch class); every destination shard equals the global tensor cut by
+    the oracle's box, and the oracle's owning-source rule agrees on sampled elements."""
+    dev = _cuda()
+    specs = [t for t in workload(5).tensors if t.path == "reshard"]
+    assert len(specs) == 3
+    cases = []
+    for spec in specs:
+        glob = global_tensor(spec, device=dev)
+        src_boxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+        dst_boxes = oracle.boxes(spec.global_shape, spec.dst_mesh, spec.dst_placements)
+        srcs = [helpers.slice_box(glob, o, sh).contiguous() for o, sh in src_boxes]
+        del glob
+        dsts = [torch.empty(sh, dtype=srcs[0].dtype, device=dev) for _, sh in dst_boxes]
+        for d in dsts:
+            d.view(-1).view(torch.uint8).fill_(FILL_BYTE)
+        cases.append((spec, helpers.spec_plan(spec), src_boxes, dst_boxes, srcs, dsts))
+    batch = rs.reshard_batch_create([c[1] for c in cases])
+    assert rs.reshard_batch_classes(batch) == (1, [0, 0, 0])
+    rs.reshard_batch_execute(batch, [c[4] for c in cases], [c[5] for c in cases])
+    torch.cuda.synchronize()
+    assert rs.reshard_device_status() == 0
+    rng = random.Random(5)
+    for spec, plan, src_boxes, dst_boxes, srcs, dsts in cases:
+        # full comparison: re-assemble the global tensor from the sources, cut each box
+        glob = torch.empty(spec.global_shape, dtype=srcs[0].dtype, device=dev)
+        for (o, sh), x in zip(src_boxes, srcs):
+            glob[tuple(slice(a, a + n) for a, n in zip(o, sh))] = x
+        for r, (o, sh) in enumerate(dst_boxes):
+            assert torch.equal(dsts[r].reshape(-1).view(torch.uint8),
+                               helpers.slice_box(glob, o, sh).reshape(-1).view(torch.uint8)), (
+                spec.name, r)
+        del glob
+        ivt = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}[spec.elem_bytes]
+        for _ in range(500):
+            r = rng.randrange(len(dst_boxes))
+            e = rng.randrange(math.prod(dst_boxes[r][1]))
+            src, j = oracle.source_of(spec.global_shape, spec.src_mesh, spec.src_placements,
+                                      spec.dst_mesh, spec.dst_placements, r, e)
+            assert int(dsts[r].reshape(-1).view(ivt)[e]) == int(srcs[src].reshape(-1).view(ivt)[j])
+
+
 def test_full_uneven_stress_sampled(oracle):
     for spec in workload(4).tensors:
         _full_size_check(oracle, spec, samples=300)
