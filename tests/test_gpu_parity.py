@@ -335,6 +335,19 @@ def test_full_moe_refit_as_one_batch_launch(oracle):
             assert int(dsts[r].reshape(-1).view(ivt)[e]) == int(srcs[src].reshape(-1).view(ivt)[j])
 
 
+@pytest.mark.parametrize("n", [3_000_000_000, 3_000_000_001])
+@pytest.mark.parametrize("kernel", [rs.KERNEL_FANOUT, rs.KERNEL_BOXCOPY])
+def test_offsets_beyond_4gib(oracle, n, kernel):
+    """A 6 GB bf16 vector held whole by one rank, split four ways: the last shards start
+    more than 4 GiB into the source buffer.  The even length keeps every piece 16-byte
+    aligned (TMA path); the odd one leaves 2-byte alignment (realigning path)."""
+    spec = TensorSpec("big", (n,), "bf16", (1,), ("R",), (4,), ("S0",), init=("bits",),
+                      seed=n % 1000)
+    plan = helpers.spec_plan(spec)
+    assert rs.reshard_plan_local_shape(plan, 1, 3)[1][0] * 2 > (1 << 32)
+    _full_size_check(oracle, spec, samples=2000, kernel=kernel)
+
+
 def test_full_uneven_stress_sampled(oracle):
     for spec in workload(4).tensors:
         _full_size_check(oracle, spec, samples=300)
