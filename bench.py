@@ -786,8 +786,22 @@ def report(args):
             for bt, b in batches:
                 rs.reshard_batch_execute(bt, [j.srcs for j in b], [j.dsts for j in b], stream)
 
+        # the same tensors as one refit spread over the side streams
+        lanes = rs.reshard_refit_create([j.plan for j in jobs], lanes=True) if len(jobs) > 1 else None
+
+        if lanes is not None:
+            # pointer tables marshalled once, outside the timed region
+            lsa, lkeep_s = rs._nested([j.srcs for j in jobs])
+            lda, lkeep_d = rs._nested([j.dsts for j in jobs])
+            lstream = rs._stream(stream)
+
+        def k2l():
+            rs._check(rs._lib.reshard_refit_execute(lanes, lsa, lda, None, 0, lstream),
+                      "reshard_refit_execute")
+
         t2, t1, tg = timed(k2, reps, flush), timed(k1, reps, flush), timed(gb, reps, flush)
         t2b = timed(k2b, reps, flush) if batches else None
+        t2l = timed(k2l, reps, flush) if lanes is not None else None
         b2 = sum(j.stats["fanout_read_bytes"] + j.stats["fanout_write_bytes"] for j in jobs)
         b1 = sum(j.stats["boxcopy_read_bytes"] + j.stats["boxcopy_write_bytes"] for j in jobs)
         bg = sum(j.stats["gb_read_bytes"] + j.stats["gb_write_bytes"] for j in jobs)
@@ -797,6 +811,8 @@ def report(args):
             "fanout_ms": round(t2, 4), "boxcopy_ms": round(t1, 4),
             "fanout_batched_ms": round(t2b, 4) if t2b else None,
             "fanout_batched_roofline_frac": round(b2 / t2b / 1e6 / peak, 4) if t2b else None,
+            "fanout_lanes_ms": round(t2l, 4) if t2l else None,
+            "fanout_lanes_roofline_frac": round(b2 / t2l / 1e6 / peak, 4) if t2l else None,
             "gather_broadcast_ms": round(tg, 4),
             "effective_GBps": round((G + D) / t2 / 1e6, 1),
             "fanout_hbm_GBps": round(b2 / t2 / 1e6, 1),
@@ -812,7 +828,7 @@ def report(args):
         }
         rows.append(row)
         print(json.dumps(row), file=sys.stderr)
-        del jobs, scratch, batches
+        del jobs, scratch, batches, lanes
         torch.cuda.empty_cache()
     rows.append(report_inplace(dev, timed, peak))
     print(json.dumps(rows[-1]), file=sys.stderr)

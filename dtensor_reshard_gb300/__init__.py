@@ -381,6 +381,8 @@ def reshard_batch_destroy(batch: Batch):
 
 ROUTE_AUTO, ROUTE_RESHARD, ROUTE_GATHER_BROADCAST = 0, 1, 2
 REFIT_BATCH = 1
+REFIT_LANES = 2
+REFIT_NUM_LANES = 4
 
 
 class Refit:
@@ -413,13 +415,16 @@ def _nested(ptr_lists):
     return out, arrs
 
 
-def reshard_refit_create(plans, routes=None, batch: bool = False) -> Refit:
-    """One refit over plans; routes[i] in ROUTE_* (None: AUTO for every plan)."""
+def reshard_refit_create(plans, routes=None, batch: bool = False, lanes: bool = False) -> Refit:
+    """One refit over plans; routes[i] in ROUTE_* (None: AUTO for every plan).
+    batch: the reshard group as one launch; lanes: the reshard group spread over
+    REFIT_NUM_LANES side streams (the two exclude each other)."""
     arr = (ctypes.c_void_p * len(plans))(*[p.handle for p in plans])
     ra = None if routes is None else (ctypes.c_int32 * len(plans))(*[int(r) for r in routes])
     h = ctypes.c_void_p()
-    _check(_lib.reshard_refit_create(arr, ra, len(plans), REFIT_BATCH if batch else 0,
-                                     ctypes.byref(h)), "reshard_refit_create")
+    flags = (REFIT_BATCH if batch else 0) | (REFIT_LANES if lanes else 0)
+    _check(_lib.reshard_refit_create(arr, ra, len(plans), flags, ctypes.byref(h)),
+           "reshard_refit_create")
     return Refit(h.value, plans)
 
 

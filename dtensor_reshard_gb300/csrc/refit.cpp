@@ -3,11 +3,14 @@
 // of "Integracio es hibrid megoldas a NeMo RL-ben", news.bpdata.com: the
 // feed-forward projections through the Reshard collective, small irregular
 // weights through gather-and-broadcast); the reshard group can go out as one
-// batch launch, and the gather-and-broadcast group shares one scratch buffer,
-// used tensor after tensor in stream order.
+// batch launch, or be spread over a few side streams so that the launches of
+// small tensors overlap, and the gather-and-broadcast group shares one scratch
+// buffer, used tensor after tensor in stream order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
+#include <map>
 #include <mutex>
 #include <new>
 #include <string>
@@ -23,6 +26,14 @@ struct reshard_refit_s {
   std::vector<int32_t> gb_idx;        // plans on gather-and-broadcast, in order
   uint64_t scratch_bytes = 0;         // largest global tensor among gb_idx
   reshard_batch_t batch = nullptr;    // reshard_idx as one batch (RESHARD_REFIT_BATCH)
+  // RESHARD_REFIT_LANES: the reshard group in issue order (largest first) and the
+  // side stream each plan runs on; fork/join events; the device they belong to.
+  std::vector<int32_t> lane_order;
+  std::vector<int32_t> lane_of;
+  int device = -1;
+  cudaEvent_t fork = nullptr;
+  std::array<cudaEvent_t, RESHARD_REFIT_NUM_LANES> join = {};
+  std::mutex issue_mu;  // one execution issues onto the lanes at a time
 };
 
 namespace rs {
@@ -39,6 +50,123 @@ bool refit_live(const reshard_refit_s* r) {
   return refits().count(r) != 0;
 }
 
+// Side streams of each device, created once and shared by every refit on that
+// device (in-order streams: executions that share them run one after another on
+// each lane).  They live until the process exits, so the per-stream work-queue
+// slots of the copy kernels are not used up by refits created and destroyed.
+std::mutex g_lane_mu;
+std::map<int, std::array<cudaStream_t, RESHARD_REFIT_NUM_LANES>> g_lanes;
+
+reshard_status_t device_lanes(int dev, std::array<cudaStream_t, RESHARD_REFIT_NUM_LANES>* out) {
+  std::lock_guard<std::mutex> lk(g_lane_mu);
+  auto it = g_lanes.find(dev);
+  if (it == g_lanes.end()) {
+    std::array<cudaStream_t, RESHARD_REFIT_NUM_LANES> l = {};
+    for (int i = 0; i < RESHARD_REFIT_NUM_LANES; ++i) {
+      cudaError_t ce = cudaStreamCreateWithFlags(&l[size_t(i)], cudaStreamNonBlocking);
+      if (ce != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaStreamDestroy(l[size_t(j)]);
+        return fail(RESHARD_ERR_CUDA, std::string("cudaStreamCreateWithFlags: ") +
+                                          cudaGetErrorString(ce));
+      }
+    }
+    it = g_lanes.emplace(dev, l).first;
+  }
+  *out = it->second;
+  return RESHARD_OK;
+}
+
+void release_events(reshard_refit_s* R) {
+  if (R->fork) cudaEventDestroy(R->fork);
+  for (cudaEvent_t& e : R->join)
+    if (e) cudaEventDestroy(e);
+  R->fork = nullptr;
+  R->join = {};
+}
+
+// Lane assignment (longest processing time first): plans sorted by the bytes the
+// read-once path moves, largest first, each to the lane with the fewest bytes so
+// far (ties: the lower lane), so the lanes finish close together.  Issue order is
+// the sorted order.
+reshard_status_t assign_lanes(reshard_refit_s* R) {
+  std::vector<int32_t> order = R->reshard_idx;
+  auto bytes = [&](int32_t i) {
+    const reshard_stats_t& s = R->plans[size_t(i)]->stats;
+    return s.fanout_read_bytes + s.fanout_write_bytes;
+  };
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t a, int32_t b) { return bytes(a) > bytes(b); });
+  std::array<int64_t, RESHARD_REFIT_NUM_LANES> load = {};
+  R->lane_of.assign(R->plans.size(), -1);
+  for (int32_t i : order) {
+    size_t best = 0;
+    for (size_t l = 1; l < load.size(); ++l)
+      if (load[l] < load[best]) best = l;
+    load[best] += bytes(i);
+    R->lane_of[size_t(i)] = int32_t(best);
+  }
+  R->lane_order = order;
+  cudaError_t ce = cudaGetDevice(&R->device);
+  if (ce != cudaSuccess)
+    return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
+  std::array<cudaStream_t, RESHARD_REFIT_NUM_LANES> lanes;
+  reshard_status_t st = device_lanes(R->device, &lanes);
+  if (st != RESHARD_OK) return st;
+  ce = cudaEventCreateWithFlags(&R->fork, cudaEventDisableTiming);
+  for (cudaEvent_t& e : R->join)
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+  if (ce != cudaSuccess) {
+    release_events(R);
+    return fail(RESHARD_ERR_CUDA, std::string("cudaEventCreateWithFlags: ") +
+                                      cudaGetErrorString(ce));
+  }
+  return RESHARD_OK;
+}
+
+// The reshard group over the side streams: the lanes wait for the caller's stream
+// (fork), each plan runs on its lane, and the caller's stream waits for every lane
+// (join) -- also after an error, so that what was enqueued stays ordered before
+// the caller's later work.
+reshard_status_t execute_lanes(reshard_refit_s* R, const void* const* const* src_ptrs,
+                               void* const* const* dst_ptrs, void* stream) {
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess)
+    return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
+  if (dev != R->device)
+    return fail(RESHARD_ERR_INVALID_ARG, "the refit's side streams belong to device " +
+                                             std::to_string(R->device) + ", current device is " +
+                                             std::to_string(dev));
+  std::array<cudaStream_t, RESHARD_REFIT_NUM_LANES> lanes;
+  reshard_status_t st = device_lanes(dev, &lanes);
+  if (st != RESHARD_OK) return st;
+  std::lock_guard<std::mutex> lk(R->issue_mu);
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  ce = cudaEventRecord(R->fork, caller);
+  if (ce != cudaSuccess)
+    return fail(RESHARD_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(ce));
+  for (cudaStream_t l : lanes) {
+    ce = cudaStreamWaitEvent(l, R->fork, 0);
+    if (ce != cudaSuccess)
+      return fail(RESHARD_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(ce));
+  }
+  for (int32_t i : R->lane_order) {
+    st = reshard_execute(R->plans[size_t(i)], src_ptrs[i], dst_ptrs[i],
+                         lanes[size_t(R->lane_of[size_t(i)])]);
+    if (st != RESHARD_OK) break;
+  }
+  std::string msg;  // keep the first error's message over the join's
+  if (st != RESHARD_OK) msg = reshard_last_error();
+  for (size_t l = 0; l < lanes.size(); ++l) {
+    ce = cudaEventRecord(R->join[l], lanes[l]);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(caller, R->join[l], 0);
+    if (ce != cudaSuccess && st == RESHARD_OK)
+      return fail(RESHARD_ERR_CUDA, std::string("lane join: ") + cudaGetErrorString(ce));
+  }
+  if (st != RESHARD_OK) return fail(st, msg);
+  return RESHARD_OK;
+}
+
 }  // namespace
 }  // namespace rs
 
@@ -51,8 +179,11 @@ reshard_status_t reshard_refit_create(const reshard_plan_t* plans, const int32_t
   if (!out_refit) return fail(RESHARD_ERR_INVALID_ARG, "out_refit is NULL");
   *out_refit = nullptr;
   if (!plans || nplans < 1) return fail(RESHARD_ERR_INVALID_ARG, "no plans");
-  if ((flags & ~uint32_t(RESHARD_REFIT_BATCH)) != 0)
+  if ((flags & ~uint32_t(RESHARD_REFIT_BATCH | RESHARD_REFIT_LANES)) != 0)
     return fail(RESHARD_ERR_INVALID_ARG, "unknown refit flags");
+  if ((flags & RESHARD_REFIT_BATCH) && (flags & RESHARD_REFIT_LANES))
+    return fail(RESHARD_ERR_INVALID_ARG,
+                "RESHARD_REFIT_BATCH and RESHARD_REFIT_LANES exclude each other");
   reshard_refit_s* R = new (std::nothrow) reshard_refit_s();
   if (!R) return fail(RESHARD_ERR_NO_MEMORY, "host allocation failed");
   try {
@@ -88,8 +219,17 @@ reshard_status_t reshard_refit_create(const reshard_plan_t* plans, const int32_t
         return st;
       }
     }
+    if ((flags & RESHARD_REFIT_LANES) && !R->reshard_idx.empty()) {
+      reshard_status_t st = rs::assign_lanes(R);
+      if (st != RESHARD_OK) {
+        rs::release_events(R);
+        delete R;
+        return st;
+      }
+    }
   } catch (const std::bad_alloc&) {
     if (R->batch) reshard_batch_destroy(R->batch);
+    rs::release_events(R);
     delete R;
     return fail(RESHARD_ERR_NO_MEMORY, "host allocation failed while routing");
   }
@@ -132,6 +272,9 @@ reshard_status_t reshard_refit_execute(reshard_refit_t refit, const void* const*
     }
     st = reshard_batch_execute(refit->batch, s.data(), d.data(), stream);
     if (st != RESHARD_OK) return st;
+  } else if (refit->fork) {
+    st = rs::execute_lanes(refit, src_ptrs, dst_ptrs, stream);
+    if (st != RESHARD_OK) return st;
   } else {
     for (int32_t i : refit->reshard_idx) {
       st = reshard_execute(refit->plans[size_t(i)], src_ptrs[i], dst_ptrs[i], stream);
@@ -153,6 +296,7 @@ reshard_status_t reshard_refit_destroy(reshard_refit_t refit) {
       return fail(RESHARD_ERR_BAD_HANDLE, "refit is NULL or already destroyed");
   }
   if (refit->batch) reshard_batch_destroy(refit->batch);
+  rs::release_events(refit);
   delete refit;
   return RESHARD_OK;
 }

@@ -445,10 +445,27 @@ typedef enum reshard_route {
 
 /* reshard_refit_create flag: batch the reshard group into one launch. */
 #define RESHARD_REFIT_BATCH 1u
+/* reshard_refit_create flag (excludes RESHARD_REFIT_BATCH): spread the reshard
+ * group over RESHARD_REFIT_NUM_LANES side streams of the current device, so that
+ * the launches of independent tensors overlap (a launch of a small tensor fills
+ * few SMs for a few microseconds, and each launch drains its last CTAs alone).
+ * Plans go to the lanes largest first, each to the lane with the fewest bytes so
+ * far.  reshard_refit_execute makes the lanes wait for the caller's stream,
+ * launches every plan on its lane and makes the caller's stream wait for every
+ * lane before the gather-and-broadcast group, so the call is ordered on the
+ * caller's stream like the one-stream form and can be captured into a CUDA graph
+ * from it.  The side streams are created at the first such refit of a device,
+ * shared by all refits of that device and kept until the process exits;
+ * executions of such refits are issued one at a time (a lock per refit), and the
+ * refit must be executed with the device current that it was created on
+ * (INVALID_ARG otherwise). */
+#define RESHARD_REFIT_LANES 2u
+#define RESHARD_REFIT_NUM_LANES 4
 
-/* Errors: INVALID_ARG (no plans, unknown route or flag), BAD_HANDLE (a plan is
- * not live), UNSUPPORTED (RESHARD_REFIT_BATCH and the reshard group exceeds one
- * batch's buffer table), NO_MEMORY. */
+/* Errors: INVALID_ARG (no plans, unknown route or flag, both BATCH and LANES),
+ * BAD_HANDLE (a plan is not live), UNSUPPORTED (RESHARD_REFIT_BATCH and the
+ * reshard group exceeds one batch's buffer table), CUDA (LANES: creating the
+ * side streams or events failed), NO_MEMORY. */
 reshard_status_t reshard_refit_create(const reshard_plan_t* plans, const int32_t* routes,
                                       int32_t nplans, uint32_t flags, reshard_refit_t* out_refit);
 

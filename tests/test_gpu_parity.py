@@ -745,12 +745,13 @@ def test_excluded_ranks_get_null_buffers(oracle, kernel, misalign):
 
 
 # ---------------------------------------------------------------------- whole-model refit
-@pytest.mark.parametrize("batch", [False, True])
+@pytest.mark.parametrize("mode", ["one_stream", "batch", "lanes"])
 @pytest.mark.parametrize("misalign", [0, 2])
-def test_refit_hybrid_routes(oracle, batch, misalign):
+def test_refit_hybrid_routes(oracle, mode, misalign):
     """The reduced MoE model in one reshard_refit_execute: expert weights on the reshard
-    route, attention and norm weights on gather-and-broadcast (the configuration's split),
-    one shared scratch; every byte checked."""
+    route (one launch per plan, one batch launch, or spread over side streams), attention
+    and norm weights on gather-and-broadcast (the configuration's split), one shared
+    scratch; every byte checked."""
     _cuda()
     w = workload(5, reduced=True)
     plans, sptrs, dptrs, wants, keep = [], [], [], [], []
@@ -769,7 +770,7 @@ def test_refit_hybrid_routes(oracle, batch, misalign):
     routes = [rs.ROUTE_GATHER_BROADCAST if spec.path == "gather_broadcast" else rs.ROUTE_AUTO
               for spec in w.tensors]
     assert rs.ROUTE_GATHER_BROADCAST in routes and rs.ROUTE_AUTO in routes
-    refit = rs.reshard_refit_create(plans, routes, batch=batch)
+    refit = rs.reshard_refit_create(plans, routes, batch=mode == "batch", lanes=mode == "lanes")
     got_routes, need = rs.reshard_refit_info(refit)
     assert got_routes == [rs.ROUTE_RESHARD if r == rs.ROUTE_AUTO else r for r in routes]
     scratch = Guarded(need, misalign)
@@ -780,6 +781,76 @@ def test_refit_hybrid_routes(oracle, batch, misalign):
             assert np.array_equal(g.payload().cpu().numpy(), x), spec.name
             assert g.guards_intact()
     assert scratch.guards_intact()
+    assert rs.reshard_device_status() == 0
+
+
+def _refit_set(oracle, w, misalign=0):
+    plans, sptrs, dptrs, wants, keep = [], [], [], [], []
+    for spec in w.tensors:
+        glob = global_tensor(spec)
+        srcs = [helpers.to_bytes(x) for x in helpers.scatter_with_oracle(
+            oracle, glob, spec.src_mesh, spec.src_placements)]
+        want = helpers.expected_dst(oracle, spec, srcs)
+        ds = _upload(srcs, misalign)
+        dd = [Guarded(x.size, misalign) for x in want]
+        plans.append(helpers.spec_plan(spec))
+        sptrs.append([g.ptr for g in ds])
+        dptrs.append([g.ptr for g in dd])
+        wants.append(want)
+        keep.append((ds, dd))
+    return plans, sptrs, dptrs, wants, keep
+
+
+def _check_refit_set(w, wants, keep):
+    for spec, want, (ds, dd) in zip(w.tensors, wants, keep):
+        for r, (g, x) in enumerate(zip(dd, want)):
+            assert np.array_equal(g.payload().cpu().numpy(), x), (spec.name, r)
+            assert g.guards_intact()
+
+
+@pytest.mark.parametrize("misalign", [0, 3])
+def test_refit_lanes_uneven_set(oracle, misalign):
+    """The 60 reduced uneven-stress tensors (every copy kernel, many tiny launches) in one
+    refit spread over the side streams, executed twice on a non-default stream; every byte
+    of every destination checked against the oracle after each execution."""
+    _cuda()
+    w = workload(4, reduced=True)
+    plans, sptrs, dptrs, wants, keep = _refit_set(oracle, w, misalign)
+    refit = rs.reshard_refit_create(plans, lanes=True)
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        for ds, dd in keep:
+            for g in dd:
+                g.payload().fill_(FILL_BYTE)
+        torch.cuda.synchronize()
+        rs.reshard_refit_execute(refit, sptrs, dptrs, None, 0, s)
+        s.synchronize()
+        _check_refit_set(w, wants, keep)
+    assert rs.reshard_device_status() == 0
+
+
+def test_refit_lanes_in_cuda_graph(oracle):
+    """A lanes refit captured into a CUDA graph from one stream (the side streams fork from
+    and join back into the capture) and replayed twice; every byte checked after each."""
+    _cuda()
+    w = workload(4, reduced=True)
+    keep_w = type(w)(w.name, w.tensors[:24], w.note)
+    plans, sptrs, dptrs, wants, keep = _refit_set(oracle, keep_w)
+    refit = rs.reshard_refit_create(plans, lanes=True)
+    s = torch.cuda.Stream()
+    rs.reshard_refit_execute(refit, sptrs, dptrs, None, 0, s)  # first use uploads the plans
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        rs.reshard_refit_execute(refit, sptrs, dptrs, None, 0, s)
+    for _ in range(2):
+        for ds, dd in keep:
+            for x in dd:
+                x.payload().fill_(FILL_BYTE)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        _check_refit_set(keep_w, wants, keep)
     assert rs.reshard_device_status() == 0
 
 
