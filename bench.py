@@ -230,10 +230,18 @@ def run_job(job, stream, kernel):
 
 
 def launches_of(job, kernel):
+    """Kernel launches of one execution: the copy program, its transpose blocks and, on the
+    read-once path, the replicate step."""
+    import dtensor_reshard_gb300 as rs
     t = job.stats["n_tiles"]
     if job.spec.path == "gather_broadcast":
         return int(t[2] > 0) + int(t[3] > 0)
-    return int(t[0 if kernel == 0 else 1] > 0)
+    prog = rs.PROGRAM_FANOUT if kernel == rs.KERNEL_FANOUT else rs.PROGRAM_BOXCOPY
+    blocks, _ = rs.reshard_plan_transposes(job.plan, prog)
+    n = int(t[prog] > 0) + int(len(blocks) > 0)
+    if prog == rs.PROGRAM_FANOUT:
+        n += int(job.stats["n_replicate_tiles"] > 0)
+    return n
 
 
 # ------------------------------------------------------------------------------ CPU oracle

@@ -35,7 +35,7 @@ STATUS = {0: "RESHARD_OK", 1: "RESHARD_ERR_INVALID_ARG", 2: "RESHARD_ERR_UNSUPPO
 
 KERNEL_FANOUT = 0
 KERNEL_BOXCOPY = 1
-PROGRAM_FANOUT, PROGRAM_BOXCOPY, PROGRAM_GATHER, PROGRAM_SLICE = 0, 1, 2, 3
+PROGRAM_FANOUT, PROGRAM_BOXCOPY, PROGRAM_GATHER, PROGRAM_SLICE, PROGRAM_REPLICATE = 0, 1, 2, 3, 4
 
 
 class reshard_placement_t(ctypes.Structure):
@@ -56,7 +56,8 @@ class reshard_stats_t(ctypes.Structure):
                 ("boxcopy_read_bytes", ctypes.c_int64), ("boxcopy_write_bytes", ctypes.c_int64),
                 ("gb_read_bytes", ctypes.c_int64), ("gb_write_bytes", ctypes.c_int64),
                 ("max_replica_read_bytes", ctypes.c_int64), ("max_fanout", ctypes.c_int64),
-                ("planner_ns", ctypes.c_int64), ("inplace_bytes", ctypes.c_int64)]
+                ("planner_ns", ctypes.c_int64), ("inplace_bytes", ctypes.c_int64),
+                ("assembled_classes", ctypes.c_int64), ("n_replicate_tiles", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         out = {}

@@ -152,7 +152,7 @@ reshard_status_t reshard_batch_create(const reshard_plan_t* plans, int32_t nplan
         return fail(RESHARD_ERR_UNSUPPORTED, "plan " + std::to_string(i) +
                                                  " has more ranks than one launch can address");
       }
-      if (!rs::mergeable(F)) {
+      if (!rs::mergeable(F) || !p->prog[RESHARD_PROGRAM_REPLICATE].tiles.empty()) {
         B->classes.emplace_back(new rs::BatchClass());
         B->classes.back()->members.push_back(i);
         continue;
@@ -221,7 +221,7 @@ reshard_status_t reshard_batch_execute(reshard_batch_t batch, const void* const*
       const std::vector<unsigned char*>& t = tables[size_t(c.members[0])];
       reshard_status_t st = reshard_plan_upload(p);
       if (st != RESHARD_OK) return st;
-      st = rs::launch_program(p, p->prog[RESHARD_PROGRAM_FANOUT], t.data(), int(t.size()), stream);
+      st = rs::launch_fanout(p, t.data(), int(t.size()), stream);
       if (st != RESHARD_OK) return st;
       continue;
     }

@@ -44,6 +44,15 @@ constexpr int64_t kGatherBlockFanout = 8;
 // Largest destination group one tile fans out to (larger groups are split).
 constexpr int kMaxGroup = 256;
 
+// Programs a plan holds: the four of reshard_program_t and the replicate step.
+constexpr int kNumPrograms = 5;
+// A destination class with at least this many replicas whose copies would go
+// through the register realigning kernel (tiles off the 16-byte grid, mostly in
+// rows of 512 bytes to 8 KiB) is assembled in one replica and then copied to the
+// others as one aligned run (RESHARD_PROGRAM_REPLICATE).  Measured on GB300, a
+// 138 MB fp32 gather of 56 pieces of 628 bytes into 15 replicas: 0.553 -> 0.386 ms.
+constexpr int64_t kAssembleFanout = 8;
+
 // Fixed work of one row (offsets, partial first and last words, a row-table
 // entry), counted in bytes of streaming when rows are grouped into units.
 constexpr int64_t kRowCostBytes = 256;
@@ -152,7 +161,7 @@ struct reshard_plan_s {
   int64_t gshape[RESHARD_MAX_TENSOR_NDIM] = {};
   int32_t elem_bytes = 0;
   rs::Layout src, dst;
-  rs::Program prog[4];
+  rs::Program prog[rs::kNumPrograms];
   reshard_stats_t stats = {};
   // in-place plans: source rank s lives inside destination rank alias_dst[s]
   // (-1: separate buffer) at byte offset alias_off[s]
@@ -185,6 +194,10 @@ reshard_status_t fail(reshard_status_t st, const std::string& msg);
 // bufs[nbufs] on `stream`.  Returns OK when there is nothing to do.
 reshard_status_t launch_program(const reshard_plan_s* plan, const Program& p,
                                 unsigned char* const* bufs, int nbufs, void* stream);
+// The read-once path of a plan: its FANOUT program, then (same stream) its
+// REPLICATE program when some destination classes are assembled in one replica.
+reshard_status_t launch_fanout(const reshard_plan_s* plan, unsigned char* const* bufs, int nbufs,
+                               void* stream);
 // Same, with the program's tables at explicit device addresses (no uploaded plan).
 reshard_status_t launch_program_tables(const Program& p, const reshard_tile_t* d_tiles,
                                        const int64_t* d_prefix, const uint32_t* d_goff,

@@ -590,6 +590,13 @@ reshard_status_t launch_program(const reshard_plan_s* plan, const Program& prog,
   return launch_transposes(plan, prog, bufs, nbufs, flags, stream);
 }
 
+reshard_status_t launch_fanout(const reshard_plan_s* plan, unsigned char* const* bufs, int nbufs,
+                               void* stream) {
+  reshard_status_t st = launch_program(plan, plan->prog[RESHARD_PROGRAM_FANOUT], bufs, nbufs, stream);
+  if (st != RESHARD_OK) return st;
+  return launch_program(plan, plan->prog[RESHARD_PROGRAM_REPLICATE], bufs, nbufs, stream);
+}
+
 reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t* d_tiles,
                                        const int64_t* d_prefix, const uint32_t* d_goff,
                                        const uint16_t* d_gbuf, int num_sms,

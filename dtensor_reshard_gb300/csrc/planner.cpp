@@ -338,6 +338,49 @@ RowView row_view(int32_t nd, const int64_t* lo, const int64_t* ext, const Box& s
   return v;
 }
 
+// A region's bytes on one side as planes x rows x width: rows along tensor dim
+// nd - 2, planes over the dims before it, which must collapse into one level.
+// For regions whose rows do not collapse into one level (a 3-D piece of a
+// shard whose middle dim is cut as well).
+struct PlaneView {
+  bool ok = false;
+  int64_t base = 0, pstride = 0, planes = 1, stride = 0, rows = 1, width = 0;
+};
+
+PlaneView plane_view(int32_t nd, const int64_t* lo, const int64_t* ext, const Box& side,
+                     int64_t eb) {
+  PlaneView v;
+  if (nd < 3) return v;
+  int64_t st[RESHARD_MAX_TENSOR_NDIM];
+  row_major_strides(nd, side.shp, st);
+  v.width = ext[nd - 1] * eb;
+  for (int k = 0; k < nd; ++k) v.base += (lo[k] - side.off[k]) * st[k] * eb;
+  v.rows = ext[nd - 2];
+  v.stride = st[nd - 2] * eb;
+  std::vector<Dim> m;
+  for (int k = 0; k + 2 < nd; ++k) {
+    if (ext[k] <= 1) continue;
+    const Dim d = {ext[k], st[k], 0};
+    if (!m.empty() && m.back().ss == d.e * d.ss) m.back() = {m.back().e * d.e, d.ss, 0};
+    else m.push_back(d);
+  }
+  if (m.size() > 1) return v;
+  v.planes = m.empty() ? 1 : m[0].e;
+  v.pstride = m.empty() ? 0 : m[0].ss * eb;
+  v.ok = true;
+  return v;
+}
+
+PlaneView as_planes(const RowView& r) {
+  PlaneView v;
+  v.ok = r.ok;
+  v.base = r.base;
+  v.stride = r.stride;
+  v.rows = r.rows;
+  v.width = r.width;
+  return v;
+}
+
 reshard_status_t build_plan(reshard_plan_s* P) {
   const int32_t nd = P->ndim;
   const int64_t eb = P->elem_bytes;
@@ -429,7 +472,8 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   Program& PB = P->prog[RESHARD_PROGRAM_BOXCOPY];
   Program& PG = P->prog[RESHARD_PROGRAM_GATHER];
   Program& PS = P->prog[RESHARD_PROGRAM_SLICE];
-  for (Program* p : {&PF, &PB, &PG, &PS}) p->goff.push_back(0);
+  Program& PR = P->prog[RESHARD_PROGRAM_REPLICATE];
+  for (Program* p : {&PF, &PB, &PG, &PS, &PR}) p->goff.push_back(0);
   for (size_t di = 0; di < dc.size(); ++di)
     S.max_fanout = std::max<int64_t>(S.max_fanout, int64_t(dc[di].ranks.size()));
   // FANOUT groups, one per distinct list of target ranks (a destination class,
@@ -464,12 +508,14 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   if (!P->inplace && nd >= 2) {
     struct Piece {
       size_t ri;
-      RowView wide, narrow;
+      PlaneView wide, narrow;
       int64_t col;
     };
     // Emits the blocks of one group; `gather` = narrow sources into one destination class.
-    auto emit_group = [&](std::vector<Piece>& ps, bool gather, int64_t rows, int64_t L,
-                          int64_t wide_base, const std::vector<uint16_t>& wide_ids) {
+    // Blocks stay inside one plane of `rows` wide rows (wide planes wide_pstride apart).
+    auto emit_group = [&](std::vector<Piece>& ps, bool gather, int64_t planes, int64_t rows,
+                          int64_t L, int64_t wide_base, int64_t wide_pstride,
+                          const std::vector<uint16_t>& wide_ids) {
       std::sort(ps.begin(), ps.end(), [](const Piece& a, const Piece& b) { return a.col < b.col; });
       // narrow buffer (gather) or destination groups (scatter) of every piece, once
       std::vector<std::vector<uint16_t>> narrow_ids(ps.size());
@@ -479,59 +525,79 @@ reshard_status_t build_plan(reshard_plan_s* P) {
         else narrow_ids[i] = fan_groups(dc[g.d].ranks);
       }
       // rows per block: enough blocks to occupy the GPU, at most one shared-memory image
-      const int64_t nb = std::max<int64_t>(
-          1, std::min<int64_t>(kTransposeBlockBytes / L, (rows + kTransposeMinBlocks - 1) /
-                                                             kTransposeMinBlocks));
+      const int64_t nb = std::min<int64_t>(
+          rows, std::max<int64_t>(1, std::min<int64_t>(kTransposeBlockBytes / L,
+                                                       (planes * rows + kTransposeMinBlocks - 1) /
+                                                           kTransposeMinBlocks)));
       for (uint16_t wid : wide_ids) {
-        for (int64_t r0 = 0; r0 < rows; r0 += nb) {
-          reshard_tblock_t blk = {};
-          blk.wide_off = wide_base + r0 * L;
-          blk.row_bytes = uint32_t(L);
-          blk.nrows = uint32_t(std::min(nb, rows - r0));
-          blk.seg_begin = uint32_t(PF.tsegs.size());
-          blk.wide = wid;
-          blk.direction = gather ? 0 : 1;
-          for (size_t i = 0; i < ps.size(); ++i) {
-            const Piece& pc = ps[i];
-            for (uint16_t nid : narrow_ids[i]) {
-              reshard_tseg_t sg = {};
-              sg.narrow_off = pc.narrow.base + r0 * pc.narrow.width;
-              sg.width = uint32_t(pc.narrow.width);
-              sg.col = uint32_t(pc.col);
-              sg.narrow = nid;
-              PF.tsegs.push_back(sg);
+        for (int64_t pl = 0; pl < planes; ++pl) {
+          for (int64_t r0 = 0; r0 < rows; r0 += nb) {
+            reshard_tblock_t blk = {};
+            blk.wide_off = wide_base + pl * wide_pstride + r0 * L;
+            blk.row_bytes = uint32_t(L);
+            blk.nrows = uint32_t(std::min(nb, rows - r0));
+            blk.seg_begin = uint32_t(PF.tsegs.size());
+            blk.wide = wid;
+            blk.direction = gather ? 0 : 1;
+            for (size_t i = 0; i < ps.size(); ++i) {
+              const Piece& pc = ps[i];
+              for (uint16_t nid : narrow_ids[i]) {
+                reshard_tseg_t sg = {};
+                sg.narrow_off = pc.narrow.base + pl * pc.narrow.pstride + r0 * pc.narrow.width;
+                sg.width = uint32_t(pc.narrow.width);
+                sg.col = uint32_t(pc.col);
+                sg.narrow = nid;
+                PF.tsegs.push_back(sg);
+              }
             }
+            blk.seg_count = uint32_t(PF.tsegs.size()) - blk.seg_begin;
+            PF.tblocks.push_back(blk);
           }
-          blk.seg_count = uint32_t(PF.tsegs.size()) - blk.seg_begin;
-          PF.tblocks.push_back(blk);
         }
       }
       for (const Piece& pc : ps) consumed[pc.ri] = 1;
     };
-    // Checks a candidate group: same rows, narrow sides dense, wide side covered exactly.
+    // Checks a candidate group: same rows (and planes), narrow sides dense within a
+    // plane, wide side covered exactly.  Rows that collapse into one level on both
+    // sides are one plane; otherwise the group is tried as planes of rows.
     auto try_group = [&](const std::vector<size_t>& members, bool gather) {
       if (members.size() < 2 || members.size() > size_t(kTransposeMaxSegs)) return;
-      std::vector<Piece> ps;
-      int64_t rows = -1, L = -1, base = INT64_MAX;
-      for (size_t ri : members) {
+      for (size_t ri : members)
         if (consumed[ri]) return;
-        const Region& g = regions[ri];
-        const Box& sb = P->src.box[size_t(g.replica)];
-        const Box& db = dc[g.d].box;
-        const RowView sv = row_view(nd, g.lo, g.ext, sb, eb);
-        const RowView dv = row_view(nd, g.lo, g.ext, db, eb);
-        if (!sv.ok || !dv.ok) return;
-        const RowView& wide = gather ? dv : sv;
-        const RowView& narrow = gather ? sv : dv;
-        if (narrow.width >= kTransposeMaxWidth) return;
-        if (rows < 0) rows = wide.rows;
-        if (wide.rows != rows || rows < 2) return;
-        if (narrow.stride != narrow.width) return;  // narrow side dense
-        if (L < 0) L = wide.stride;
-        if (wide.stride != L) return;
-        base = std::min(base, wide.base);
-        ps.push_back({ri, wide, narrow, 0});
+      std::vector<Piece> ps;
+      int64_t planes = -1, rows = -1, L = -1, wps = -1, base = INT64_MAX;
+      for (int as_plane_rows = 0; as_plane_rows < 2 && ps.size() != members.size();
+           ++as_plane_rows) {
+        ps.clear();
+        planes = rows = L = wps = -1;
+        base = INT64_MAX;
+        for (size_t ri : members) {
+          const Region& g = regions[ri];
+          const Box& sb = P->src.box[size_t(g.replica)];
+          const Box& db = dc[g.d].box;
+          const PlaneView sv = as_plane_rows ? plane_view(nd, g.lo, g.ext, sb, eb)
+                                             : as_planes(row_view(nd, g.lo, g.ext, sb, eb));
+          const PlaneView dv = as_plane_rows ? plane_view(nd, g.lo, g.ext, db, eb)
+                                             : as_planes(row_view(nd, g.lo, g.ext, db, eb));
+          if (!sv.ok || !dv.ok) break;
+          const PlaneView& wide = gather ? dv : sv;
+          const PlaneView& narrow = gather ? sv : dv;
+          if (narrow.width >= kTransposeMaxWidth) break;
+          if (rows < 0) {
+            planes = wide.planes;
+            rows = wide.rows;
+            L = wide.stride;
+            wps = wide.pstride;
+          }
+          if (wide.rows != rows || rows < 2 || narrow.rows != rows) break;
+          if (wide.planes != planes || narrow.planes != planes || wide.pstride != wps) break;
+          if (narrow.stride != narrow.width) break;  // narrow side dense within a plane
+          if (wide.stride != L) break;
+          base = std::min(base, wide.base);
+          ps.push_back({ri, wide, narrow, 0});
+        }
       }
+      if (ps.size() != members.size()) return;
       if (L <= 0 || L > kTransposeBlockBytes) return;
       int64_t covered = 0;
       for (Piece& pc : ps) {
@@ -541,12 +607,15 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       }
       if (covered != L) return;  // with disjoint regions: exact cover of every wide row
       // Measured on GB300 (uneven-stress tensors): regrouping pays when a gather
-      // fans out to several destination replicas, or when the pieces are tiny
-      // (at most 4 bytes) and numerous; otherwise per-piece copies are faster.
+      // fans out to several destination replicas, or when the pieces are narrow
+      // (at most 32 bytes) and numerous (a scatter of 45 pieces of 32 bytes: 0.250
+      // -> 0.205 ms; of 47 pieces of 18 bytes: 0.059 -> 0.049 ms); with fewer
+      // pieces (a scatter of 8 pieces of 4 bytes out of 32-byte rows: 0.15 -> 0.34
+      // ms) or wider ones, per-piece copies are faster.
       int64_t max_w = 0;
       for (const Piece& pc : ps) max_w = std::max(max_w, pc.narrow.width);
       const bool fanned = gather && dc[regions[members[0]].d].ranks.size() >= 2;
-      if (!fanned && !(max_w <= 4 && ps.size() >= 16)) return;
+      if (!fanned && !(max_w <= 32 && ps.size() >= 16)) return;
       if (!gather) {
         size_t nsegs = 0;
         for (const Piece& pc : ps) {
@@ -561,7 +630,7 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       std::vector<uint16_t> wide_ids;
       if (gather) wide_ids = fan_groups(dc[regions[members[0]].d].ranks);
       else wide_ids.push_back(uint16_t(regions[members[0]].replica));
-      emit_group(ps, gather, rows, L, base, wide_ids);
+      emit_group(ps, gather, planes, rows, L, base, wps, wide_ids);
     };
     std::vector<std::vector<size_t>> into(dc.size()), outof(sc.size());
     for (size_t ri = 0; ri < regions.size(); ++ri) {
@@ -594,6 +663,56 @@ reshard_status_t build_plan(reshard_plan_s* P) {
   // ---- step 5b: tiles
   int64_t gst[RESHARD_MAX_TENSOR_NDIM];
   row_major_strides(nd, P->gshape, gst);
+  // Region placement in its source replica and destination class (element offsets
+  // and strides of both local layouts).
+  struct Place {
+    int64_t s0 = 0, d0 = 0;
+    int64_t sst[RESHARD_MAX_TENSOR_NDIM] = {}, dst[RESHARD_MAX_TENSOR_NDIM] = {};
+  };
+  auto place_of = [&](const Region& g) {
+    Place q;
+    const Box& sb = P->src.box[size_t(g.replica)];
+    const Box& db = dc[g.d].box;
+    row_major_strides(nd, sb.shp, q.sst);
+    row_major_strides(nd, db.shp, q.dst);
+    for (int d = 0; d < nd; ++d) {
+      q.s0 += (g.lo[d] - sb.off[d]) * q.sst[d];
+      q.d0 += (g.lo[d] - db.off[d]) * q.dst[d];
+    }
+    return q;
+  };
+  // Destination classes assembled in one replica (their first rank) and then
+  // replicated: many replicas, several regions meeting in each shard (a single
+  // region would be copied twice for nothing), every region on per-piece tiles
+  // (no transpose block), and tiles that would take the register realigning kernel (off the
+  // 16-byte grid, mostly rows of 512 bytes and more, not mostly rows of 8 KiB
+  // in a class large enough for the staged kernel).  The pages' two-stage
+  // transfer reads the same way: one copy crosses once, then is replicated
+  // where it landed.
+  std::vector<int64_t> assemble_at(dc.size(), -1);
+  if (!P->inplace) {
+    std::vector<std::vector<size_t>> of_class(dc.size());
+    for (size_t ri = 0; ri < regions.size(); ++ri) of_class[regions[ri].d].push_back(ri);
+    for (size_t di = 0; di < dc.size(); ++di) {
+      if (int64_t(dc[di].ranks.size()) < kAssembleFanout || of_class[di].size() < 2) continue;
+      bool blocked = false;
+      for (size_t ri : of_class[di]) blocked = blocked || consumed[ri];
+      if (blocked) continue;
+      Program T;
+      T.goff = {0, 1};
+      T.gbuf = {0};
+      for (size_t ri : of_class[di]) {
+        const Region& g = regions[ri];
+        const Place q = place_of(g);
+        emit_box(T, 0, 0, nd, g.ext, q.s0, q.sst, q.d0, q.dst, eb);
+      }
+      finish_program(T);
+      const bool aligned = (T.align_bits & 15u) == 0;
+      const bool long_rows = 2 * T.long_row_bytes >= T.tile_bytes;
+      const bool staged = 2 * T.wide_row_bytes >= T.tile_bytes && T.tile_bytes >= (int64_t(48) << 20);
+      if (!aligned && long_rows && !staged) assemble_at[di] = dc[di].ranks[0];
+    }
+  }
   for (size_t ri = 0; ri < regions.size(); ++ri) {
     const Region& g = regions[ri];
     // destination ranks that still need the region (in-place plans drop the
@@ -618,14 +737,30 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       s0 += (g.lo[d] - sb.off[d]) * sst[d];
       d0 += (g.lo[d] - db.off[d]) * dst[d];
     }
-    if (!consumed[ri])
-      for (uint16_t grp : fan_groups(targets))
+    if (!consumed[ri]) {
+      const std::vector<int64_t> assembly = {assemble_at[g.d]};
+      for (uint16_t grp : fan_groups(assemble_at[g.d] >= 0 ? assembly : targets))
         emit_box(PF, uint16_t(g.replica), grp, nd, g.ext, s0, sst, d0, dst, eb,
                  int64_t(PF.goff[grp + 1] - PF.goff[grp]));
+    }
     for (int64_t r : targets)
       emit_box(PB, uint16_t(g.replica), uint16_t(r), nd, g.ext, s0, sst, d0, dst, eb);
   }
   if (too_many_groups) return fail(RESHARD_ERR_UNSUPPORTED, "more than 65535 fan-out groups");
+  // replicate: each assembled destination shard, one run, to the class's other ranks
+  for (size_t di = 0; di < dc.size(); ++di) {
+    if (assemble_at[di] < 0) continue;
+    ++S.assembled_classes;
+    const int64_t vol = box_volume(nd, dc[di].box);
+    const int64_t unit = 1;
+    for (size_t a = 1; a < dc[di].ranks.size(); a += kMaxGroup) {
+      const uint16_t grp = uint16_t(PR.goff.size() - 1);
+      for (size_t b = a; b < std::min(dc[di].ranks.size(), a + size_t(kMaxGroup)); ++b)
+        PR.gbuf.push_back(uint16_t(M + dc[di].ranks[b]));
+      PR.goff.push_back(uint32_t(PR.gbuf.size()));
+      emit_box(PR, uint16_t(M + assemble_at[di]), grp, 1, &vol, 0, &unit, 0, &unit, eb);
+    }
+  }
   // gather: one replica of every source class into the full tensor
   {
     std::vector<size_t> order(sc.size());
@@ -656,16 +791,19 @@ reshard_status_t build_plan(reshard_plan_s* P) {
     for (int d = 0; d < nd; ++d) s0 += b.off[d] * gst[d];
     emit_box(PS, scratch_buf, uint16_t(r), nd, b.shp, s0, gst, 0, dst, eb);
   }
-  for (Program* p : {&PF, &PB, &PG, &PS}) finish_program(*p);
+  for (Program* p : {&PF, &PB, &PG, &PS, &PR}) finish_program(*p);
   PF.staged = true;
+  PR.staged = true;
   for (int k = 0; k < 4; ++k) S.n_tiles[k] = int64_t(P->prog[k].tiles.size());
+  S.n_replicate_tiles = int64_t(PR.tiles.size());
 
   // ---- traffic accounting
-  for (const reshard_tile_t& t : PF.tiles) {
-    const int64_t R = P->prog[0].goff[t.dst_group + 1] - P->prog[0].goff[t.dst_group];
-    S.fanout_read_bytes += tile_bytes(t);
-    S.fanout_write_bytes += R * tile_bytes(t);
-  }
+  for (const Program* p : {&PF, &PR})
+    for (const reshard_tile_t& t : p->tiles) {
+      const int64_t R = p->goff[t.dst_group + 1] - p->goff[t.dst_group];
+      S.fanout_read_bytes += tile_bytes(t);
+      S.fanout_write_bytes += R * tile_bytes(t);
+    }
   for (const reshard_tblock_t& b : PF.tblocks) {
     PF.talign_bits |= uint64_t(b.row_bytes) | uint64_t(b.wide_off);
     for (uint32_t k = b.seg_begin; k < b.seg_begin + b.seg_count; ++k)
@@ -964,8 +1102,8 @@ reshard_status_t upload_plan(reshard_plan_s* plan) {
   // one allocation: per program tiles | prefix | goff | gbuf, each 256-byte aligned
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t total = 0;
-  size_t offs[4][6];
-  for (int k = 0; k < 4; ++k) {
+  size_t offs[rs::kNumPrograms][6];
+  for (int k = 0; k < rs::kNumPrograms; ++k) {
     const rs::Program& p = plan->prog[k];
     const size_t sz[6] = {p.tiles.size() * sizeof(reshard_tile_t), p.prefix.size() * sizeof(int64_t),
                           p.goff.size() * sizeof(uint32_t), p.gbuf.size() * sizeof(uint16_t),
@@ -982,7 +1120,7 @@ reshard_status_t upload_plan(reshard_plan_s* plan) {
   } catch (const std::bad_alloc&) {
     return fail(RESHARD_ERR_NO_MEMORY, "host staging allocation failed");
   }
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < rs::kNumPrograms; ++k) {
     const rs::Program& p = plan->prog[k];
     if (!p.tiles.empty()) std::memcpy(&host[offs[k][0]], p.tiles.data(), p.tiles.size() * sizeof(reshard_tile_t));
     if (!p.prefix.empty()) std::memcpy(&host[offs[k][1]], p.prefix.data(), p.prefix.size() * sizeof(int64_t));
@@ -1002,7 +1140,7 @@ reshard_status_t upload_plan(reshard_plan_s* plan) {
     return fail(RESHARD_ERR_CUDA, std::string("cudaMemcpy: ") + cudaGetErrorString(ce));
   }
   unsigned char* base = static_cast<unsigned char*>(d);
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < rs::kNumPrograms; ++k) {
     rs::Program& p = plan->prog[k];
     p.d_tiles = reinterpret_cast<const reshard_tile_t*>(base + offs[k][0]);
     p.d_prefix = reinterpret_cast<const int64_t*>(base + offs[k][1]);
@@ -1075,9 +1213,9 @@ reshard_status_t reshard_execute_ex(reshard_plan_t plan, const void* const* src_
   if (st != RESHARD_OK) return st;
   st = reshard_plan_upload(plan);
   if (st != RESHARD_OK) return st;
-  const rs::Program& p =
-      plan->prog[kernel == RESHARD_KERNEL_FANOUT ? RESHARD_PROGRAM_FANOUT : RESHARD_PROGRAM_BOXCOPY];
-  return rs::launch_program(plan, p, bufs.data(), int(bufs.size()), stream);
+  if (kernel == RESHARD_KERNEL_FANOUT) return rs::launch_fanout(plan, bufs.data(), int(bufs.size()), stream);
+  return rs::launch_program(plan, plan->prog[RESHARD_PROGRAM_BOXCOPY], bufs.data(), int(bufs.size()),
+                            stream);
 }
 
 reshard_status_t reshard_plan_path(reshard_plan_t plan, const void* const* src_ptrs,
@@ -1150,7 +1288,8 @@ reshard_status_t reshard_plan_program(reshard_plan_t plan, int32_t program,
                                       const int64_t** unit_prefix, const uint32_t** group_offsets,
                                       const uint16_t** group_buffers, int64_t* ngroups) {
   if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
-  if (program < 0 || program > 3) return fail(RESHARD_ERR_INVALID_ARG, "unknown program");
+  if (program < 0 || program >= rs::kNumPrograms)
+    return fail(RESHARD_ERR_INVALID_ARG, "unknown program");
   const rs::Program& p = plan->prog[program];
   if (tiles) *tiles = p.tiles.data();
   if (ntiles) *ntiles = int64_t(p.tiles.size());
@@ -1165,7 +1304,8 @@ reshard_status_t reshard_plan_transposes(reshard_plan_t plan, int32_t program,
                                          const reshard_tblock_t** blocks, int64_t* nblocks,
                                          const reshard_tseg_t** segs, int64_t* nsegs) {
   if (!rs::live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
-  if (program < 0 || program > 3) return fail(RESHARD_ERR_INVALID_ARG, "unknown program");
+  if (program < 0 || program >= rs::kNumPrograms)
+    return fail(RESHARD_ERR_INVALID_ARG, "unknown program");
   const rs::Program& p = plan->prog[program];
   if (blocks) *blocks = p.tblocks.data();
   if (nblocks) *nblocks = int64_t(p.tblocks.size());

@@ -129,7 +129,10 @@ typedef enum reshard_program {
   RESHARD_PROGRAM_FANOUT = 0,  /* reshard, read-once fan-out */
   RESHARD_PROGRAM_BOXCOPY = 1, /* reshard, one copy per destination replica */
   RESHARD_PROGRAM_GATHER = 2,  /* gather-and-broadcast step 1: shards -> full */
-  RESHARD_PROGRAM_SLICE = 3    /* gather-and-broadcast step 2: full -> shards */
+  RESHARD_PROGRAM_SLICE = 3,   /* gather-and-broadcast step 2: full -> shards */
+  RESHARD_PROGRAM_REPLICATE = 4 /* reshard, second step of FANOUT: a destination shard that the
+                                   first step assembled in one replica, copied as one run to
+                                   the class's other replicas (empty for most plans) */
 } reshard_program_t;
 
 /* Planner and traffic statistics of one plan (all byte counts exact). */
@@ -150,6 +153,8 @@ typedef struct reshard_stats {
   int64_t max_fanout;          /* largest number of destination replicas of one box */
   int64_t planner_ns;          /* wall time of reshard_plan_create */
   int64_t inplace_bytes;       /* destination bytes already in place (in-place plans), not written */
+  int64_t assembled_classes;   /* destination classes assembled in one replica, then replicated */
+  int64_t n_replicate_tiles;   /* tiles of RESHARD_PROGRAM_REPLICATE */
 } reshard_stats_t;
 
 /*

@@ -51,8 +51,17 @@ def run_program_cpu(plan, program, bufs):
     ``bufs`` is the buffer table [sources..., destinations..., scratch].  Returns,
     per buffer, a count array of how many times each byte was written.
     """
-    tiles, prefix, goff, gbuf = rs.reshard_plan_program(plan, program)
     writes = [np.zeros(b.size, dtype=np.int32) for b in bufs]
+    _run_tiles_cpu(plan, program, bufs, writes)
+    run_transposes_cpu(plan, program, bufs, writes)
+    if program == rs.PROGRAM_FANOUT:
+        # second step: destination shards assembled in one replica, copied to the others
+        _run_tiles_cpu(plan, rs.PROGRAM_REPLICATE, bufs, writes)
+    return writes
+
+
+def _run_tiles_cpu(plan, program, bufs, writes):
+    tiles, prefix, goff, gbuf = rs.reshard_plan_program(plan, program)
     for t in tiles:
         src = bufs[t["src_buf"]]
         for g in range(goff[t["dst_group"]], goff[t["dst_group"] + 1]):
@@ -67,8 +76,6 @@ def run_program_cpu(plan, program, bufs):
                     assert 0 <= do and do + n <= dst.size, ("destination out of bounds", t)
                     dst[do:do + n] = src[so:so + n]
                     writes[di][do:do + n] += 1
-    run_transposes_cpu(plan, program, bufs, writes)
-    return writes
 
 
 def run_transposes_cpu(plan, program, bufs, writes):

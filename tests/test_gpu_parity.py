@@ -654,6 +654,10 @@ TRANSPOSE_CASES = [
     _spec((300, 40), "u8", (1,), ("R",), (40,), ("S1",), seed=4),               # scatter, 1 B
     _spec((40, 45, 17), "fp32", (6,), ("S0",), (17,), ("S2",), seed=5),         # scatter 3-D
     _spec((4097, 20), "u8", (20,), ("S1",), (4,), ("R",), seed=6),              # gather, 1 B, R=4
+    _spec((40, 451, 715), "bf16", (6,), ("S0",), (45,), ("S2",), seed=7),       # scatter, 32 B
+    _spec((2000, 288), "bf16", (18,), ("S1",), (4,), ("S0",), seed=8),          # gather, 32 B, R=1
+    _spec((50, 553, 122), "bf16", (32,), ("S2",), (16,), ("S1",), seed=9),      # gather, planes
+    _spec((30, 40, 300), "bf16", (4,), ("S1",), (20,), ("S2",), seed=10),       # scatter, planes
 ]
 
 
@@ -665,6 +669,28 @@ def test_transpose_blocks(oracle, i, misalign):
     assert blocks, "layout expected to use transpose blocks"
     run_and_compare(oracle, spec, misalign=misalign)
     run_and_compare(oracle, spec, misalign=misalign, dst_misalign=lambda r: (r * 5) % 16)
+
+
+# ---------------------------------------------------------------------- assemble, then replicate
+# Column bands of 632-byte rows (off the 16-byte grid) gathered into 9 and into 15 replicas:
+# the first step assembles the shard in one replica, the second copies it as one run to the
+# others (TMA fan-out when the buffers are aligned, the vector kernel otherwise).
+ASSEMBLE_CASES = [
+    _spec((600, 2200), "fp32", (14,), ("S1",), (9,), ("R",), seed=21),
+    _spec((393, 8780), "fp32", (56,), ("S1",), (15,), ("R",), seed=22),
+    _spec((2, 300, 4424), "bf16", (2, 14), ("R", "S2"), (3, 12), ("S0", "R"), seed=23),
+]
+
+
+@pytest.mark.parametrize("i", range(len(ASSEMBLE_CASES)))
+@pytest.mark.parametrize("misalign", [0, 3])
+def test_assemble_then_replicate(oracle, i, misalign):
+    spec = ASSEMBLE_CASES[i]
+    plan = helpers.spec_plan(spec)
+    st = rs.reshard_plan_stats(plan)
+    assert st["assembled_classes"] >= 1 and st["n_replicate_tiles"] >= 1
+    run_and_compare(oracle, spec, misalign=misalign)
+    run_and_compare(oracle, spec, misalign=misalign, dst_misalign=lambda r: (r * 4) % 16)
 
 
 # ---------------------------------------------------------------------- staged realigning copy

@@ -59,6 +59,69 @@ def test_reduced_workloads(oracle, cfg):
         _check_spec(oracle, spec)
 
 
+@pytest.mark.parametrize("case,transposed", [
+    # 45 pieces of 32 bytes cut out of 1430-byte rows: transpose blocks
+    (((6, 40, 715), "bf16", (6,), ("S0",), (45,), ("S2",)), True),
+    # 18 narrow sources of 32 bytes into one destination replica: transpose blocks
+    (((200, 288), "bf16", (18,), ("S1",), (4,), ("S0",)), True),
+    # 3-D gather: 31 narrow sources of 8 bytes whose rows break into planes of 8 rows
+    (((10, 30, 122), "bf16", (32,), ("S2",), (4,), ("S1",)), True),
+    # 3-D scatter: 20 pieces of 30 bytes into destinations cut along the middle dim too
+    (((10, 40, 300), "bf16", (4,), ("S1",), (20,), ("S2",)), True),
+    # pieces of 34 bytes: per-piece copies
+    (((6, 40, 765), "bf16", (6,), ("S0",), (45,), ("S2",)), False),
+    # 8 pieces of 4 bytes out of 32-byte rows (too few): per-piece copies
+    (((60, 50, 8), "fp32", (8,), ("S0",), (17,), ("S2",)), False),
+])
+def test_transpose_rule_for_narrow_pieces(oracle, case, transposed):
+    """Narrow innermost pieces (at most 32 bytes per row, at least 16 of them) are regrouped
+    into transpose blocks, in planes of rows where the rows do not collapse into one level;
+    wider or fewer pieces stay per-piece tiles.  Either way the program, executed on the
+    CPU, reproduces the oracle."""
+    spec = _case(*case, seed=9)
+    plan = _check_spec(oracle, spec)
+    blocks, _ = rs.reshard_plan_transposes(plan, rs.PROGRAM_FANOUT)
+    assert bool(blocks) == transposed
+
+
+@pytest.mark.parametrize("case,assembled", [
+    # 14 column bands of 632 bytes (off the 16-byte grid) into 9 replicas: assembled
+    (((60, 2200), "fp32", (14,), ("S1",), (9,), ("R",)), 1),
+    # two destination classes of 12 replicas each, bands of 632 bytes in 3-D: assembled
+    (((2, 30, 4424), "bf16", (2, 14), ("R", "S2"), (2, 12), ("S0", "R")), 2),
+    # 7 replicas: too few
+    (((60, 2200), "fp32", (14,), ("S1",), (7,), ("R",)), 0),
+    # bands of 640 bytes, on the 16-byte grid: the TMA fan-out takes them directly
+    (((60, 2240), "fp32", (14,), ("S1",), (9,), ("R",)), 0),
+    # one source region per shard (a replicated tensor): nothing to assemble
+    (((60, 2201), "fp32", (3,), ("R",), (9,), ("R",)), 0),
+])
+def test_assemble_then_replicate(oracle, case, assembled):
+    """Destination shards that many replicas need, cut from pieces off the 16-byte grid, are
+    assembled in their first replica and then copied as one run to the others: every byte
+    written once, the oracle's result, and traffic G + D plus one read per assembled shard."""
+    spec = _case(*case, seed=5)
+    plan = _check_spec(oracle, spec)
+    st = rs.reshard_plan_stats(plan)
+    assert st["assembled_classes"] == assembled
+    tiles, _, goff, gbuf = rs.reshard_plan_program(plan, rs.PROGRAM_REPLICATE)
+    assert len(tiles) == st["n_replicate_tiles"] == assembled
+    M = spec.n_src
+    shard = 0
+    for t in tiles:
+        first = t["src_buf"] - M
+        others = [b - M for b in gbuf[goff[t["dst_group"]]:goff[t["dst_group"] + 1]]]
+        assert first not in others
+        shp, _ = rs.reshard_plan_local_shape(plan, 1, first)
+        assert t["row_bytes"] == math.prod(shp) * spec.elem_bytes and t["src_off"] == 0
+        for r in others:
+            assert rs.reshard_plan_local_shape(plan, 1, r) == rs.reshard_plan_local_shape(
+                plan, 1, first)
+        shard += t["row_bytes"]
+    assert st["fanout_read_bytes"] == st["global_bytes"] + shard
+    assert st["fanout_write_bytes"] == st["dst_bytes"]
+
+
 def test_uneven_stress_reduced(oracle):
     for spec in workload(4, reduced=True).tensors:
         _check_spec(oracle, spec)
