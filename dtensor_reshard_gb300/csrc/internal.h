@@ -142,9 +142,10 @@ struct Program {
   const reshard_tseg_t* d_tsegs = nullptr;
 };
 
-// Narrow pieces (bytes per row) below this go through transpose blocks, and a
-// block holds at most this many bytes of wide rows in shared memory.
-constexpr int64_t kTransposeMaxWidth = 64;
+// Narrow pieces (bytes per row) below this may go through transpose blocks
+// (the planner's rule narrows it further), and a block holds at most this many
+// bytes of wide rows in shared memory.
+constexpr int64_t kTransposeMaxWidth = 129;
 constexpr int64_t kTransposeBlockBytes = 20 * 1024;
 // Blocks a transpose group aims for (smaller blocks when the group is small).
 constexpr int64_t kTransposeMinBlocks = 512;

@@ -609,13 +609,20 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       // Measured on GB300 (uneven-stress tensors): regrouping pays when a gather
       // fans out to several destination replicas, or when the pieces are narrow
       // (at most 32 bytes) and numerous (a scatter of 45 pieces of 32 bytes: 0.250
-      // -> 0.205 ms; of 47 pieces of 18 bytes: 0.059 -> 0.049 ms); with fewer
-      // pieces (a scatter of 8 pieces of 4 bytes out of 32-byte rows: 0.15 -> 0.34
-      // ms) or wider ones, per-piece copies are faster.
+      // -> 0.205 ms; of 47 pieces of 18 bytes: 0.059 -> 0.049 ms), or for gathers
+      // of 16 or more pieces up to 128 bytes into wide rows short enough for four
+      // of them per block (42 pieces of 68 bytes: 0.133 -> 0.113 ms; 55 of 72
+      // bytes: 0.018 -> 0.014 ms).  With fewer pieces (a scatter of 8 pieces of 4
+      // bytes out of 32-byte rows: 0.15 -> 0.34 ms), wider scatters (68-byte
+      // pieces: +0.008 ms) or gathers into rows of 9 KB (two rows per block:
+      // +0.008 ms), per-piece copies are faster.
       int64_t max_w = 0;
       for (const Piece& pc : ps) max_w = std::max(max_w, pc.narrow.width);
       const bool fanned = gather && dc[regions[members[0]].d].ranks.size() >= 2;
-      if (!fanned && !(max_w <= 32 && ps.size() >= 16)) return;
+      const bool narrow_many = max_w <= 32 && ps.size() >= 16;
+      const bool gather_wide = gather && max_w <= 128 && ps.size() >= 16 &&
+                               4 * L <= kTransposeBlockBytes;
+      if (!fanned && !narrow_many && !gather_wide) return;
       if (!gather) {
         size_t nsegs = 0;
         for (const Piece& pc : ps) {

@@ -658,6 +658,7 @@ TRANSPOSE_CASES = [
     _spec((2000, 288), "bf16", (18,), ("S1",), (4,), ("S0",), seed=8),          # gather, 32 B, R=1
     _spec((50, 553, 122), "bf16", (32,), ("S2",), (16,), ("S1",), seed=9),      # gather, planes
     _spec((30, 40, 300), "bf16", (4,), ("S1",), (20,), ("S2",), seed=10),       # scatter, planes
+    _spec((3, 400, 1416), "bf16", (42,), ("S2",), (5,), ("S1",), seed=11),      # gather, 68 B
 ]
 
 

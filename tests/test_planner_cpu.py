@@ -68,15 +68,24 @@ def test_reduced_workloads(oracle, cfg):
     (((10, 30, 122), "bf16", (32,), ("S2",), (4,), ("S1",)), True),
     # 3-D scatter: 20 pieces of 30 bytes into destinations cut along the middle dim too
     (((10, 40, 300), "bf16", (4,), ("S1",), (20,), ("S2",)), True),
-    # pieces of 34 bytes: per-piece copies
+    # scatter of pieces of 34 bytes: per-piece copies
     (((6, 40, 765), "bf16", (6,), ("S0",), (45,), ("S2",)), False),
+    # gather of 42 pieces of 68 bytes into 2832-byte rows (7 per block), 3-D: transposed
+    (((3, 40, 1416), "bf16", (42,), ("S2",), (5,), ("S1",)), True),
+    # gather of 46 pieces of 206 bytes: too wide
+    (((40, 4717), "bf16", (46,), ("S1",), (1,), ("S1",)), False),
+    # gather of 32 pieces of 128 bytes into 4 KB rows: transposed
+    (((40, 1024), "fp32", (32,), ("S1",), (4,), ("S0",)), True),
+    # gather of 80 pieces of 128 bytes into 10 KB rows (two per block): per-piece copies
+    (((40, 2560), "fp32", (80,), ("S1",), (4,), ("S0",)), False),
     # 8 pieces of 4 bytes out of 32-byte rows (too few): per-piece copies
     (((60, 50, 8), "fp32", (8,), ("S0",), (17,), ("S2",)), False),
 ])
 def test_transpose_rule_for_narrow_pieces(oracle, case, transposed):
-    """Narrow innermost pieces (at most 32 bytes per row, at least 16 of them) are regrouped
-    into transpose blocks, in planes of rows where the rows do not collapse into one level;
-    wider or fewer pieces stay per-piece tiles.  Either way the program, executed on the
+    """Narrow innermost pieces (at least 16 of them, at most 32 bytes per row, or up to 128
+    bytes gathered into rows short enough for four per block) are regrouped into transpose
+    blocks, in planes of rows where the rows do not collapse into one level; wider or fewer
+    pieces stay per-piece tiles.  Either way the program, executed on the
     CPU, reproduces the oracle."""
     spec = _case(*case, seed=9)
     plan = _check_spec(oracle, spec)
