@@ -33,7 +33,6 @@ struct reshard_refit_s {
   int device = -1;
   cudaEvent_t fork = nullptr;
   std::array<cudaEvent_t, RESHARD_REFIT_NUM_LANES> join = {};
-  std::mutex issue_mu;  // one execution issues onto the lanes at a time
 };
 
 namespace rs {
@@ -56,6 +55,10 @@ bool refit_live(const reshard_refit_s* r) {
 // slots of the copy kernels are not used up by refits created and destroyed.
 std::mutex g_lane_mu;
 std::map<int, std::array<cudaStream_t, RESHARD_REFIT_NUM_LANES>> g_lanes;
+// Executions over the side streams are issued one at a time, whichever refit they
+// belong to: a lane that joined one caller's CUDA-graph capture must not receive
+// another execution's launches until that execution has joined back.
+std::mutex g_issue_mu;
 
 reshard_status_t device_lanes(int dev, std::array<cudaStream_t, RESHARD_REFIT_NUM_LANES>* out) {
   std::lock_guard<std::mutex> lk(g_lane_mu);
@@ -140,8 +143,26 @@ reshard_status_t execute_lanes(reshard_refit_s* R, const void* const* const* src
   std::array<cudaStream_t, RESHARD_REFIT_NUM_LANES> lanes;
   reshard_status_t st = device_lanes(dev, &lanes);
   if (st != RESHARD_OK) return st;
-  std::lock_guard<std::mutex> lk(R->issue_mu);
+  std::lock_guard<std::mutex> lk(g_issue_mu);
   cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  // A lane still belongs to a capture that another execution joined it to until
+  // that capture ends: refuse to mix this execution into it.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  unsigned long long cid = 0;
+  ce = cudaStreamGetCaptureInfo(caller, &cs, &cid);
+  if (ce != cudaSuccess)
+    return fail(RESHARD_ERR_CUDA, std::string("cudaStreamGetCaptureInfo: ") + cudaGetErrorString(ce));
+  const unsigned long long caller_id = cs == cudaStreamCaptureStatusActive ? cid : 0;
+  for (cudaStream_t l : lanes) {
+    cudaStreamCaptureStatus ls = cudaStreamCaptureStatusNone;
+    unsigned long long lid = 0;
+    ce = cudaStreamGetCaptureInfo(l, &ls, &lid);
+    if (ce != cudaSuccess)
+      return fail(RESHARD_ERR_CUDA, std::string("cudaStreamGetCaptureInfo: ") + cudaGetErrorString(ce));
+    if (ls != cudaStreamCaptureStatusNone && (ls != cudaStreamCaptureStatusActive || lid != caller_id))
+      return fail(RESHARD_ERR_UNSUPPORTED,
+                  "the side streams are taking part in another stream capture until it ends");
+  }
   ce = cudaEventRecord(R->fork, caller);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(ce));

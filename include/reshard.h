@@ -461,9 +461,13 @@ typedef enum reshard_route {
  * caller's stream like the one-stream form and can be captured into a CUDA graph
  * from it.  The side streams are created at the first such refit of a device,
  * shared by all refits of that device and kept until the process exits;
- * executions of such refits are issued one at a time (a lock per refit), and the
- * refit must be executed with the device current that it was created on
- * (INVALID_ARG otherwise). */
+ * executions of such refits are issued one at a time (one process-wide lock, so
+ * that a lane taking part in one caller's CUDA-graph capture gets no other
+ * execution's launches), and the refit must be executed with the device current
+ * that it was created on (INVALID_ARG otherwise).  While one caller's stream
+ * capture that took in a lanes execution is open, the side streams belong to it:
+ * an execution from any other stream returns UNSUPPORTED until that capture
+ * ends. */
 #define RESHARD_REFIT_LANES 2u
 #define RESHARD_REFIT_NUM_LANES 4
 

@@ -881,6 +881,44 @@ def test_refit_lanes_in_cuda_graph(oracle):
     assert rs.reshard_device_status() == 0
 
 
+def test_refit_lanes_refuse_a_foreign_capture(oracle):
+    """While a capture that took in a lanes execution is open, the side streams belong to
+    it: a lanes execution from another stream is refused (UNSUPPORTED, nothing enqueued),
+    and runs normally once the capture has ended."""
+    _cuda()
+    w = workload(4, reduced=True)
+    wa = type(w)(w.name, w.tensors[:6], w.note)
+    wb = type(w)(w.name, w.tensors[6:12], w.note)
+    pa, sa, da, want_a, keep_a = _refit_set(oracle, wa)
+    pb, sb, db, want_b, keep_b = _refit_set(oracle, wb)
+    ra = rs.reshard_refit_create(pa, lanes=True)
+    rb = rs.reshard_refit_create(pb, lanes=True)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    rs.reshard_refit_execute(ra, sa, da, None, 0, s1)  # first use uploads the plans
+    rs.reshard_refit_execute(rb, sb, db, None, 0, s2)
+    torch.cuda.synchronize()
+    for ds, dd in keep_a + keep_b:
+        for x in dd:
+            x.payload().fill_(FILL_BYTE)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s1, capture_error_mode="thread_local"):
+        rs.reshard_refit_execute(ra, sa, da, None, 0, s1)
+        with pytest.raises(rs.ReshardError) as e:
+            rs.reshard_refit_execute(rb, sb, db, None, 0, s2)
+        assert e.value.status == 2
+    torch.cuda.synchronize()
+    for ds, dd in keep_b:                      # the refused execution wrote nothing
+        for x in dd:
+            assert (x.payload().cpu().numpy() == FILL_BYTE).all()
+    g.replay()
+    rs.reshard_refit_execute(rb, sb, db, None, 0, s2)
+    torch.cuda.synchronize()
+    _check_refit_set(wa, want_a, keep_a)
+    _check_refit_set(wb, want_b, keep_b)
+    assert rs.reshard_device_status() == 0
+
+
 # ---------------------------------------------------------------------- concurrency
 def test_first_use_from_several_host_threads(oracle):
     """Eight host threads execute one fresh plan at once (each into its own buffers): the
