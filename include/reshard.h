@@ -106,7 +106,11 @@ typedef struct reshard_refit_s* reshard_refit_t;
 typedef enum reshard_kernel {
   /* Read-once fan-out (default): each region is read once from one source
    * replica and written to every destination replica that needs it.  HBM
-   * traffic = global bytes G (read) + destination bytes D (write). */
+   * traffic = global bytes G (read) + destination bytes D (write).  Where the
+   * planner assembles a destination shard in one replica first (program
+   * RESHARD_PROGRAM_REPLICATE: many replicas fed by pieces off the 16-byte
+   * grid), a second launch on the same stream copies it to the other replicas,
+   * and that shard is read once more. */
   RESHARD_KERNEL_FANOUT = 0,
   /* Plain box copy: one copy per (region, destination replica); the source
    * is re-read for every replica.  HBM traffic = D (read) + D (write). */
@@ -539,7 +543,9 @@ reshard_status_t reshard_plan_transposes(reshard_plan_t plan, int32_t program,
  * and no device memory is touched, so any pointers that pass the execution's
  * argument checks may be given.  *path receives a reshard_path_t, *width the
  * widest access in bytes every tile allows (1..16).  Either output may be
- * NULL.  Errors: BAD_HANDLE, INVALID_ARG (as reshard_execute_ex), UNSUPPORTED.
+ * NULL.  For the fan-out this is the path of the first launch; a REPLICATE
+ * step, when the plan has one, is a plain run copy.  Errors: BAD_HANDLE,
+ * INVALID_ARG (as reshard_execute_ex), UNSUPPORTED.
  */
 reshard_status_t reshard_plan_path(reshard_plan_t plan, const void* const* src_ptrs,
                                    void* const* dst_ptrs, int32_t kernel, int32_t* path,
