@@ -612,14 +612,18 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       // -> 0.205 ms; of 47 pieces of 18 bytes: 0.059 -> 0.049 ms), or for gathers
       // of 16 or more pieces up to 128 bytes into wide rows short enough for four
       // of them per block (42 pieces of 68 bytes: 0.133 -> 0.113 ms; 55 of 72
-      // bytes: 0.018 -> 0.014 ms).  With fewer pieces (a scatter of 8 pieces of 4
-      // bytes out of 32-byte rows: 0.15 -> 0.34 ms), wider scatters (68-byte
+      // bytes: 0.018 -> 0.014 ms), or for scatters of rows of at most 8 bytes (3
+      // pieces of 2 bytes: 0.176 -> 0.125 ms).  With fewer pieces of longer rows (8
+      // pieces of 4 bytes out of 32-byte rows: 0.15 -> 0.34 ms), wider scatters (68-byte
       // pieces: +0.008 ms) or gathers into rows of 9 KB (two rows per block:
       // +0.008 ms), per-piece copies are faster.
       int64_t max_w = 0;
       for (const Piece& pc : ps) max_w = std::max(max_w, pc.narrow.width);
       const bool fanned = gather && dc[regions[members[0]].d].ranks.size() >= 2;
-      const bool narrow_many = max_w <= 32 && ps.size() >= 16;
+      // a scatter of rows of at most 8 bytes (a de-interleave): the per-piece copies
+      // read every source sector once per piece, the blocks once
+      const bool tiny_scatter = !gather && L <= 8;
+      const bool narrow_many = (max_w <= 32 && ps.size() >= 16) || tiny_scatter;
       const bool gather_wide = gather && max_w <= 128 && ps.size() >= 16 &&
                                4 * L <= kTransposeBlockBytes;
       if (!fanned && !narrow_many && !gather_wide) return;

@@ -659,6 +659,8 @@ TRANSPOSE_CASES = [
     _spec((50, 553, 122), "bf16", (32,), ("S2",), (16,), ("S1",), seed=9),      # gather, planes
     _spec((30, 40, 300), "bf16", (4,), ("S1",), (20,), ("S2",), seed=10),       # scatter, planes
     _spec((3, 400, 1416), "bf16", (42,), ("S2",), (5,), ("S1",), seed=11),      # gather, 68 B
+    _spec((520, 583, 3), "fp16", (1,), ("S1",), (45,), ("S2",), seed=12),       # de-interleave
+    _spec((700, 3), "fp16", (1,), ("R",), (2,), ("S1",), seed=13),              # 4 + 2 bytes
 ]
 
 

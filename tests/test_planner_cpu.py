@@ -78,13 +78,17 @@ def test_reduced_workloads(oracle, cfg):
     (((40, 1024), "fp32", (32,), ("S1",), (4,), ("S0",)), True),
     # gather of 80 pieces of 128 bytes into 10 KB rows (two per block): per-piece copies
     (((40, 2560), "fp32", (80,), ("S1",), (4,), ("S0",)), False),
+    # a 3-way de-interleave of 6-byte rows: transposed
+    (((200, 50, 3), "fp16", (1,), ("S1",), (45,), ("S2",)), True),
+    # a 2-way de-interleave of 6-byte rows into pieces of 4 and 2 bytes: transposed
+    (((200, 50, 3), "fp16", (1,), ("S1",), (2,), ("S2",)), True),
     # 8 pieces of 4 bytes out of 32-byte rows (too few): per-piece copies
     (((60, 50, 8), "fp32", (8,), ("S0",), (17,), ("S2",)), False),
 ])
 def test_transpose_rule_for_narrow_pieces(oracle, case, transposed):
     """Narrow innermost pieces (at least 16 of them, at most 32 bytes per row, or up to 128
-    bytes gathered into rows short enough for four per block) are regrouped into transpose
-    blocks, in planes of rows where the rows do not collapse into one level; wider or fewer
+    bytes gathered into rows short enough for four per block, or any pieces scattered out of
+    rows of at most 8 bytes) are regrouped into transpose blocks, in planes of rows where the rows do not collapse into one level; wider or fewer
     pieces stay per-piece tiles.  Either way the program, executed on the
     CPU, reproduces the oracle."""
     spec = _case(*case, seed=9)
