@@ -66,7 +66,8 @@ def parse_args(argv=None):
                          "(the default when they all take the TMA fan-out)")
     ap.add_argument("--lanes", action="store_true",
                     help="run the reshard tensors as one refit over the library's side streams "
-                         "(RESHARD_REFIT_LANES) instead of one stream")
+                         "(RESHARD_REFIT_LANES; with batching unless --no-batch) instead of one "
+                         "stream")
     ap.add_argument("--reshard-only", action="store_true",
                     help="leave out the gather-and-broadcast tensors (profiling captures)")
     ap.add_argument("--experts", type=int, default=256,
@@ -562,7 +563,8 @@ def ours_arm(args, rank, world, local):
     lanes = None
     if args.lanes and kernel == rs.KERNEL_FANOUT and len(dom_jobs) > 1:
         batch = None
-        lanes = rs.reshard_refit_create([j.plan for j in dom_jobs], lanes=True)
+        lanes = rs.reshard_refit_create([j.plan for j in dom_jobs], lanes=True,
+                                        batch=not args.no_batch)
     ops = make_step(jobs, kernel, batch, lanes)
     ms_step, dom_ms, clocks = device_time(ops, stream, args.steps, args.warmup, dctx, gpu_uuid)
     ms_step_max = dctx.max(ms_step)
@@ -815,8 +817,10 @@ def report(args):
             for bt, b in batches:
                 rs.reshard_batch_execute(bt, [j.srcs for j in b], [j.dsts for j in b], stream)
 
-        # the same tensors as one refit spread over the side streams
-        lanes = rs.reshard_refit_create([j.plan for j in jobs], lanes=True) if len(jobs) > 1 else None
+        # the same tensors as one refit spread over the side streams (the plans a batch
+        # merges into one launch as one unit)
+        lanes = rs.reshard_refit_create([j.plan for j in jobs], lanes=True,
+                                        batch=True) if len(jobs) > 1 else None
 
         if lanes is not None:
             # pointer tables marshalled once, outside the timed region

@@ -418,8 +418,9 @@ def _nested(ptr_lists):
 
 def reshard_refit_create(plans, routes=None, batch: bool = False, lanes: bool = False) -> Refit:
     """One refit over plans; routes[i] in ROUTE_* (None: AUTO for every plan).
-    batch: the reshard group as one launch; lanes: the reshard group spread over
-    REFIT_NUM_LANES side streams (the two exclude each other)."""
+    batch: the reshard group in as few launches as a batch makes; lanes: the reshard
+    group spread over REFIT_NUM_LANES side streams (with batch as well, the plans a
+    batch merges into one launch run as one unit on one lane)."""
     arr = (ctypes.c_void_p * len(plans))(*[p.handle for p in plans])
     ra = None if routes is None else (ctypes.c_int32 * len(plans))(*[int(r) for r in routes])
     h = ctypes.c_void_p()

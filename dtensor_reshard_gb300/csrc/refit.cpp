@@ -26,10 +26,16 @@ struct reshard_refit_s {
   std::vector<int32_t> gb_idx;        // plans on gather-and-broadcast, in order
   uint64_t scratch_bytes = 0;         // largest global tensor among gb_idx
   reshard_batch_t batch = nullptr;    // reshard_idx as one batch (RESHARD_REFIT_BATCH)
-  // RESHARD_REFIT_LANES: the reshard group in issue order (largest first) and the
-  // side stream each plan runs on; fork/join events; the device they belong to.
-  std::vector<int32_t> lane_order;
-  std::vector<int32_t> lane_of;
+  // RESHARD_REFIT_LANES: the reshard group as units in issue order (largest
+  // first) -- one plan each, or (with RESHARD_REFIT_BATCH too) the plans that one
+  // batch launch merges -- with the side stream each unit runs on; fork/join
+  // events; the device they belong to.
+  struct Unit {
+    std::vector<int32_t> plans;
+    reshard_batch_t batch = nullptr;  // merged plans: their own batch (one launch)
+    int32_t lane = 0;
+  };
+  std::vector<Unit> units;
   int device = -1;
   cudaEvent_t fork = nullptr;
   std::array<cudaEvent_t, RESHARD_REFIT_NUM_LANES> join = {};
@@ -85,30 +91,66 @@ void release_events(reshard_refit_s* R) {
     if (e) cudaEventDestroy(e);
   R->fork = nullptr;
   R->join = {};
+  for (reshard_refit_s::Unit& u : R->units)
+    if (u.batch) reshard_batch_destroy(u.batch);
+  R->units.clear();
 }
 
-// Lane assignment (longest processing time first): plans sorted by the bytes the
-// read-once path moves, largest first, each to the lane with the fewest bytes so
-// far (ties: the lower lane), so the lanes finish close together.  Issue order is
-// the sorted order.
-reshard_status_t assign_lanes(reshard_refit_s* R) {
-  std::vector<int32_t> order = R->reshard_idx;
+// Units and lanes.  With `merge`, the plans that the refit's batch concatenates
+// into one launch (a batch class of several plans) form one unit with a batch of
+// their own; every other plan is a unit of one.  Lane assignment is longest
+// processing time first: units sorted by the bytes the read-once path moves,
+// largest first, each to the lane with the fewest bytes so far (ties: the lower
+// lane), so the lanes finish close together.  Issue order is the sorted order.
+reshard_status_t assign_lanes(reshard_refit_s* R, bool merge) {
   auto bytes = [&](int32_t i) {
     const reshard_stats_t& s = R->plans[size_t(i)]->stats;
     return s.fanout_read_bytes + s.fanout_write_bytes;
   };
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int32_t a, int32_t b) { return bytes(a) > bytes(b); });
+  std::vector<char> merged(R->plans.size(), 0);
+  if (merge && R->batch) {
+    int32_t ncls = 0;
+    std::vector<int32_t> cls(R->reshard_idx.size(), -1);
+    reshard_status_t st = reshard_batch_classes(R->batch, &ncls, cls.data());
+    if (st != RESHARD_OK) return st;
+    std::map<int32_t, std::vector<int32_t>> members;
+    for (size_t k = 0; k < cls.size(); ++k)
+      if (cls[k] >= 0) members[cls[k]].push_back(R->reshard_idx[k]);
+    for (auto& cm : members) {
+      if (cm.second.size() < 2) continue;
+      std::vector<reshard_plan_t> ps;
+      for (int32_t i : cm.second) ps.push_back(R->plans[size_t(i)]);
+      reshard_refit_s::Unit u;
+      u.plans = cm.second;
+      st = reshard_batch_create(ps.data(), int32_t(ps.size()), &u.batch);
+      if (st != RESHARD_OK) return st;
+      R->units.push_back(u);
+      for (int32_t i : cm.second) merged[size_t(i)] = 1;
+    }
+  }
+  for (int32_t i : R->reshard_idx) {
+    if (merged[size_t(i)]) continue;
+    reshard_refit_s::Unit u;
+    u.plans.push_back(i);
+    R->units.push_back(u);
+  }
+  auto unit_bytes = [&](const reshard_refit_s::Unit& u) {
+    int64_t b = 0;
+    for (int32_t i : u.plans) b += bytes(i);
+    return b;
+  };
+  std::stable_sort(R->units.begin(), R->units.end(),
+                   [&](const reshard_refit_s::Unit& a, const reshard_refit_s::Unit& b) {
+                     return unit_bytes(a) > unit_bytes(b);
+                   });
   std::array<int64_t, RESHARD_REFIT_NUM_LANES> load = {};
-  R->lane_of.assign(R->plans.size(), -1);
-  for (int32_t i : order) {
+  for (reshard_refit_s::Unit& u : R->units) {
     size_t best = 0;
     for (size_t l = 1; l < load.size(); ++l)
       if (load[l] < load[best]) best = l;
-    load[best] += bytes(i);
-    R->lane_of[size_t(i)] = int32_t(best);
+    load[best] += unit_bytes(u);
+    u.lane = int32_t(best);
   }
-  R->lane_order = order;
   cudaError_t ce = cudaGetDevice(&R->device);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
@@ -171,9 +213,20 @@ reshard_status_t execute_lanes(reshard_refit_s* R, const void* const* const* src
     if (ce != cudaSuccess)
       return fail(RESHARD_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(ce));
   }
-  for (int32_t i : R->lane_order) {
-    st = reshard_execute(R->plans[size_t(i)], src_ptrs[i], dst_ptrs[i],
-                         lanes[size_t(R->lane_of[size_t(i)])]);
+  for (const reshard_refit_s::Unit& u : R->units) {
+    cudaStream_t lane = lanes[size_t(u.lane)];
+    if (u.batch) {
+      std::vector<const void* const*> s;
+      std::vector<void* const*> d;
+      for (int32_t i : u.plans) {
+        s.push_back(src_ptrs[i]);
+        d.push_back(dst_ptrs[i]);
+      }
+      st = reshard_batch_execute(u.batch, s.data(), d.data(), lane);
+    } else {
+      const int32_t i = u.plans[0];
+      st = reshard_execute(R->plans[size_t(i)], src_ptrs[i], dst_ptrs[i], lane);
+    }
     if (st != RESHARD_OK) break;
   }
   std::string msg;  // keep the first error's message over the join's
@@ -202,9 +255,6 @@ reshard_status_t reshard_refit_create(const reshard_plan_t* plans, const int32_t
   if (!plans || nplans < 1) return fail(RESHARD_ERR_INVALID_ARG, "no plans");
   if ((flags & ~uint32_t(RESHARD_REFIT_BATCH | RESHARD_REFIT_LANES)) != 0)
     return fail(RESHARD_ERR_INVALID_ARG, "unknown refit flags");
-  if ((flags & RESHARD_REFIT_BATCH) && (flags & RESHARD_REFIT_LANES))
-    return fail(RESHARD_ERR_INVALID_ARG,
-                "RESHARD_REFIT_BATCH and RESHARD_REFIT_LANES exclude each other");
   reshard_refit_s* R = new (std::nothrow) reshard_refit_s();
   if (!R) return fail(RESHARD_ERR_NO_MEMORY, "host allocation failed");
   try {
@@ -241,7 +291,10 @@ reshard_status_t reshard_refit_create(const reshard_plan_t* plans, const int32_t
       }
     }
     if ((flags & RESHARD_REFIT_LANES) && !R->reshard_idx.empty()) {
-      reshard_status_t st = rs::assign_lanes(R);
+      reshard_status_t st = rs::assign_lanes(R, (flags & RESHARD_REFIT_BATCH) != 0);
+      // the units hold what the whole-group batch was needed for
+      if (R->batch) reshard_batch_destroy(R->batch);
+      R->batch = nullptr;
       if (st != RESHARD_OK) {
         rs::release_events(R);
         delete R;
@@ -284,7 +337,10 @@ reshard_status_t reshard_refit_execute(reshard_refit_t refit, const void* const*
     if (!rs::plan_live(refit->plans[i]))
       return fail(RESHARD_ERR_BAD_HANDLE, "plan " + std::to_string(i) + " was destroyed");
   reshard_status_t st = RESHARD_OK;
-  if (refit->batch) {
+  if (refit->fork) {
+    st = rs::execute_lanes(refit, src_ptrs, dst_ptrs, stream);
+    if (st != RESHARD_OK) return st;
+  } else if (refit->batch) {
     std::vector<const void* const*> s;
     std::vector<void* const*> d;
     for (int32_t i : refit->reshard_idx) {
@@ -292,9 +348,6 @@ reshard_status_t reshard_refit_execute(reshard_refit_t refit, const void* const*
       d.push_back(dst_ptrs[i]);
     }
     st = reshard_batch_execute(refit->batch, s.data(), d.data(), stream);
-    if (st != RESHARD_OK) return st;
-  } else if (refit->fork) {
-    st = rs::execute_lanes(refit, src_ptrs, dst_ptrs, stream);
     if (st != RESHARD_OK) return st;
   } else {
     for (int32_t i : refit->reshard_idx) {

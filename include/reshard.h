@@ -454,12 +454,14 @@ typedef enum reshard_route {
 
 /* reshard_refit_create flag: batch the reshard group into one launch. */
 #define RESHARD_REFIT_BATCH 1u
-/* reshard_refit_create flag (excludes RESHARD_REFIT_BATCH): spread the reshard
- * group over RESHARD_REFIT_NUM_LANES side streams of the current device, so that
- * the launches of independent tensors overlap (a launch of a small tensor fills
- * few SMs for a few microseconds, and each launch drains its last CTAs alone).
- * Plans go to the lanes largest first, each to the lane with the fewest bytes so
- * far.  reshard_refit_execute makes the lanes wait for the caller's stream,
+/* reshard_refit_create flag: spread the reshard group over
+ * RESHARD_REFIT_NUM_LANES side streams of the current device, so that the
+ * launches of independent tensors overlap (a launch of a small tensor fills few
+ * SMs for a few microseconds, and each launch drains its last CTAs alone).  The
+ * group is cut into units: one plan each, or, with RESHARD_REFIT_BATCH as well,
+ * the plans that a batch concatenates into one launch form one unit (a batch of
+ * their own) and every other plan is a unit of one.  Units go to the lanes
+ * largest first, each to the lane with the fewest bytes so far.  reshard_refit_execute makes the lanes wait for the caller's stream,
  * launches every plan on its lane and makes the caller's stream wait for every
  * lane before the gather-and-broadcast group, so the call is ordered on the
  * caller's stream like the one-stream form and can be captured into a CUDA graph
@@ -475,7 +477,7 @@ typedef enum reshard_route {
 #define RESHARD_REFIT_LANES 2u
 #define RESHARD_REFIT_NUM_LANES 4
 
-/* Errors: INVALID_ARG (no plans, unknown route or flag, both BATCH and LANES),
+/* Errors: INVALID_ARG (no plans, unknown route or flag),
  * BAD_HANDLE (a plan is not live), UNSUPPORTED (RESHARD_REFIT_BATCH and the
  * reshard group exceeds one batch's buffer table), CUDA (LANES: creating the
  * side streams or events failed), NO_MEMORY. */

@@ -263,9 +263,6 @@ def test_refit_routes_and_host_checks():
     with pytest.raises(rs.ReshardError) as e:
         rs.reshard_refit_create([a], [7])
     assert e.value.status == 1
-    with pytest.raises(rs.ReshardError) as e:          # one batch launch or side streams, not both
-        rs.reshard_refit_create([a, c], batch=True, lanes=True)
-    assert e.value.status == 1
     with pytest.raises(rs.ReshardError) as e:
         rs._check(rs._lib.reshard_refit_create((ctypes.c_void_p * 1)(a.handle), None, 1, 8,
                                                ctypes.byref(ctypes.c_void_p())), "create")

@@ -774,7 +774,7 @@ def test_excluded_ranks_get_null_buffers(oracle, kernel, misalign):
 
 
 # ---------------------------------------------------------------------- whole-model refit
-@pytest.mark.parametrize("mode", ["one_stream", "batch", "lanes"])
+@pytest.mark.parametrize("mode", ["one_stream", "batch", "lanes", "both"])
 @pytest.mark.parametrize("misalign", [0, 2])
 def test_refit_hybrid_routes(oracle, mode, misalign):
     """The reduced MoE model in one reshard_refit_execute: expert weights on the reshard
@@ -799,7 +799,8 @@ def test_refit_hybrid_routes(oracle, mode, misalign):
     routes = [rs.ROUTE_GATHER_BROADCAST if spec.path == "gather_broadcast" else rs.ROUTE_AUTO
               for spec in w.tensors]
     assert rs.ROUTE_GATHER_BROADCAST in routes and rs.ROUTE_AUTO in routes
-    refit = rs.reshard_refit_create(plans, routes, batch=mode == "batch", lanes=mode == "lanes")
+    refit = rs.reshard_refit_create(plans, routes, batch=mode in ("batch", "both"),
+                                    lanes=mode in ("lanes", "both"))
     got_routes, need = rs.reshard_refit_info(refit)
     assert got_routes == [rs.ROUTE_RESHARD if r == rs.ROUTE_AUTO else r for r in routes]
     scratch = Guarded(need, misalign)
@@ -837,15 +838,17 @@ def _check_refit_set(w, wants, keep):
             assert g.guards_intact()
 
 
+@pytest.mark.parametrize("batch", [False, True])
 @pytest.mark.parametrize("misalign", [0, 3])
-def test_refit_lanes_uneven_set(oracle, misalign):
+def test_refit_lanes_uneven_set(oracle, misalign, batch):
     """The 60 reduced uneven-stress tensors (every copy kernel, many tiny launches) in one
-    refit spread over the side streams, executed twice on a non-default stream; every byte
-    of every destination checked against the oracle after each execution."""
+    refit spread over the side streams (with batch, the TMA fan-out plans as one batch unit),
+    executed twice on a non-default stream; every byte of every destination checked against
+    the oracle after each execution."""
     _cuda()
     w = workload(4, reduced=True)
     plans, sptrs, dptrs, wants, keep = _refit_set(oracle, w, misalign)
-    refit = rs.reshard_refit_create(plans, lanes=True)
+    refit = rs.reshard_refit_create(plans, lanes=True, batch=batch)
     s = torch.cuda.Stream()
     for _ in range(2):
         for ds, dd in keep:
