@@ -605,9 +605,14 @@ def ours_arm(args, rank, world, local):
             cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                    "sample": desc, "seconds": round(secs, 2)}
 
-    if batch is not None:
+    # the batch whose classes set the launches: the step's own, or the one a lanes refit
+    # with batching forms its units from
+    count_batch = batch
+    if lanes is not None and not args.no_batch:
+        count_batch = rs.reshard_batch_create([j.plan for j in dom_jobs])
+    if count_batch is not None:
         # one launch per class of the batch (a class of one plan: that plan's launches)
-        _, per = rs.reshard_batch_classes(batch)
+        _, per = rs.reshard_batch_classes(count_batch)
         members = {}
         for j, c in zip(dom_jobs, per):
             if c >= 0:
