@@ -73,6 +73,7 @@ void append_plan(Program& C, const Program& F, int64_t base) {
   C.tile_bytes += F.tile_bytes;
   C.write_bytes += F.write_bytes;
   C.talign_bits |= F.talign_bits;
+  C.tscatter = C.tscatter || F.tscatter;
   C.long_row_bytes += F.long_row_bytes;
   C.wide_row_bytes += F.wide_row_bytes;
 }

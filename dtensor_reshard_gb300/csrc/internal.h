@@ -138,6 +138,7 @@ struct Program {
   // OR of every block's row length and wide offset and every segment's width,
   // column and narrow offset (with the buffers' addresses: the element width)
   uint64_t talign_bits = 0;
+  bool tscatter = false;  // some transpose block scatters (wide source -> narrow destinations)
   const reshard_tblock_t* d_tblocks = nullptr;
   const reshard_tseg_t* d_tsegs = nullptr;
 };

@@ -821,6 +821,7 @@ reshard_status_t build_plan(reshard_plan_s* P) {
       PF.talign_bits |= uint64_t(PF.tsegs[k].width) | PF.tsegs[k].col |
                         uint64_t(PF.tsegs[k].narrow_off);
     const int64_t bytes = int64_t(b.row_bytes) * b.nrows;
+    if (b.direction != 0) PF.tscatter = true;
     S.fanout_read_bytes += bytes;
     if (b.direction == 0) {
       S.fanout_write_bytes += bytes * int64_t(PF.goff[b.wide + 1] - PF.goff[b.wide]);

@@ -38,7 +38,11 @@ namespace {
 constexpr int kTThreads = 256;
 constexpr int kTVecUnroll = 4;  // wide-side 16-byte loads in flight per thread
 constexpr int kImageBytes = int(kTransposeBlockBytes) + 64;
-constexpr int kDynSmem = kImageBytes;
+// DB (programs with scatter blocks): two images, a scatter block's wide rows
+// bulk-loaded into one while the previous scatter block is built from the other.
+// Programs of gather blocks only keep one image (the second one's shared memory
+// was measured to cost them 5-10%).
+template <bool DB> constexpr int dyn_smem() { return DB ? 2 * kImageBytes : kImageBytes; }
 constexpr int kMaxReplicaPtrs = int(kTransposeMaxReplicaPtrs);
 
 struct TransposeParams {
@@ -241,24 +245,58 @@ __device__ __forceinline__ void scatter_direct(const SegInfo* si, int K, uint32_
 // length, columns, widths and narrow addresses (the host takes it from the
 // plan's offsets and the buffers' addresses); a block that does not allow it
 // is skipped and reported in the status word.
-template <int U>
+template <int U, bool DB>
 __global__ void __launch_bounds__(kTThreads, 4)
     reshard_transpose_kernel(const __grid_constant__ TransposeParams p) {
   extern __shared__ __align__(16) unsigned char dyn[];
-  unsigned char* img = dyn;  // wide rows, shifted by the wide address mod 16
+  // wide rows, shifted by the wide address mod 16: gathers build theirs in image 0,
+  // scatter blocks alternate between images 0 and 1
   __shared__ SegInfo si[kTransposeMaxSegs];
   __shared__ unsigned char* ptrs[kMaxReplicaPtrs];
   __shared__ unsigned int s_align;
   __shared__ uint32_t s_ngran;
+  __shared__ __align__(8) uint64_t s_bar[2];  // one bulk load in flight per image
   const bool congruent = (p.flags & kFlagDstCongruent) != 0;
   const int64_t b0 = p.nblocks * int64_t(blockIdx.x) / int64_t(gridDim.x);
   const int64_t b1 = p.nblocks * int64_t(blockIdx.x + 1) / int64_t(gridDim.x);
+  if (DB && threadIdx.x == 0) {
+    staging::mbar_init(&s_bar[0], 1);
+    staging::mbar_init(&s_bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // The wide rows of scatter block b -> image `buf` by one bulk copy of the aligned
+  // 16-byte granules holding them (thread 0; at most kTransposeBlockBytes + 16
+  // bytes, inside the image).
+  auto load_wide = [&](int64_t b, uint32_t buf) {
+    const reshard_tblock_t nb = p.blocks[b];
+    const unsigned char* src = p.bufs[nb.wide] + nb.wide_off;
+    const uint32_t m = uint32_t(reinterpret_cast<uintptr_t>(src) & 15u);
+    const uint32_t bytes = (m + nb.row_bytes * nb.nrows + 15u) & ~15u;
+    staging::mbar_arrive_expect(&s_bar[buf], bytes);
+    staging::bulk_load(dyn + buf * kImageBytes, src - m, bytes, &s_bar[buf]);
+  };
+  // uniform over the CTA: scatter blocks seen, loads issued per image, wait parities
+  uint32_t nscatter = 0, pending = 0, parity = 0;
   for (int64_t bi = b0; bi < b1; ++bi) {
     const reshard_tblock_t blk = p.blocks[bi];
     const uint32_t L = blk.row_bytes, nr = blk.nrows, K = blk.seg_count;
     const uint32_t n = L * nr;
     const bool gather = blk.direction == 0;
-    __syncthreads();  // the previous block is completely done with img/si/ptrs
+    __syncthreads();  // the previous block is completely done with its image, si and ptrs
+    const uint32_t buf = (DB && !gather) ? (nscatter & 1u) : 0u;
+    unsigned char* img = dyn + buf * kImageBytes;
+    if (DB && !gather) {
+      // this block's rows (unless already on their way), then the next scatter
+      // block's into the other image, which the previous block is done with
+      if (!((pending >> buf) & 1u)) {
+        if (threadIdx.x == 0) load_wide(bi, buf);
+        pending |= 1u << buf;
+      }
+      if (bi + 1 < b1 && p.blocks[bi + 1].direction != 0) {
+        if (threadIdx.x == 0) load_wide(bi + 1, buf ^ 1u);
+        pending |= 1u << (buf ^ 1u);
+      }
+    }
     // wide-side pointers: gather -> the destination group in ptrs[0..R); scatter -> source
     int R = 0;
     const unsigned char* wsrc = nullptr;
@@ -297,6 +335,21 @@ __global__ void __launch_bounds__(kTThreads, 4)
       atomicOr(&s_align, a);
     }
     __syncthreads();
+    if (DB && !gather) {
+      // this block's image (every thread polls; the outcome is made uniform)
+      const bool landed = staging::mbar_wait(&s_bar[buf], (parity >> buf) & 1u,
+                                             staging::kWaitPolls);
+      parity ^= 1u << buf;
+      pending &= ~(1u << buf);
+      ++nscatter;
+      if (!__syncthreads_and(landed)) {
+        // give the other image's load, if one is on its way, its own bounded wait
+        if ((pending >> (buf ^ 1u)) & 1u)
+          staging::mbar_wait(&s_bar[buf ^ 1u], (parity >> (buf ^ 1u)) & 1u, staging::kWaitPolls);
+        if (threadIdx.x == 0) atomicExch(p.status, staging::kStatusConsumerWait);
+        return;
+      }
+    }
     if ((s_align & uint32_t(U - 1)) != 0) {
       if (threadIdx.x == 0) atomicExch(p.status, staging::kStatusTransposeAlign);
       continue;  // uniform: every thread read the same s_align
@@ -369,6 +422,9 @@ __global__ void __launch_bounds__(kTThreads, 4)
                  *reinterpret_cast<const uint4*>(img + mis + h + 16 * k));
         for (uint32_t i = h + 16 * m16 + threadIdx.x; i < n; i += kTThreads) d[i] = img[mis + i];
       }
+    } else if constexpr (DB) {
+      // the wide rows arrived by the bulk copy waited for above
+      scatter_direct<U>(si, int(K), ngran, img, mis, L, ptrs);
     } else {
       // wide rows -> image, 16-byte loads from the aligned granules holding them
       const unsigned char* base = wsrc - mis;
@@ -394,11 +450,14 @@ __global__ void __launch_bounds__(kTThreads, 4)
 }
 
 std::mutex g_t_mu;
-std::map<std::pair<int, int>, int> g_t_occ;  // (device, log2 U) -> blocks per SM
+std::map<std::pair<int, int>, int> g_t_occ;  // (device, 2 log2 U + DB) -> blocks per SM
 
 using TransposeFn = void (*)(TransposeParams);
-const TransposeFn kTransposeKernels[4] = {reshard_transpose_kernel<1>, reshard_transpose_kernel<2>,
-                                          reshard_transpose_kernel<4>, reshard_transpose_kernel<8>};
+const TransposeFn kTransposeKernels[2][4] = {
+    {reshard_transpose_kernel<1, false>, reshard_transpose_kernel<2, false>,
+     reshard_transpose_kernel<4, false>, reshard_transpose_kernel<8, false>},
+    {reshard_transpose_kernel<1, true>, reshard_transpose_kernel<2, true>,
+     reshard_transpose_kernel<4, true>, reshard_transpose_kernel<8, true>}};
 
 }  // namespace
 
@@ -415,19 +474,21 @@ reshard_status_t launch_transposes(const reshard_plan_s* plan, const Program& pr
   uint64_t bits = prog.talign_bits | 8u;
   for (int i = 0; i < nbufs; ++i) bits |= uint64_t(reinterpret_cast<uintptr_t>(bufs[i]));
   const int ulog = (bits & 1u) ? 0 : (bits & 2u) ? 1 : (bits & 4u) ? 2 : 3;
-  const void* fn = reinterpret_cast<const void*>(kTransposeKernels[ulog]);
+  const int db = prog.tscatter ? 1 : 0;
+  const int smem = db ? dyn_smem<true>() : dyn_smem<false>();
+  const void* fn = reinterpret_cast<const void*>(kTransposeKernels[db][ulog]);
   int bps = 0;
   {
     std::lock_guard<std::mutex> lk(g_t_mu);
-    auto it = g_t_occ.find({dev, ulog});
+    auto it = g_t_occ.find({dev, 2 * ulog + db});
     if (it == g_t_occ.end()) {
-      ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+      ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (ce == cudaSuccess)
-        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, kTThreads, kDynSmem);
+        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, kTThreads, smem);
       if (ce != cudaSuccess)
         return fail(RESHARD_ERR_CUDA, std::string("transpose kernel set-up: ") + cudaGetErrorString(ce));
       bps = bps > 0 ? bps : 1;
-      g_t_occ[{dev, ulog}] = bps;
+      g_t_occ[{dev, 2 * ulog + db}] = bps;
     } else {
       bps = it->second;
     }
@@ -449,7 +510,7 @@ reshard_status_t launch_transposes(const reshard_plan_s* plan, const Program& pr
   const int64_t max_grid = int64_t(plan->num_sms) * bps;
   const unsigned grid = unsigned(tp.nblocks < max_grid ? tp.nblocks : max_grid);
   void* args[] = {&tp};
-  ce = cudaLaunchKernel(fn, dim3(grid), dim3(kTThreads), args, kDynSmem,
+  ce = cudaLaunchKernel(fn, dim3(grid), dim3(kTThreads), args, size_t(smem),
                         static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(ce));
