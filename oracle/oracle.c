@@ -216,9 +216,16 @@ static int fill_rank(const src_boxes* sb, int32_t ndim, const int64_t* gshape, i
   int64_t i[ORACLE_MAX_NDIM], g[ORACLE_MAX_NDIM], j[ORACLE_MAX_NDIM];
   /* local multi-index of element e_begin */
   int64_t rest = e_begin;
+#if ORACLE_PLANT == 8
+  /* planted mistake: start index unravelled with the first dim fastest */
+  for (int32_t d = 0; d < ndim; ++d) {
+#else
   for (int32_t d = ndim - 1; d >= 0; --d) {
+#endif
     i[d] = dshp[d] ? rest % dshp[d] : 0;
+#if ORACLE_PLANT != 9 /* planted mistake 9: the carry into the outer dims is dropped */
     rest = dshp[d] ? rest / dshp[d] : 0;
+#endif
   }
   for (int64_t e = e_begin; e < e_end; ++e) {
     /* e is the row-major linear index of local multi-index i */

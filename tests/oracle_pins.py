@@ -280,6 +280,56 @@ def pin_source_of(o):
             assert not all(g[d] in set(ix2[d].tolist()) for d in range(nd)), "not first owner"
 
 
+def pin_reshard_elems(o):
+    """A range [e_begin, e_end) of one destination rank: exactly that slice of the
+    torch.chunk-sliced expected shard is written, and nothing outside it.
+
+    Ranges start anywhere (mid-row, mid-plane, at the last element), so the
+    unravel of the start index into a multi-index is exercised, not only e = 0.
+    """
+    rng = random.Random(8)
+    layouts = {nd: [(m, p) for m in tcl.all_meshes(4) for p in tcl.all_placements(len(m), nd)]
+               for nd in (1, 2, 3)}
+    checked = 0
+    while checked < 400:
+        nd = rng.choice((1, 2, 3))
+        gshape = tuple(rng.randint(1, 9) for _ in range(nd))
+        (sm, sp), (dm, dp) = rng.choice(layouts[nd]), rng.choice(layouts[nd])
+        eb = rng.choice((1, 2, 4, 8))
+        glob = _raw_global(gshape, eb, rng.randrange(1 << 30))
+        srcs = [_bytes(tcl.local_shard(glob, sm, sp, r)) for r in range(math.prod(sm))]
+        r = rng.randrange(math.prod(dm))
+        want = _bytes(tcl.local_shard(glob, dm, dp, r))
+        n = want.size // eb
+        if n < 2:
+            continue
+        e0 = rng.randrange(n)
+        e1 = rng.randrange(e0, n + 1)
+        sentinel = np.full(want.size, 0xA5, dtype=np.uint8)
+        out = sentinel.copy()
+        ptrs = [b.ctypes.data if b.size else None for b in srcs]
+        o.reshard_elems(gshape, eb, sm, sp, dm, dp, ptrs, out.ctypes.data, r, e0, e1)
+        assert np.array_equal(out[e0 * eb:e1 * eb], want[e0 * eb:e1 * eb]), \
+            (gshape, sm, sp, dm, dp, r, e0, e1)
+        assert np.array_equal(out[:e0 * eb], sentinel[:e0 * eb]), "wrote before e_begin"
+        assert np.array_equal(out[e1 * eb:], sentinel[e1 * eb:]), "wrote past e_end"
+        checked += 1
+    # splitting a rank into consecutive ranges reproduces the whole shard
+    for gshape, sm, sp, dm, dp in (((9, 7, 5), (2, 2), ("S0", "S2"), (3,), ("S1",)),
+                                   ((7, 8), (4,), ("S1",), (2, 2), ("S0", "R"))):
+        glob = _raw_global(gshape, 2, seed=81)
+        srcs = [_bytes(tcl.local_shard(glob, sm, sp, r)) for r in range(math.prod(sm))]
+        ptrs = [b.ctypes.data if b.size else None for b in srcs]
+        for r in range(math.prod(dm)):
+            want = _bytes(tcl.local_shard(glob, dm, dp, r))
+            out = np.zeros_like(want)
+            n = want.size // 2
+            cuts = sorted({0, n, *(rng.randrange(n + 1) for _ in range(4))})
+            for a, b in zip(cuts, cuts[1:]):
+                o.reshard_elems(gshape, 2, sm, sp, dm, dp, ptrs, out.ctypes.data, r, a, b)
+            assert np.array_equal(out, want), (gshape, r, cuts)
+
+
 PINS = {
     "worked_example": pin_worked_example,
     "resolve_chunk_1d": pin_resolve_chunk_1d,
@@ -290,6 +340,7 @@ PINS = {
     "hybridflow_concat": pin_hybridflow_concat,
     "gather_full": pin_gather_full,
     "source_of": pin_source_of,
+    "reshard_elems": pin_reshard_elems,
 }
 
 

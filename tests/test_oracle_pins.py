@@ -27,6 +27,8 @@ PLANTS = {
     5: "mesh dims applied innermost first",
     6: "empty-shard offset convention skipped",
     7: "outer split offset dropped in nested sharding",
+    8: "range start index unravelled with the first dim fastest",
+    9: "range start index unravel drops the carry into outer dims",
 }
 
 
