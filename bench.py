@@ -28,6 +28,7 @@ import io
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -252,27 +253,42 @@ def launches_of(job, kernel):
 _HOST_SRC = {}
 
 
-def oracle_sample(jobs, seconds):
-    """Time the CPU oracle on a bounded sample of the workload's reshard tensors.
+def host_cpu():
+    """(nproc, CPU model) of this host, for the oracle timing."""
+    nproc = os.cpu_count() or 1
+    try:
+        nproc = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        pass
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                v = line.split(":", 1)[1].strip()
+                if v and not v.isdigit():
+                    model = v
+                    break
+    except Exception:  # noqa: BLE001 - lscpu missing or failing
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return nproc, model or platform.processor() or platform.machine()
 
-    Sample: for every reshard tensor, destination rank 0, chunks of slices of its
-    outermost dim taken in bit-reversed order (so any prefix is spread evenly over
-    the tensor), until the tensor's share of ``seconds`` of CPU time is spent.  Only the source shards a chunk touches
-    are copied to the host (outside the timed calls).
-    Returns (effective GB/s, sample description, cores used, CPU seconds).
-    """
-    import numpy as np
-    import torch
 
-    import oracle as oracle_mod
-
-    o = oracle_mod.load()
-    rjobs = [j for j in jobs if j.spec.path == "reshard"]
-    if not rjobs:
-        return None
-    budget = seconds / len(rjobs)
-    tot_t, tot_b, desc = 0.0, 0.0, []
-    for j in rjobs:
+def _oracle_tasks(o, jobs):
+    """Per reshard tensor: destination rank 0 cut into chunks of about 4 MiB of elements
+    along its outermost dim, in bit-reversed order (any prefix is spread evenly over the
+    tensor), with the source shards each chunk touches."""
+    tensors = []
+    for j in jobs:
         spec = j.spec
         doff, dshp = o.resolve(spec.global_shape, spec.dst_mesh, spec.dst_placements, 0)
         if math.prod(dshp) == 0:
@@ -280,47 +296,118 @@ def oracle_sample(jobs, seconds):
         per = math.prod(dshp[1:])
         chunk = max(1, (4 << 20) // max(1, per))
         nchunks = (dshp[0] + chunk - 1) // chunk
-        # chunk order: bit-reversed, so that every prefix is spread over the whole dim
         bits = max(1, (nchunks - 1).bit_length())
         order = [c for c in (int(format(i, f"0{bits}b")[::-1], 2) for i in range(1 << bits))
                  if c < nchunks]
         sboxes = o.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
-        out = np.empty(math.prod(dshp) * spec.elem_bytes, dtype=np.uint8)
-        t_spent, done, n = 0.0, 0, 0
+        tasks = []
         for ci in order:
-            if t_spent >= budget:
-                break
             first = ci * chunk
             k = min(chunk, dshp[0] - first)
             lo = list(doff)
             hi = [a + b for a, b in zip(doff, dshp)]
             lo[0], hi[0] = doff[0] + first, doff[0] + first + k
-            ptrs = []
-            for s, (so, ss) in enumerate(sboxes):
-                touch = math.prod(ss) and all(
-                    max(a, c) < min(b, c + d) for a, b, c, d in zip(lo, hi, so, ss))
-                if touch:
-                    key = (id(j), s)
-                    if key not in _HOST_SRC:
-                        _HOST_SRC[key] = j.srcs[s].reshape(-1).view(torch.uint8).cpu().numpy()
-                    ptrs.append(_HOST_SRC[key].ctypes.data)
-                else:
-                    ptrs.append(None)
-            t0 = time.perf_counter()
-            o.reshard_elems(spec.global_shape, spec.elem_bytes, spec.src_mesh,
-                            spec.src_placements, spec.dst_mesh, spec.dst_placements, ptrs,
-                            out.ctypes.data, 0, first * per, (first + k) * per)
-            t_spent += time.perf_counter() - t0
-            n += k * per
-            done += k
-        st = j.stats
-        tot_t += t_spent
-        tot_b += n * spec.elem_bytes * (1.0 + st["global_bytes"] / st["dst_bytes"])
-        desc.append(f"{spec.name}: dst rank 0, {done} of {dshp[0]} dim-0 slices spread over "
-                    f"the tensor ({n} elements)")
-    if tot_t == 0:
+            touch = [bool(math.prod(ss)) and all(max(a, c) < min(b, c + d) for a, b, c, d in
+                                                 zip(lo, hi, so, ss)) for so, ss in sboxes]
+            tasks.append((first * per, (first + k) * per, k, touch))
+        tensors.append((j, dshp, tasks))
+    return tensors
+
+
+def _src_ptrs(j, touch):
+    """Host copies of the touched source shards (made outside the timed calls)."""
+    import torch
+    ptrs = []
+    for s, t in enumerate(touch):
+        if not t:
+            ptrs.append(None)
+            continue
+        key = (id(j), s)
+        if key not in _HOST_SRC:
+            _HOST_SRC[key] = j.srcs[s].reshape(-1).view(torch.uint8).cpu().numpy()
+        ptrs.append(_HOST_SRC[key].ctypes.data)
+    return ptrs
+
+
+def oracle_sample(jobs, seconds, threads=None):
+    """Time the CPU oracle on a bounded sample of the workload's reshard tensors.
+
+    Sample: for every reshard tensor, destination rank 0, chunks of slices of its
+    outermost dim in bit-reversed order (spread evenly over the tensor).  First one
+    thread takes chunks until the tensor's share of ``seconds`` is spent; then
+    ``threads`` threads (default: every core of this process) share a larger prefix
+    of the same chunk order -- disjoint element ranges of the rank, each through
+    one oracle call, which runs without the interpreter lock -- sized to take about
+    as long on all cores.  Only the source shards a chunk touches are copied to the
+    host, outside the timed calls.
+    Returns a dict: all-core GB/s, single-thread GB/s, threads used, nproc, CPU
+    model, sample description and CPU seconds; None without reshard tensors.
+    """
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    import oracle as oracle_mod
+
+    o = oracle_mod.load()
+    rjobs = [j for j in jobs if j.spec.path == "reshard"]
+    tensors = _oracle_tasks(o, rjobs)
+    if not tensors:
         return None
-    return tot_b / tot_t / 1e9, "; ".join(desc), 1, tot_t
+    nproc, model = host_cpu()
+    threads = max(1, int(threads or nproc))
+    budget = seconds / len(tensors)
+
+    def run(j, ptrs, out, e0, e1):
+        spec = j.spec
+        o.reshard_elems(spec.global_shape, spec.elem_bytes, spec.src_mesh, spec.src_placements,
+                        spec.dst_mesh, spec.dst_placements, ptrs, out.ctypes.data, 0, e0, e1)
+
+    def bytes_of(j, n):
+        st = j.stats
+        return n * j.spec.elem_bytes * (1.0 + st["global_bytes"] / st["dst_bytes"])
+
+    one_t = one_b = all_t = all_b = cpu_s = 0.0
+    desc = []
+    with cf.ThreadPoolExecutor(max_workers=threads) as pool:
+        for j, dshp, tasks in tensors:
+            out = np.empty(math.prod(dshp) * j.spec.elem_bytes, dtype=np.uint8)
+            # one thread, until the budget is spent
+            t_spent, done, n1 = 0.0, 0, 0
+            for e0, e1, k, touch in tasks:
+                if t_spent >= budget:
+                    break
+                ptrs = _src_ptrs(j, touch)
+                t0 = time.perf_counter()
+                run(j, ptrs, out, e0, e1)
+                t_spent += time.perf_counter() - t0
+                n1 += e1 - e0
+                done += 1
+            one_t += t_spent
+            one_b += bytes_of(j, n1)
+            # all threads, on the first chunks of the same order: about the same wall time
+            m = min(len(tasks), max(threads, done * threads))
+            sub = -(-4 * threads // m)   # at least 4 ranges per thread
+            work = []
+            for e0, e1, _, touch in tasks[:m]:
+                ptrs = _src_ptrs(j, touch)
+                step = -(-(e1 - e0) // sub)
+                work += [(a, min(a + step, e1), ptrs) for a in range(e0, e1, step)]
+            t0 = time.perf_counter()
+            list(pool.map(lambda w: run(j, w[2], out, w[0], w[1]), work))
+            wall = time.perf_counter() - t0
+            nm = sum(e1 - e0 for e0, e1, _ in work)
+            all_t += wall
+            all_b += bytes_of(j, nm)
+            cpu_s += t_spent + wall * threads
+            desc.append(f"{j.spec.name}: dst rank 0, {done} chunks on one thread and {m} on "
+                        f"{threads} threads of {len(tasks)} spread over dim 0 ({n1} / {nm} "
+                        f"elements)")
+    if one_t == 0 or all_t == 0:
+        return None
+    return {"value": all_b / all_t / 1e9, "single_thread": one_b / one_t / 1e9,
+            "cores": threads, "nproc": nproc, "cpu_model": model,
+            "sample": "; ".join(desc), "seconds": cpu_s}
 
 
 # ------------------------------------------------------------------------------ timing
@@ -506,19 +593,24 @@ def reference_arm(args, rank, world):
     per_step = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
     vals = []
     desc = ""
+    res = None
     for i in range(args.warmup + args.steps):
-        v, desc, cores, _ = oracle_sample(jobs, per_step)
+        res = oracle_sample(jobs, per_step)
         if i >= args.warmup:
-            vals.append(v)
+            vals.append(res["value"])
     value = statistics.median(vals)
+    desc = res["sample"]
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic",
         "config": {"workload": w.name, "elements": elem_types(w), "sample": desc},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                         "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": res["cores"],
+                         "kind": "oracle", "sample": desc, "nproc": res["nproc"],
+                         "cpu_model": res["cpu_model"],
+                         "single_thread": {"value": round(res["single_thread"], 4),
+                                           "cores": 1}},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -601,9 +693,10 @@ def ours_arm(args, rank, world, local):
     if rank == 0 and world >= 1 and not args.no_cpu_baseline:
         res = oracle_sample(jobs, args.cpu_seconds)
         if res:
-            v, desc, cores, secs = res
-            cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                   "sample": desc, "seconds": round(secs, 2)}
+            cpu = {"value": round(res["value"], 4), "unit": "GB/s", "cores": res["cores"],
+                   "kind": "oracle", "sample": res["sample"], "nproc": res["nproc"],
+                   "cpu_model": res["cpu_model"], "seconds": round(res["seconds"], 2),
+                   "single_thread": {"value": round(res["single_thread"], 4), "cores": 1}}
 
     # the batch whose classes set the launches: the step's own, or the one a lanes refit
     # with batching forms its units from
@@ -854,10 +947,13 @@ def report(args):
             "gather_broadcast_ms": round(tg, 4),
             "effective_GBps": round((G + D) / t2 / 1e6, 1),
             "fanout_hbm_GBps": round(b2 / t2 / 1e6, 1),
-            "boxcopy_hbm_GBps": round(b1 / t1 / 1e6, 1),
+            # K1 issues 2D bytes (each replica re-reads its source), but L2 serves most
+            # re-reads: its DRAM floor is G + D, so that is what its fraction is taken on
+            "boxcopy_issued_GBps": round(b1 / t1 / 1e6, 1),
+            "boxcopy_min_bytes_GBps": round((G + D) / t1 / 1e6, 1),
             "gb_hbm_GBps": round(bg / tg / 1e6, 1),
             "fanout_roofline_frac": round(b2 / t2 / 1e6 / peak, 4),
-            "boxcopy_roofline_frac": round(b1 / t1 / 1e6 / peak, 4),
+            "boxcopy_roofline_frac": round((G + D) / t1 / 1e6 / peak, 4),
             "min_bytes_roofline_frac": round((G + D) / t2 / 1e6 / peak, 4),
             "hbm_bytes_fanout_vs_gb": round(b2 / bg, 4),
             "payload_vs_pages_2G": round(D / (2 * G), 4),

@@ -16,14 +16,34 @@ from __future__ import annotations
 import ctypes
 import math
 import os
+import re
 from typing import Sequence
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libreshard.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "reshard.h")
 
-MAX_TENSOR_NDIM = 4
-MAX_MESH_NDIM = 4
-MAX_EXEC_BUFFERS = 1024
+
+def header_defines(path: str = HEADER_PATH) -> dict:
+    """Integer macros ``RESHARD_*`` of the library's header, by name.
+
+    Values are plain integers or ``(a << b)`` shifts, with C integer suffixes.
+    """
+    out = {}
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"\s*#define\s+(RESHARD_\w+)\s+\(?\s*(\d+)[uUlL]*"
+                         r"(?:\s*<<\s*(\d+))?\s*\)?", line)
+            if m:
+                v = int(m.group(2))
+                out[m.group(1)] = v << int(m.group(3)) if m.group(3) else v
+    return out
+
+
+_DEFINES = header_defines()
+MAX_TENSOR_NDIM = _DEFINES["RESHARD_MAX_TENSOR_NDIM"]
+MAX_MESH_NDIM = _DEFINES["RESHARD_MAX_MESH_NDIM"]
+MAX_EXEC_BUFFERS = _DEFINES["RESHARD_MAX_EXEC_BUFFERS"]
 
 DTYPES = {"u8": 0, "bf16": 1, "fp16": 2, "fp32": 3, "i32": 4, "fp64": 5, "i64": 6}
 ELEM_BYTES = {"u8": 1, "bf16": 2, "fp16": 2, "fp32": 4, "i32": 4, "fp64": 8, "i64": 8}
@@ -381,9 +401,9 @@ def reshard_batch_destroy(batch: Batch):
 
 
 ROUTE_AUTO, ROUTE_RESHARD, ROUTE_GATHER_BROADCAST = 0, 1, 2
-REFIT_BATCH = 1
-REFIT_LANES = 2
-REFIT_NUM_LANES = 4
+REFIT_BATCH = _DEFINES["RESHARD_REFIT_BATCH"]
+REFIT_LANES = _DEFINES["RESHARD_REFIT_LANES"]
+REFIT_NUM_LANES = _DEFINES["RESHARD_REFIT_NUM_LANES"]
 
 
 class Refit:
@@ -509,8 +529,9 @@ def reshard_selftest_wait_timeout(polls: int = 4096, stream=None):
            "reshard_selftest_wait_timeout")
 
 
-STATIC_SCRATCH_BYTES = 64 << 20
-STATIC_TABLE_BYTES = 1 << 20
+# sizes of the static device arrays behind gather_broadcast_execute_static
+STATIC_SCRATCH_BYTES = _DEFINES["RESHARD_STATIC_SCRATCH_BYTES"]
+STATIC_TABLE_BYTES = _DEFINES["RESHARD_STATIC_TABLE_BYTES"]
 
 
 def reshard_plan_local_shape(plan: Plan, side: int, rank: int):

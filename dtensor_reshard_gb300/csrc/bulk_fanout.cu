@@ -20,8 +20,9 @@
 // engine, without passing through registers.  No multicast is used.
 //
 // Every mbarrier wait is bounded.  A wait that runs out records a code in the
-// device status word, waits (boundedly) for the CTA's own bulk copies and
-// returns, so the context stays usable; reshard_device_status() reads it.
+// device status word, waits (boundedly) for the CTA's own bulk copies -- the
+// loads into its stages as well as its stores -- and returns, so the context
+// stays usable; reshard_device_status() reads it.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -50,9 +51,11 @@ __device__ unsigned int g_device_status;
 // they ask, so CTAs that run fast take more pieces and all finish
 // together.  Every launch takes its own slot {next piece, CTAs finished}; the
 // last CTA of the launch puts the slot back to zero.
-// Slots [0, kStreamSlots) belong to streams, one each; the rest go to launches
-// captured into CUDA graphs, one each, never handed out again (a graph may be
-// replayed on any stream, beside the eager launches of the stream it came from).
+// Slots [0, kStreamSlots) belong to streams, one each at a time (a slot passes to
+// another stream once its last launch has finished, see SlotTable); the rest go
+// to launches captured into CUDA graphs, one each, never handed out again (a
+// graph may be replayed on any stream, beside the eager launches of the stream
+// it came from).
 constexpr int kQueueSlots = 4096;
 constexpr int kStreamSlots = 1024;
 __device__ unsigned int g_queue[kQueueSlots][2];
@@ -134,11 +137,22 @@ __global__ void __launch_bounds__(kStagedThreads)
       const int s = int(n % kStages);
       if (n >= uint32_t(kStages) && !mbar_wait(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls)) {
         if (lane == 0) atomicExch(status, kStatusProducerWait);
-      } else if (lane == 0) {
-        desc[s].ti = -1;
-        mbar_arrive(&full[s]);
+      } else {
+        if (lane == 0) {
+          desc[s].ti = -1;
+          mbar_arrive(&full[s]);
+        }
+        ++n;
       }
     }
+    // wait (boundedly) for the copies still landing in the stages: after a wait
+    // ran out, the consumer may have stopped before reading them, and the CTA
+    // must not exit while bulk copies still write its shared memory.  Each of
+    // the last kStages stages is waited on at the phase of its latest use (on
+    // the normal path those phases have completed and the waits return at once).
+    const uint32_t issued = n;
+    for (uint32_t m = issued > uint32_t(kStages) ? issued - kStages : 0u; m < issued; ++m)
+      mbar_wait(&full[m % kStages], (m / kStages) & 1u, kWaitPolls);
   } else {
     // consumer: stage -> every destination replica
     int cur_tile = -1, R = 0;
@@ -210,12 +224,28 @@ struct DeviceState {
   int blocks_per_sm = 0;
 };
 std::mutex g_dev_mu;
-// per device: the slot of each stream (keyed by handle; the per-thread default
-// stream also by thread) and the next free slot of each kind
+// Per device, the stream slots: which stream holds each one, an event recorded
+// on that stream after the slot's latest launch, and whether a launch is between
+// acquire and release.  A slot changes hands only when its event reports that
+// the slot's last launch has finished (the launch's last CTA has put it back to
+// zero), or, when no slot is idle, after the new stream has been made to wait
+// for that event.  Streams are told apart by their unique ids (a handle can be
+// reused after a stream is destroyed); the per-thread default stream also by
+// thread.
+using StreamKey = std::pair<unsigned long long, std::thread::id>;
+struct StreamSlot {
+  StreamKey key{};
+  bool held = false;         // some stream holds the slot
+  bool busy = false;         // acquired, launch not yet released
+  cudaEvent_t done = nullptr;  // recorded after the slot's latest launch
+  uint64_t last_use = 0;
+};
 struct SlotTable {
-  std::map<std::pair<uintptr_t, std::thread::id>, uint32_t> by_stream;
+  std::map<StreamKey, uint32_t> by_stream;
+  StreamSlot slot[kStreamSlots];
   uint32_t next_stream = 0;
   uint32_t next_captured = kStreamSlots;
+  uint64_t clock = 0;
 };
 std::mutex g_slot_mu;
 DeviceState g_dev[kMaxDevices];
@@ -259,7 +289,7 @@ reshard_status_t device_state(DeviceState* out) {
 
 }  // namespace
 
-reshard_status_t work_queue_slot(void* stream, unsigned int** slot) {
+reshard_status_t work_queue_acquire(void* stream, QueueSlot* q) {
   DeviceState d;
   reshard_status_t st = device_state(&d);
   if (st != RESHARD_OK) return st;
@@ -267,35 +297,103 @@ reshard_status_t work_queue_slot(void* stream, unsigned int** slot) {
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
+  cudaStream_t cs_stream = static_cast<cudaStream_t>(stream);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  ce = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs);
+  ce = cudaStreamIsCapturing(cs_stream, &cs);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(ce));
   std::lock_guard<std::mutex> lk(g_slot_mu);
   SlotTable& t = g_slots[dev];
-  uint32_t idx = 0;
+  q->dev = dev;
   if (cs != cudaStreamCaptureStatusNone) {
     if (t.next_captured >= uint32_t(kQueueSlots))
       return fail(RESHARD_ERR_UNSUPPORTED, "more than " + std::to_string(kQueueSlots - kStreamSlots) +
                                                " work-queue launches captured into CUDA graphs "
                                                "on this device");
-    idx = t.next_captured++;
-  } else {
-    const uintptr_t h = reinterpret_cast<uintptr_t>(stream);
-    const std::thread::id who = stream == static_cast<void*>(cudaStreamPerThread)
-                                    ? std::this_thread::get_id()
-                                    : std::thread::id();
-    auto it = t.by_stream.find({h, who});
-    if (it == t.by_stream.end()) {
-      if (t.next_stream >= uint32_t(kStreamSlots))
-        return fail(RESHARD_ERR_UNSUPPORTED, "work-queue launches on more than " +
-                                                 std::to_string(kStreamSlots) +
-                                                 " streams of this device");
-      it = t.by_stream.emplace(std::make_pair(h, who), t.next_stream++).first;
-    }
-    idx = it->second;
+    q->idx = -1;  // captured: a slot of its own for good, no event
+    q->addr = d.queue + 2 * t.next_captured++;
+    return RESHARD_OK;
   }
-  *slot = d.queue + 2 * idx;
+  unsigned long long id = 0;
+  if (cudaStreamGetId(cs_stream, &id) != cudaSuccess) {
+    cudaGetLastError();  // clear the failed query from the library's runtime
+    id = static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(stream));
+  }
+  const StreamKey key(id, cs_stream == cudaStreamPerThread ? std::this_thread::get_id()
+                                                           : std::thread::id());
+  auto it = t.by_stream.find(key);
+  uint32_t idx = 0;
+  if (it != t.by_stream.end()) {
+    idx = it->second;  // this stream's own slot: its launches run in turn
+  } else {
+    bool wait_for_previous = false;
+    if (t.next_stream < uint32_t(kStreamSlots)) {
+      idx = t.next_stream++;
+    } else {
+      // every slot has been used: take an idle one (its last launch has finished),
+      // the least recently used first; if none is idle, the least recently used
+      // one, after which the new stream waits for its last launch
+      uint32_t order[kStreamSlots];
+      uint32_t nfree = 0;
+      for (uint32_t i = 0; i < uint32_t(kStreamSlots); ++i)
+        if (!t.slot[i].busy) order[nfree++] = i;
+      std::sort(order, order + nfree, [&t](uint32_t a, uint32_t b) {
+        return t.slot[a].last_use < t.slot[b].last_use;
+      });
+      int64_t idle = -1;
+      bool pending = false;
+      for (uint32_t k = 0; k < nfree && idle < 0; ++k) {
+        const StreamSlot& sl = t.slot[order[k]];
+        const cudaError_t q = sl.done ? cudaEventQuery(sl.done) : cudaSuccess;
+        if (q == cudaSuccess) idle = order[k];
+        else pending = true;
+      }
+      // the library's own runtime records cudaErrorNotReady of a pending event
+      // as its last error: clear it, it is not an error
+      if (pending) cudaGetLastError();
+      if (idle >= 0) {
+        idx = uint32_t(idle);
+      } else if (nfree > 0) {
+        idx = order[0];
+        wait_for_previous = true;
+      } else {
+        return fail(RESHARD_ERR_UNSUPPORTED,
+                    "all " + std::to_string(kStreamSlots) +
+                        " work-queue slots of this device are between acquire and launch");
+      }
+      if (t.slot[idx].held) t.by_stream.erase(t.slot[idx].key);
+    }
+    StreamSlot& sl = t.slot[idx];
+    if (wait_for_previous && sl.done) {
+      ce = cudaStreamWaitEvent(cs_stream, sl.done, 0);
+      if (ce != cudaSuccess)
+        return fail(RESHARD_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(ce));
+    }
+    sl.key = key;
+    sl.held = true;
+    t.by_stream.emplace(key, idx);
+  }
+  t.slot[idx].busy = true;
+  q->idx = int(idx);
+  q->addr = d.queue + 2 * idx;
+  return RESHARD_OK;
+}
+
+reshard_status_t work_queue_release(const QueueSlot& q, void* stream, bool launched) {
+  if (q.idx < 0) return RESHARD_OK;
+  std::lock_guard<std::mutex> lk(g_slot_mu);
+  StreamSlot& sl = g_slots[q.dev].slot[q.idx];
+  sl.busy = false;
+  if (!launched) return RESHARD_OK;
+  sl.last_use = ++g_slots[q.dev].clock;
+  cudaError_t ce = cudaSuccess;
+  if (!sl.done) ce = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming);
+  if (ce == cudaSuccess) ce = cudaEventRecord(sl.done, static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) {
+    // without a record the slot can no longer be shown idle: keep it with its stream
+    sl.busy = true;
+    return fail(RESHARD_ERR_CUDA, std::string("work-queue event: ") + cudaGetErrorString(ce));
+  }
   return RESHARD_OK;
 }
 
@@ -338,18 +436,20 @@ reshard_status_t launch_fanout_staged(const reshard_plan_s* plan, const KernelPa
   const unsigned grid = unsigned(kp.total_units < max_grid ? kp.total_units : max_grid);
   KernelParams params = kp;
   unsigned int* status = d.status;
-  unsigned int* queue = nullptr;
-  st = work_queue_slot(stream, &queue);
+  QueueSlot slot;
+  st = work_queue_acquire(stream, &slot);
   if (st != RESHARD_OK) return st;
+  unsigned int* queue = slot.addr;
   PieceSchedule sched = work_queue_schedule(kp.total_units, prog.tile_bytes, prog.write_bytes,
                                             grid, 0);
   void* args[] = {&params, &status, &queue, &sched};
   cudaError_t ce = cudaLaunchKernel(reinterpret_cast<const void*>(fanout_staged_kernel),
                                     dim3(grid), dim3(kStagedThreads), args,
                                     kStages * kStageBytes, static_cast<cudaStream_t>(stream));
+  st = work_queue_release(slot, stream, ce == cudaSuccess);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(ce));
-  return RESHARD_OK;
+  return st;
 }
 
 }  // namespace rs

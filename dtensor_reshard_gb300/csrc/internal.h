@@ -187,6 +187,10 @@ reshard_status_t upload_plan(reshard_plan_s* plan);
 reshard_status_t buffer_table(reshard_plan_s* plan, const void* const* src_ptrs,
                               void* const* dst_ptrs, void* scratch,
                               std::vector<unsigned char*>* bufs);
+// The same checks, into a caller-owned array of `capacity` entries (no heap use).
+reshard_status_t buffer_table(reshard_plan_s* plan, const void* const* src_ptrs,
+                              void* const* dst_ptrs, void* scratch, unsigned char** out,
+                              int64_t capacity);
 bool plan_live(const reshard_plan_s* plan);
 
 // Error reporting (thread-local message).
@@ -224,10 +228,20 @@ reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, cons
                                        void* stream);
 // A work-queue slot {next piece, CTAs finished} of the current device for one
 // launch on `stream`; the launch's last CTA puts it back to zero.  Launches on one
-// stream run in turn and share the stream's slot; a launch being captured into a
-// CUDA graph gets a slot of its own for good (bulk_fanout.cu).  UNSUPPORTED when
-// a device's slots for streams or for captured launches run out.
-reshard_status_t work_queue_slot(void* stream, unsigned int** slot);
+// stream run in turn and share the stream's slot; a slot passes to another stream
+// once its last launch has finished (an event recorded at release tells), or, when
+// no slot is idle, the new stream first waits for the least recently used slot's
+// last launch.  A launch being captured into a CUDA graph gets a slot of its own
+// for good (bulk_fanout.cu); UNSUPPORTED when a device's slots for captured
+// launches run out.  Every acquire is followed by one release after the launch
+// (launched = whether the launch was enqueued).
+struct QueueSlot {
+  unsigned int* addr = nullptr;
+  int dev = -1;
+  int idx = -1;  // stream slot index, -1 for a captured launch
+};
+reshard_status_t work_queue_acquire(void* stream, QueueSlot* slot);
+reshard_status_t work_queue_release(const QueueSlot& slot, void* stream, bool launched);
 // The pieces a work queue hands out, in order: pieces of `big` units up to unit
 // `split` (a multiple of big), then pieces of `small` units up to `total`, so
 // that the last pieces taken are short and the CTAs of a launch finish close

@@ -601,6 +601,10 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
                                        const int64_t* d_prefix, const uint32_t* d_goff,
                                        const uint16_t* d_gbuf, int num_sms,
                                        unsigned char* const* bufs, int nbufs, void* stream) {
+  // tables at explicit addresses carry tiles only: a program with transpose
+  // blocks would leave the regions those blocks cover unwritten
+  if (!prog.tblocks.empty())
+    return fail(RESHARD_ERR_UNSUPPORTED, "program with transpose blocks at explicit table addresses");
   const int64_t total = prog.total_units();
   if (total == 0) return RESHARD_OK;
   if (nbufs > RESHARD_MAX_EXEC_BUFFERS) return fail(RESHARD_ERR_UNSUPPORTED, "too many buffers");

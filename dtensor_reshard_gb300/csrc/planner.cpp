@@ -1173,34 +1173,37 @@ reshard_status_t upload_plan(reshard_plan_s* plan) {
 
 namespace rs {
 
-// Build the buffer table [src..., dst..., scratch] and check null pointers.
+// Build the buffer table [src..., dst..., scratch] into out[M + N + 1] and check
+// null pointers (a NULL pointer is accepted for an empty shard and for a rank an
+// excluded plan leaves out) and, for in-place plans, the source aliases.
 reshard_status_t buffer_table(reshard_plan_t plan, const void* const* src_ptrs,
-                              void* const* dst_ptrs, void* scratch, std::vector<unsigned char*>* bufs) {
+                              void* const* dst_ptrs, void* scratch, unsigned char** out,
+                              int64_t capacity) {
   const int64_t M = plan->src.nranks, N = plan->dst.nranks;
-  if (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS)
+  if (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS || M + N + 1 > capacity)
     return fail(RESHARD_ERR_UNSUPPORTED, "M + N + 1 exceeds RESHARD_MAX_EXEC_BUFFERS");
   if (!src_ptrs || !dst_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "null pointer array");
-  bufs->resize(size_t(M + N + 1));
+  unsigned char** const b = out;
   for (int64_t r = 0; r < M; ++r) {
     if (!src_ptrs[r] && rs::box_volume(plan->ndim, plan->src.box[size_t(r)]) > 0 &&
         (plan->src_gone.empty() || !plan->src_gone[size_t(r)]))
       return fail(RESHARD_ERR_INVALID_ARG, "NULL source pointer for a non-empty shard (rank " +
                                                std::to_string(r) + ")");
-    (*bufs)[size_t(r)] = static_cast<unsigned char*>(const_cast<void*>(src_ptrs[r]));
+    b[r] = static_cast<unsigned char*>(const_cast<void*>(src_ptrs[r]));
   }
   for (int64_t r = 0; r < N; ++r) {
     if (!dst_ptrs[r] && rs::box_volume(plan->ndim, plan->dst.box[size_t(r)]) > 0 &&
         (plan->dst_gone.empty() || !plan->dst_gone[size_t(r)]))
       return fail(RESHARD_ERR_INVALID_ARG, "NULL destination pointer for a non-empty shard (rank " +
                                                std::to_string(r) + ")");
-    (*bufs)[size_t(M + r)] = static_cast<unsigned char*>(dst_ptrs[r]);
+    b[M + r] = static_cast<unsigned char*>(dst_ptrs[r]);
   }
-  (*bufs)[size_t(M + N)] = static_cast<unsigned char*>(scratch);
+  b[M + N] = static_cast<unsigned char*>(scratch);
   if (plan->inplace) {
     for (int64_t r = 0; r < M; ++r) {
       const int64_t d = plan->alias_dst[size_t(r)];
       if (d < 0) continue;
-      if ((*bufs)[size_t(r)] != (*bufs)[size_t(M + d)] + plan->alias_off[size_t(r)])
+      if (b[r] != b[M + d] + plan->alias_off[size_t(r)])
         return fail(RESHARD_ERR_INVALID_ARG,
                     "in-place plan: source rank " + std::to_string(r) +
                         " must point into destination rank " + std::to_string(d) +
@@ -1208,6 +1211,15 @@ reshard_status_t buffer_table(reshard_plan_t plan, const void* const* src_ptrs,
     }
   }
   return RESHARD_OK;
+}
+
+reshard_status_t buffer_table(reshard_plan_t plan, const void* const* src_ptrs,
+                              void* const* dst_ptrs, void* scratch, std::vector<unsigned char*>* bufs) {
+  const int64_t n = plan->src.nranks + plan->dst.nranks + 1;
+  if (n > RESHARD_MAX_EXEC_BUFFERS)
+    return fail(RESHARD_ERR_UNSUPPORTED, "M + N + 1 exceeds RESHARD_MAX_EXEC_BUFFERS");
+  bufs->resize(size_t(n));
+  return buffer_table(plan, src_ptrs, dst_ptrs, scratch, bufs->data(), n);
 }
 
 }  // namespace rs

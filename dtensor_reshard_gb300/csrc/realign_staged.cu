@@ -436,9 +436,10 @@ reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, cons
   const int64_t max_grid = int64_t(num_sms) * bps;
   const unsigned grid = unsigned(kp.total_units < max_grid ? kp.total_units : max_grid);
   KernelParams params = kp;
-  unsigned int* queue = nullptr;
-  st = work_queue_slot(stream, &queue);
+  QueueSlot slot;
+  st = work_queue_acquire(stream, &slot);
   if (st != RESHARD_OK) return st;
+  unsigned int* queue = slot.addr;
   // pieces of at least 16 KiB: tiny ones cost more in grabs and short chunks
   // than they gain in balance (measured on the small uneven-stress tensors)
   PieceSchedule sched = work_queue_schedule(kp.total_units, prog.tile_bytes, prog.write_bytes, grid,
@@ -452,9 +453,10 @@ reshard_status_t launch_realign_staged(int num_sms, const KernelParams& kp, cons
     ce = cudaLaunchKernel(reinterpret_cast<const void*>(realign_staged_kernel<false>), dim3(grid),
                           dim3(Config<false>::kThreads), args, Config<false>::kDynSmem,
                           static_cast<cudaStream_t>(stream));
+  st = work_queue_release(slot, stream, ce == cudaSuccess);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(ce));
-  return RESHARD_OK;
+  return st;
 }
 
 }  // namespace rs

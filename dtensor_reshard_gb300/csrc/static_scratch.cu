@@ -104,9 +104,8 @@ extern "C" reshard_status_t gather_broadcast_execute_static(reshard_plan_t plan,
                                                             const void* const* src_ptrs,
                                                             void* const* dst_ptrs, void* stream) {
   rs::TraceRange trace("gb.exec_static");
-  reshard_stats_t st;
-  if (reshard_plan_stats(plan, &st) != RESHARD_OK)
-    return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  if (!rs::plan_live(plan)) return fail(RESHARD_ERR_BAD_HANDLE, "invalid plan handle");
+  const reshard_stats_t& st = plan->stats;
   if (uint64_t(st.global_bytes) > RESHARD_STATIC_SCRATCH_BYTES)
     return fail(RESHARD_ERR_UNSUPPORTED,
                 "global tensor of " + std::to_string(st.global_bytes) +
@@ -123,37 +122,22 @@ extern "C" reshard_status_t gather_broadcast_execute_static(reshard_plan_t plan,
                     " bytes exceed the static table array of " +
                     std::to_string(uint64_t(RESHARD_STATIC_TABLE_BYTES)) + " bytes");
 
-  // buffer table [sources..., destinations..., scratch]
-  const int64_t M = plan->src.nranks, N = plan->dst.nranks;
-  if (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS)
-    return fail(RESHARD_ERR_UNSUPPORTED, "M + N + 1 exceeds RESHARD_MAX_EXEC_BUFFERS");
-  if (!src_ptrs || !dst_ptrs) return fail(RESHARD_ERR_INVALID_ARG, "null pointer array");
+  // buffer table [sources..., destinations..., scratch], with the same pointer
+  // checks as every other execution (NULL for empty shards and for ranks an
+  // excluded plan leaves out; source aliases of in-place plans); the scratch
+  // slot is filled in below once the static array's address is known
   unsigned char* bufs[RESHARD_MAX_EXEC_BUFFERS];
-  for (int64_t r = 0; r < M; ++r) {
-    int64_t shp[RESHARD_MAX_TENSOR_NDIM];
-    reshard_plan_local_shape(plan, 0, r, shp, nullptr);
-    int64_t vol = 1;
-    for (int d = 0; d < plan->ndim; ++d) vol *= shp[d];
-    if (!src_ptrs[r] && vol > 0)
-      return fail(RESHARD_ERR_INVALID_ARG, "NULL source pointer for a non-empty shard");
-    bufs[r] = static_cast<unsigned char*>(const_cast<void*>(src_ptrs[r]));
-  }
-  for (int64_t r = 0; r < N; ++r) {
-    int64_t shp[RESHARD_MAX_TENSOR_NDIM];
-    reshard_plan_local_shape(plan, 1, r, shp, nullptr);
-    int64_t vol = 1;
-    for (int d = 0; d < plan->ndim; ++d) vol *= shp[d];
-    if (!dst_ptrs[r] && vol > 0)
-      return fail(RESHARD_ERR_INVALID_ARG, "NULL destination pointer for a non-empty shard");
-    bufs[M + r] = static_cast<unsigned char*>(dst_ptrs[r]);
-  }
+  reshard_status_t rc =
+      rs::buffer_table(plan, src_ptrs, dst_ptrs, nullptr, bufs, RESHARD_MAX_EXEC_BUFFERS);
+  if (rc != RESHARD_OK) return rc;
+  const int64_t M = plan->src.nranks, N = plan->dst.nranks;
 
   int dev = -1;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
   rs::StaticArrays arr;
-  reshard_status_t rc = rs::static_arrays(dev, &arr);
+  rc = rs::static_arrays(dev, &arr);
   if (rc != RESHARD_OK) return rc;
   bufs[M + N] = arr.scratch;
   const int nbufs = int(M + N + 1);

@@ -289,9 +289,12 @@ reshard_status_t reshard_plan_upload(reshard_plan_t plan);
  * execution has run on the device, executions can be recorded into a CUDA graph
  * by stream capture and replayed; the graph keeps the buffer addresses.
  * Errors: BAD_HANDLE, INVALID_ARG (null pointer for a non-empty shard),
- * UNSUPPORTED (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS, or the device's work-queue
- * slots are used up: one per stream for 1024 streams, one per launch captured
- * into a CUDA graph for 3072 captured launches), CUDA (launch failed).
+ * UNSUPPORTED (M + N + 1 > RESHARD_MAX_EXEC_BUFFERS, or the device's 3072
+ * work-queue slots for launches captured into CUDA graphs are used up: each
+ * captured launch keeps one for good), CUDA (launch failed).  Eager executions
+ * on any number of streams are supported: the 1024 per-stream slots pass from a
+ * stream to another once the slot's last launch has finished (when none has, the
+ * new stream first waits for the least recently used slot's last launch).
  */
 reshard_status_t reshard_execute(reshard_plan_t plan, const void* const* src_ptrs,
                                  void* const* dst_ptrs, void* stream);
@@ -364,8 +367,7 @@ reshard_status_t reshard_selftest_wait_timeout(uint32_t polls, void* stream);
  * The first call on a device looks up the arrays' device addresses
  * (cudaGetSymbolAddress) with that device current; make that first call before
  * any stream capture.  Each call copies the plan's tables from host memory into
- * the static array with cudaMemcpyAsync on `stream` (pageable source, so the
- * call waits until earlier work on `stream` has finished) and then launches the
+ * the static array with cudaMemcpyAsync on `stream` and then launches the
  * gather and slice kernels on `stream`.  No part of the arrays needs to start at
  * zero: the gather writes every byte of the global tensor before the slice reads
  * it, and the tables are rewritten by every call.
@@ -373,8 +375,12 @@ reshard_status_t reshard_selftest_wait_timeout(uint32_t polls, void* stream);
  * All calls share the arrays and each call overwrites the previous contents:
  * calls that can overlap on the GPU (different streams without ordering between
  * them, or several host threads) race and produce wrong results.  Calls on one
- * stream are ordered and safe.  No cudaMalloc, cudaFree or other allocating
- * library routine is called.
+ * stream are safe because the stream orders each call's table copy after the
+ * previous call's kernels.  No cudaMalloc, cudaFree or other allocating library
+ * routine is called.  The pointers are checked as for every other execution: a
+ * NULL pointer is accepted for an empty shard and for a rank that an excluded
+ * plan (reshard_plan_exclude) leaves out, and in-place plans must pass aliased
+ * source pointers.
  *
  * Errors: as gather_broadcast_execute, plus UNSUPPORTED when the global tensor
  * exceeds RESHARD_STATIC_SCRATCH_BYTES or the gather + slice tables exceed

@@ -292,3 +292,77 @@ def test_refit_batch_limit_is_reported():
         rs.reshard_refit_create(big, batch=True)
     assert e.value.status == 2
     rs.reshard_refit_create(big, batch=False)
+
+
+def test_binding_constants_come_from_the_header():
+    """The binding's sizes are the header's (no hand copies that could drift)."""
+    text = open(HEADER).read()
+
+    def define(name):
+        m = re.search(r"#define\s+" + name + r"\s+\(?(\d+)[uUlL]*(?:\s*<<\s*(\d+))?", text)
+        assert m, name
+        return int(m.group(1)) << int(m.group(2) or 0)
+    assert rs.STATIC_SCRATCH_BYTES == define("RESHARD_STATIC_SCRATCH_BYTES") == 64 << 20
+    assert rs.STATIC_TABLE_BYTES == define("RESHARD_STATIC_TABLE_BYTES") == 1 << 20
+    assert rs.MAX_EXEC_BUFFERS == define("RESHARD_MAX_EXEC_BUFFERS")
+    assert rs.MAX_TENSOR_NDIM == define("RESHARD_MAX_TENSOR_NDIM")
+    assert rs.MAX_MESH_NDIM == define("RESHARD_MAX_MESH_NDIM")
+    assert rs.REFIT_NUM_LANES == define("RESHARD_REFIT_NUM_LANES")
+
+
+def _static_table_bytes(plan):
+    """Bytes the gather and slice tables take in the static table array (256-byte slots)."""
+    def a256(x):
+        return (x + 255) // 256 * 256
+    end = 0
+    for prog in (rs.PROGRAM_GATHER, rs.PROGRAM_SLICE):
+        tiles, prefix, goff, gbuf = rs.reshard_plan_program(plan, prog)
+        p = a256(end + 64 * len(tiles))
+        g = a256(p + 8 * len(prefix))
+        b = a256(g + 4 * len(goff))
+        end = a256(b + 2 * len(gbuf))
+    return end
+
+
+def test_static_entry_point_host_checks():
+    """Every rejection of gather_broadcast_execute_static happens before device work."""
+    # a 4-D tensor whose gather needs one tile per outermost index: 1.1 MiB of tables
+    # for a 0.5 MiB tensor
+    p = rs.reshard_plan_create((2048, 4, 4, 4), "fp32", (2, 2, 2), ("S1", "S2", "S3"),
+                               (2,), ("S0",))
+    assert rs.reshard_plan_stats(p)["global_bytes"] <= rs.STATIC_SCRATCH_BYTES
+    assert _static_table_bytes(p) > rs.STATIC_TABLE_BYTES
+    srcs = (ctypes.c_void_p * 8)(*([0x1000] * 8))
+    dsts = (ctypes.c_void_p * 2)(0x2000, 0x3000)
+    assert rs._lib.gather_broadcast_execute_static(p, srcs, dsts, None) == 2
+    assert "static table" in rs.reshard_last_error()
+    # half the outer extent fits
+    q = rs.reshard_plan_create((1024, 4, 4, 4), "fp32", (2, 2, 2), ("S1", "S2", "S3"),
+                               (2,), ("S0",))
+    assert _static_table_bytes(q) <= rs.STATIC_TABLE_BYTES
+    # the global tensor above the scratch
+    rows = rs.STATIC_SCRATCH_BYTES // (2 * 4096) + 1
+    big = rs.reshard_plan_create((rows, 4096), "bf16", (2,), ("S0",), (2,), ("S1",))
+    two = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    assert rs._lib.gather_broadcast_execute_static(big, two, two, None) == 2
+    assert "static scratch" in rs.reshard_last_error()
+    # pointer checks are the library's own: NULL for a non-empty shard, bad handle
+    w = rs.reshard_plan_create((8, 8), "bf16", (2,), ("S0",), (4,), ("S1",))
+    nul = (ctypes.c_void_p * 2)(None, 0x1000)
+    four = (ctypes.c_void_p * 4)(0x2000, 0x3000, 0x4000, 0x5000)
+    assert rs._lib.gather_broadcast_execute_static(w, nul, four, None) == 1
+    assert "source" in rs.reshard_last_error()
+    assert rs._lib.gather_broadcast_execute_static(w, None, four, None) == 1
+    assert rs._lib.gather_broadcast_execute_static(None, two, four, None) == 6
+
+
+def test_static_entry_point_checks_inplace_aliases():
+    """An in-place plan's source pointers must alias the destinations, as elsewhere."""
+    # generation rank 4t+d holds training shards 4t..4t+3; training shard s lives in rank s
+    p = rs.reshard_plan_create_inplace((64, 16), "fp32", (8,), ("S0",), (2, 4), ("S0", "R"),
+                                       src_alias=list(range(8)))
+    n_src, n_dst = p.n_src, p.n_dst
+    srcs = (ctypes.c_void_p * n_src)(*[0x10000 * (i + 1) for i in range(n_src)])
+    dsts = (ctypes.c_void_p * n_dst)(*[0x1000000 * (i + 1) for i in range(n_dst)])
+    assert rs._lib.gather_broadcast_execute_static(p, srcs, dsts, None) == 1
+    assert "in-place" in rs.reshard_last_error()

@@ -646,6 +646,95 @@ def test_streams_and_graph_replay_beside_eager_launches(oracle):
     check([0, 3])
 
 
+def _driver_streams():
+    """cuStreamCreate / cuStreamDestroy from the driver library: torch.cuda.Stream() hands
+    out streams from a small pool, and these tests need genuinely new streams."""
+    import ctypes
+    lib = ctypes.CDLL("libcuda.so.1")
+    lib.cuStreamCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
+    lib.cuStreamCreate.restype = ctypes.c_int
+    lib.cuStreamDestroy_v2.argtypes = [ctypes.c_void_p]
+    lib.cuStreamDestroy_v2.restype = ctypes.c_int
+
+    def create():
+        h = ctypes.c_void_p()
+        assert lib.cuStreamCreate(ctypes.byref(h), 1) == 0   # CU_STREAM_NON_BLOCKING
+        return h.value
+
+    def destroy(h):
+        assert lib.cuStreamDestroy_v2(h) == 0
+    return create, destroy
+
+
+def test_work_queue_slots_pass_between_streams(oracle):
+    """More streams than the device has work-queue slots (1024): 1500 streams created,
+    used once and destroyed one after another, then 1100 live streams whose launches all
+    wait behind one long kernel, so that no slot is idle when the later streams ask for
+    one.  Every launch writes its own destinations, and each is exact."""
+    dev = _cuda()
+    specs = [_spec((64, 32, 96), "fp32", (2, 2), ("S0", "S2"), (4,), ("S1",), seed=14),
+             _spec((600, 1001), "bf16", (3,), ("S0",), (2,), ("S1",), seed=15)]
+    cases = []
+    for spec, path in zip(specs, ("tma_fanout", "staged")):
+        glob = global_tensor(spec)
+        boxes = oracle.boxes(spec.global_shape, spec.src_mesh, spec.src_placements)
+        host = [helpers.slice_box(glob, o, sh) for o, sh in boxes]
+        want = helpers.expected_dst(oracle, spec, [helpers.to_bytes(h) for h in host])
+        srcs = [h.to(dev) for h in host]
+        plan = helpers.spec_plan(spec)
+        wants = [torch.from_numpy(w).to(dev) for w in want]
+
+        def new_dsts(wants=wants):
+            return [torch.full_like(w, FILL_BYTE) for w in wants]
+        assert rs.reshard_plan_path(plan, srcs, new_dsts())[0] == path, spec.name
+        cases.append((plan, srcs, wants, new_dsts))
+    create, destroy = _driver_streams()
+
+    # streams created and destroyed one after another; each checks its own launches
+    bad = torch.zeros((), dtype=torch.int64, device=dev)
+    dsts = [c[3]() for c in cases]
+    for k in range(1500):
+        h = create()
+        st = torch.cuda.ExternalStream(h)
+        st.wait_stream(torch.cuda.current_stream())   # one stream after the other
+        with torch.cuda.stream(st):
+            for (plan, srcs, wants, _), d in zip(cases, dsts):
+                for t in d:
+                    t.fill_(FILL_BYTE)
+                rs.reshard_execute(plan, srcs, d, st)
+                for t, w in zip(d, wants):
+                    bad += (t != w).sum()
+        torch.cuda.current_stream().wait_stream(st)
+        destroy(h)
+    torch.cuda.synchronize()
+    assert int(bad) == 0
+    assert rs.reshard_device_status() == 0
+
+    # live streams beyond the slot count, all held back behind one long kernel
+    plan, srcs, wants, new_dsts = cases[0]
+    outs = [new_dsts() for _ in range(1100)]
+    torch.cuda.synchronize()
+    gate = torch.cuda.Stream()
+    with torch.cuda.stream(gate):
+        torch.cuda._sleep(1_000_000_000)          # about half a second of one SM
+    opened = torch.cuda.Event()
+    opened.record(gate)
+    handles = []
+    for d in outs:
+        h = create()
+        st = torch.cuda.ExternalStream(h)
+        st.wait_event(opened)
+        rs.reshard_execute(plan, srcs, d, st)
+        handles.append(h)
+    torch.cuda.synchronize()
+    for k, d in enumerate(outs):
+        for t, w in zip(d, wants):
+            assert torch.equal(t, w), f"stream {k}"
+    for h in handles:
+        destroy(h)
+    assert rs.reshard_device_status() == 0
+
+
 # ---------------------------------------------------------------------- transpose blocks
 TRANSPOSE_CASES = [
     _spec((74, 65, 1721), "fp16", (61,), ("S2",), (3,), ("R",), seed=1),        # gather, R=3

@@ -95,6 +95,12 @@ def test_transpose_rule_for_narrow_pieces(oracle, case, transposed):
     plan = _check_spec(oracle, spec)
     blocks, _ = rs.reshard_plan_transposes(plan, rs.PROGRAM_FANOUT)
     assert bool(blocks) == transposed
+    # transpose blocks are a fan-out device only: the box-copy, gather, slice and
+    # replicate programs (which the allocation-free entry point runs from tables at
+    # explicit addresses) stay tiles alone
+    for prog in (rs.PROGRAM_BOXCOPY, rs.PROGRAM_GATHER, rs.PROGRAM_SLICE, rs.PROGRAM_REPLICATE):
+        blocks, segs = rs.reshard_plan_transposes(plan, prog)
+        assert not blocks and not segs, prog
 
 
 @pytest.mark.parametrize("case,assembled", [
