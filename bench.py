@@ -75,8 +75,9 @@ def parse_args(argv=None):
                     help="experts of the MoE workload (smaller for profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="target CPU time of the oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of each leg (one thread, all cores) of the oracle "
+                         "sample")
     ap.add_argument("--report", default=None,
                     help="write a per-workload table (JSON lines) to this file")
     args = ap.parse_args(argv)
@@ -335,10 +336,9 @@ def oracle_sample(jobs, seconds, threads=None):
     Sample: for every reshard tensor, destination rank 0, chunks of slices of its
     outermost dim in bit-reversed order (spread evenly over the tensor).  First one
     thread takes chunks until the tensor's share of ``seconds`` is spent; then
-    ``threads`` threads (default: every core of this process) share a larger prefix
-    of the same chunk order -- disjoint element ranges of the rank, each through
-    one oracle call, which runs without the interpreter lock -- sized to take about
-    as long on all cores.  Only the source shards a chunk touches are copied to the
+    ``threads`` threads (default: every core of this process) share the same chunks,
+    cut into disjoint element ranges of the rank, each through one oracle call
+    (which runs without the interpreter lock).  Only the source shards a chunk touches are copied to the
     host, outside the timed calls.
     Returns a dict: all-core GB/s, single-thread GB/s, threads used, nproc, CPU
     model, sample description and CPU seconds; None without reshard tensors.
@@ -385,8 +385,8 @@ def oracle_sample(jobs, seconds, threads=None):
                 done += 1
             one_t += t_spent
             one_b += bytes_of(j, n1)
-            # all threads, on the first chunks of the same order: about the same wall time
-            m = min(len(tasks), max(threads, done * threads))
+            # all threads, on the same chunks: about the same CPU time, 1/threads the wall
+            m = max(1, done)
             sub = -(-4 * threads // m)   # at least 4 ranges per thread
             work = []
             for e0, e1, _, touch in tasks[:m]:

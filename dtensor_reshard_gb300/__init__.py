@@ -115,6 +115,28 @@ class reshard_tseg_t(ctypes.Structure):
 assert ctypes.sizeof(reshard_tblock_t) == 32 and ctypes.sizeof(reshard_tseg_t) == 24
 
 
+class reshard_xfer_t(ctypes.Structure):
+    _fields_ = [("chunk", ctypes.c_int32), ("stage", ctypes.c_int32), ("peer", ctypes.c_int32),
+                ("dir", ctypes.c_int32), ("offset", ctypes.c_int64), ("bytes", ctypes.c_int64)]
+
+
+class reshard_partition_gpu_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "send_bytes", "recv_bytes", "local_bytes", "sent_inter_bytes", "sent_intra_bytes",
+        "recv_inter_bytes", "recv_intra_bytes", "n_xfers")]
+
+
+class reshard_partition_stats_t(ctypes.Structure):
+    _fields_ = ([(n, ctypes.c_int32) for n in ("ngpus", "ndomains", "nchunks", "nslots")] +
+                [(n, ctypes.c_int64) for n in (
+                    "local_bytes", "inter_domain_bytes", "intra_domain_bytes",
+                    "max_gpu_send_bytes", "max_gpu_recv_bytes", "n_pieces", "n_messages",
+                    "planner_ns")])
+
+
+assert ctypes.sizeof(reshard_xfer_t) == 32
+
+
 class ReshardError(RuntimeError):
     def __init__(self, status: int, where: str, msg: str):
         super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}")
@@ -181,6 +203,25 @@ def _load():
                                      ctypes.POINTER(ctypes.POINTER(reshard_tseg_t)), i64p],
                                     ctypes.c_int),
         "reshard_plan_destroy": ([vp], ctypes.c_int),
+        "reshard_partition_create": ([vp, ctypes.POINTER(ctypes.c_int32),
+                                      ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                      ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, vpp],
+                                     ctypes.c_int),
+        "reshard_partition_stats": ([vp, ctypes.POINTER(reshard_partition_stats_t)], ctypes.c_int),
+        "reshard_partition_gpu": ([vp, ctypes.c_int32, ctypes.POINTER(reshard_partition_gpu_t)],
+                                  ctypes.c_int),
+        "reshard_partition_transfers": ([vp, ctypes.c_int32,
+                                         ctypes.POINTER(ctypes.POINTER(reshard_xfer_t)), i64p],
+                                        ctypes.c_int),
+        "reshard_partition_program": ([vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.POINTER(ctypes.POINTER(reshard_tile_t)), i64p,
+                                       ctypes.POINTER(i64p),
+                                       ctypes.POINTER(ctypes.POINTER(ctypes.c_uint32)),
+                                       ctypes.POINTER(ctypes.POINTER(ctypes.c_uint16)), i64p],
+                                      ctypes.c_int),
+        "reshard_partition_execute": ([vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vpp,
+                                       vpp, vp, vp, vp], ctypes.c_int),
+        "reshard_partition_destroy": ([vp], ctypes.c_int),
         "reshard_last_error": ([], ctypes.c_char_p),
         "reshard_version": ([], ctypes.c_char_p),
     }
@@ -594,3 +635,164 @@ def reshard_plan_destroy(plan: Plan):
     st = _lib.reshard_plan_destroy(plan)
     plan.handle = None
     _check(st, "reshard_plan_destroy")
+
+
+# ------------------------------------------------------------------ multi-GPU partition
+STEP_LOCAL, STEP_PACK, STEP_FORWARD, STEP_UNPACK = 0, 1, 2, 3
+
+
+class Partition:
+    """Handle of one plan cut by destination ownership over several GPUs."""
+
+    def __init__(self, handle: int, plan: Plan, ngpus: int):
+        self.handle = handle
+        self.plan = plan   # the partition's programs index the plan's ranks
+        self.ngpus = ngpus
+
+    @property
+    def _as_parameter_(self):
+        if not self.handle:
+            raise ReshardError(6, "partition", "partition already destroyed")
+        return ctypes.c_void_p(self.handle)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            try:
+                _lib.reshard_partition_destroy(ctypes.c_void_p(h))
+            except Exception:  # noqa: BLE001 - interpreter shutdown
+                pass
+            self.handle = None
+
+
+def reshard_partition_create(plan: Plan, src_gpu, dst_gpu, gpu_domain, nchunks: int = 1):
+    """Cut ``plan`` over ``len(gpu_domain)`` GPUs: src_gpu[r] / dst_gpu[r] is the GPU of
+    each source / destination rank, gpu_domain[g] the NVLink domain of GPU g."""
+    def arr(v):
+        v = [int(x) for x in v]
+        return (ctypes.c_int32 * max(1, len(v)))(*v)
+    h = ctypes.c_void_p()
+    _check(_lib.reshard_partition_create(plan, arr(src_gpu), arr(dst_gpu), len(gpu_domain),
+                                         arr(gpu_domain), int(nchunks), ctypes.byref(h)),
+           "reshard_partition_create")
+    return Partition(h.value, plan, len(gpu_domain))
+
+
+def reshard_partition_stats(part: Partition) -> dict:
+    s = reshard_partition_stats_t()
+    _check(_lib.reshard_partition_stats(part, ctypes.byref(s)), "reshard_partition_stats")
+    return {n: int(getattr(s, n)) for n, _ in s._fields_}
+
+
+def reshard_partition_gpu(part: Partition, gpu: int) -> dict:
+    s = reshard_partition_gpu_t()
+    _check(_lib.reshard_partition_gpu(part, int(gpu), ctypes.byref(s)), "reshard_partition_gpu")
+    return {n: int(getattr(s, n)) for n, _ in s._fields_}
+
+
+def reshard_partition_transfers(part: Partition, gpu: int) -> list:
+    """One GPU's messages as dicts (chunk, stage, peer, dir, offset, bytes)."""
+    xp = ctypes.POINTER(reshard_xfer_t)()
+    n = ctypes.c_int64()
+    _check(_lib.reshard_partition_transfers(part, int(gpu), ctypes.byref(xp), ctypes.byref(n)),
+           "reshard_partition_transfers")
+    return [{f: int(getattr(xp[i], f)) for f, _ in reshard_xfer_t._fields_}
+            for i in range(n.value)]
+
+
+def reshard_partition_program(part: Partition, gpu: int, step: int, chunk: int = 0):
+    """(tiles, unit_prefix, group_offsets, group_buffers) of one step of one GPU."""
+    tp = ctypes.POINTER(reshard_tile_t)()
+    nt = ctypes.c_int64()
+    pp = ctypes.POINTER(ctypes.c_int64)()
+    go = ctypes.POINTER(ctypes.c_uint32)()
+    gb = ctypes.POINTER(ctypes.c_uint16)()
+    ng = ctypes.c_int64()
+    _check(_lib.reshard_partition_program(part, int(gpu), int(step), int(chunk),
+                                          ctypes.byref(tp), ctypes.byref(nt), ctypes.byref(pp),
+                                          ctypes.byref(go), ctypes.byref(gb), ctypes.byref(ng)),
+           "reshard_partition_program")
+    n, g = nt.value, ng.value
+    tiles = [{f: getattr(tp[i], f) for f, _ in reshard_tile_t._fields_} for i in range(n)]
+    prefix = [pp[i] for i in range(n + 1)]
+    goff = [go[i] for i in range(g + 1)]
+    gbuf = [gb[i] for i in range(goff[-1])] if g >= 0 and goff else []
+    return tiles, prefix, goff, gbuf
+
+
+def reshard_partition_execute(part: Partition, gpu: int, step: int, chunk: int, src_ptrs,
+                              dst_ptrs, recv_buf, send_buf, stream=None):
+    _check(_lib.reshard_partition_execute(part, int(gpu), int(step), int(chunk),
+                                          _ptr_array(src_ptrs), _ptr_array(dst_ptrs),
+                                          _ptr(recv_buf), _ptr(send_buf), _stream(stream)),
+           "reshard_partition_execute")
+
+
+def reshard_partition_destroy(part: Partition):
+    if not part.handle:
+        raise ReshardError(6, "reshard_partition_destroy", "partition already destroyed")
+    st = _lib.reshard_partition_destroy(part)
+    part.handle = None
+    _check(st, "reshard_partition_destroy")
+
+
+def partition_schedule(nchunks: int):
+    """The order in which one GPU runs a partition: a list of ("step", STEP_*, chunk) and
+    ("exchange", [(chunk, stage), ...]) items.  Stage 1 of a chunk is exchanged together
+    with stage 0 of the next one (the pipeline of the two stages); every GPU follows the
+    same list, so grouped point-to-point calls match."""
+    out = [("step", STEP_LOCAL, 0), ("step", STEP_PACK, 0), ("exchange", [(0, 0)]),
+           ("step", STEP_FORWARD, 0)]
+    for c in range(1, nchunks):
+        out += [("step", STEP_PACK, c), ("exchange", [(c - 1, 1), (c, 0)]),
+                ("step", STEP_UNPACK, c - 1), ("step", STEP_FORWARD, c)]
+    out += [("exchange", [(nchunks - 1, 1)]), ("step", STEP_UNPACK, nchunks - 1)]
+    return out
+
+
+def partition_run(part: Partition, gpu: int, src_ptrs, dst_ptrs, recv_buf, send_buf, exchange,
+                  stream=None, run_step=None):
+    """Run GPU ``gpu``'s share of a partitioned reshard in ``partition_schedule`` order.
+
+    ``exchange(gpu, sends, recvs)`` performs one round of messages: ``sends`` and
+    ``recvs`` are this GPU's transfer dicts of that round (offsets into send_buf /
+    recv_buf), each list in (chunk, stage, peer) order; it must order them after the
+    steps already enqueued on ``stream`` and the next steps after them (NCCL on the
+    same stream does; a host-side exchange synchronises the stream first).  Each step
+    is ``reshard_partition_execute`` on ``stream`` (the library's kernels do every copy
+    on the GPU), or ``run_step(step, chunk)`` when given.
+    """
+    if run_step is None:
+        def run_step(step, chunk):
+            reshard_partition_execute(part, gpu, step, chunk, src_ptrs, dst_ptrs, recv_buf,
+                                      send_buf, stream)
+    xfers = reshard_partition_transfers(part, gpu)
+    for item in partition_schedule(reshard_partition_stats(part)["nchunks"]):
+        if item[0] == "step":
+            run_step(item[1], item[2])
+        else:
+            rounds = set(item[1])
+            sends = [x for x in xfers if (x["chunk"], x["stage"]) in rounds and x["dir"] == 0]
+            recvs = [x for x in xfers if (x["chunk"], x["stage"]) in rounds and x["dir"] == 1]
+            exchange(gpu, sends, recvs)
+
+
+def nccl_exchange(gpu_rank, send_buf, recv_buf):
+    """An ``exchange`` for partition_run over torch.distributed point-to-point (NCCL on
+    the current stream): process ``gpu_rank[g]`` runs GPU g; send_buf / recv_buf are
+    uint8 device tensors.  The messages of one round go out as one batch; two messages
+    between one pair of GPUs in a round are matched in list order on both sides.  NCCL
+    wants the process group to have run a collective before its first batch of
+    point-to-point calls (a barrier will do).  Not run on more than one GPU here."""
+    import torch.distributed as dist
+
+    def exchange(gpu, sends, recvs):
+        ops = [dist.P2POp(dist.isend, send_buf[x["offset"]:x["offset"] + x["bytes"]],
+                          gpu_rank[x["peer"]]) for x in sends]
+        ops += [dist.P2POp(dist.irecv, recv_buf[x["offset"]:x["offset"] + x["bytes"]],
+                           gpu_rank[x["peer"]]) for x in recvs]
+        if ops:
+            for w in dist.batch_isend_irecv(ops):
+                w.wait()
+    return exchange
+

@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["planner.cpp", "batch.cpp", "kernels.cu", "bulk_fanout.cu", "transpose.cu",
-           "static_scratch.cu", "realign_staged.cu", "refit.cpp"]
+           "static_scratch.cu", "realign_staged.cu", "refit.cpp", "partition.cpp"]
 HEADERS = ["internal.h", "staging.cuh"]
 
 

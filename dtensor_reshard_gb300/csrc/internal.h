@@ -143,6 +143,36 @@ struct Program {
   const reshard_tseg_t* d_tsegs = nullptr;
 };
 
+// ------------------------------------------------------------ planner pieces
+// (planner.cpp), shared with the multi-GPU partition (partition.cpp).
+
+// Box (global offset + local shape) of one flat rank of a layout: Shard(d) on a
+// mesh dim of size k splits the current local extent n of dim d into
+// torch.chunk pieces of ceil(n/k); mesh dims apply in order.
+void resolve_rank(int32_t nd, const int64_t* gshape, const Layout& L, int64_t rank, Box* b);
+int64_t box_volume(int32_t nd, const Box& b);
+// Ranks holding one identical, non-empty box (replicas), ranks ascending.
+struct Class {
+  Box box;
+  std::vector<int64_t> ranks;
+  int64_t volume = 0;
+};
+// The classes of a layout, leaving out the ranks marked in `gone` (may be empty).
+std::vector<Class> classes_of(int32_t nd, const Layout& L, const std::vector<uint8_t>& gone);
+struct Dim {
+  int64_t e, ss, ds;  // extent, source stride, destination stride (elements)
+};
+void row_major_strides(int32_t nd, const int64_t* shp, int64_t* st);
+// Appends to P the tiles copying a box of extents e[nd] (elements) that starts
+// at element src_base / dst_base of buffers with strides sst / dst (elements),
+// from buffer src_buf to destination group `group` (fanout = its replicas).
+void emit_box(Program& P, uint16_t src_buf, uint16_t group, int32_t nd, const int64_t* e,
+              int64_t src_base, const int64_t* sst, int64_t dst_base, const int64_t* dstr,
+              int64_t eb, int64_t fanout = 1);
+// Sorts P's tiles by destination and fills its prefix and summary fields.
+void finish_program(Program& P);
+int64_t tile_bytes(const reshard_tile_t& t);
+
 // Narrow pieces (bytes per row) below this may go through transpose blocks
 // (the planner's rule narrows it further), and a block holds at most this many
 // bytes of wide rows in shared memory.

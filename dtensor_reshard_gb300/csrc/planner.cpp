@@ -63,6 +63,8 @@ int elem_size(int32_t dtype) {
   }
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------- step 1: resolve
 // Shard(d) on a mesh dim of size k splits the current local extent n of dim d
 // into torch.chunk pieces of ceil(n/k); mesh dims apply in order.
@@ -99,12 +101,6 @@ int64_t box_volume(int32_t nd, const Box& b) {
   return v;
 }
 
-struct Class {
-  Box box;
-  std::vector<int64_t> ranks;  // ascending
-  int64_t volume = 0;
-};
-
 // ---------------------------------------------------------------- step 2: classes
 std::vector<Class> classes_of(int32_t nd, const Layout& L, const std::vector<uint8_t>& gone) {
   std::vector<Class> out;
@@ -132,9 +128,6 @@ std::vector<Class> classes_of(int32_t nd, const Layout& L, const std::vector<uin
 }
 
 // ---------------------------------------------------------------- step 5: tiles
-struct Dim {
-  int64_t e, ss, ds;  // extent, source stride, destination stride (elements)
-};
 
 void row_major_strides(int32_t nd, const int64_t* shp, int64_t* st) {
   int64_t s = 1;
@@ -148,7 +141,7 @@ void row_major_strides(int32_t nd, const int64_t* shp, int64_t* st) {
 // element src_base / dst_base of buffers with strides sst / dst (elements).
 void emit_box(Program& P, uint16_t src_buf, uint16_t group, int32_t nd, const int64_t* e,
               int64_t src_base, const int64_t* sst, int64_t dst_base, const int64_t* dstr,
-              int64_t eb, int64_t fanout = 1) {
+              int64_t eb, int64_t fanout) {
   std::vector<Dim> dims;
   for (int d = 0; d < nd; ++d) {
     if (e[d] == 0) return;
@@ -282,6 +275,8 @@ void finish_program(Program& P) {
 int64_t tile_bytes(const reshard_tile_t& t) {
   return int64_t(t.row_bytes) * t.nrows * t.nplanes;
 }
+
+namespace {
 
 // ---------------------------------------------------------------- validation
 reshard_status_t read_layout(const char* side, int32_t nd, const reshard_mesh_t* mesh,

@@ -508,6 +508,161 @@ reshard_status_t reshard_refit_execute(reshard_refit_t refit, const void* const*
 reshard_status_t reshard_refit_destroy(reshard_refit_t refit);
 
 /*
+ * Multi-GPU partition of one reshard (news.bpdata.com, section "A Reshard
+ * kollektiv kommunikacio": each contribution crosses the network once, the
+ * replicas are assembled inside the NVLink domain with a balanced exchange, and
+ * the two stages are pipelined; techfeed.io, section on NVIDIA's NVLink
+ * implementation: incoming data spread as evenly as possible over the replicas).
+ *
+ * reshard_partition_create cuts a plan by destination ownership.  src_gpu[M]
+ * and dst_gpu[N] give the GPU (0..ngpus-1) of every source and destination
+ * rank (ignored for ranks an excluded plan leaves out), gpu_domain[ngpus] the
+ * NVLink domain of every GPU (any non-negative ids; GPUs with equal ids share a
+ * domain).  Every GPU g then owns:
+ *   - the LOCAL step: regions whose source replica is on g, copied to all of
+ *     g's destination replicas of the region's class (one read, R writes);
+ *   - per pipeline chunk c (0..nchunks-1), three steps around two rounds of
+ *     messages:
+ *       PACK c     stage-0 pieces g sends, copied from its source shards into
+ *                  its send buffer;
+ *       (stage 0)  the messages of stage 0 of chunk c;
+ *       FORWARD c  stage-1 pieces g sends, copied from where they landed in
+ *                  its receive buffer in stage 0 into its send buffer;
+ *       (stage 1)  the messages of stage 1 of chunk c;
+ *       UNPACK c   every piece g received in chunk c, copied from its receive
+ *                  buffer to all of g's destination replicas of its class.
+ * Routing: a region that g needs and holds in a local source shard is copied
+ * locally; a domain that holds a source replica of a region gets it from one
+ * inside the domain (stage 0), the least-loaded such GPU per piece; a domain
+ * that holds none receives each piece ONCE across domains (stage 0; sender: the
+ * least-loaded GPU holding a source replica, receiver: the least-loaded GPU of
+ * the domain that needs it), and the receiver forwards it to the domain's other
+ * GPUs that need it (stage 1).  Loads are bytes sent (senders) and received
+ * (receivers), pieces taken largest first.  Regions that cross GPUs are cut
+ * along their outermost dim into nchunks (1..64) pieces, piece i in pipeline
+ * chunk i (regions with fewer rows than chunks: one piece per row, chunks taken
+ * in turn), so every link's bytes split evenly over the chunks; with
+ * nchunks > 1, chunk c uses slot c % 2 of the send and receive buffers.
+ *
+ * Messages are packed: all pieces from one GPU to another in one chunk and
+ * stage form one contiguous, 16-byte-aligned range of the sender's send buffer
+ * and of the receiver's receive buffer, pieces in the same order on both sides,
+ * each piece row-major in its own box and 16-byte aligned.  The library moves
+ * nothing between GPUs: the caller performs every message (NCCL send/recv, peer
+ * copies; never multicast) between the steps.  A valid order on one stream:
+ * LOCAL; PACK 0; stage 0 of chunk 0; FORWARD 0; then for c = 1..nchunks-1:
+ * PACK c, stage 1 of chunk c-1 together with stage 0 of chunk c, UNPACK c-1,
+ * FORWARD c; finally stage 1 of the last chunk and its UNPACK.  With a single
+ * chunk: LOCAL, PACK 0, stage 0, FORWARD 0, stage 1, UNPACK 0.
+ *
+ * The partition is a host object (no device memory until a step runs) and is
+ * the same on every process that builds it from the same plan and maps.
+ * Errors: BAD_HANDLE, INVALID_ARG (null map, a GPU id out of range, a negative
+ * domain, ngpus or nchunks out of range), UNSUPPORTED (in-place plans; M + N + 2
+ * > RESHARD_MAX_EXEC_BUFFERS), NO_MEMORY.
+ */
+typedef struct reshard_partition_s* reshard_partition_t;
+
+typedef enum {
+  RESHARD_STEP_LOCAL = 0,
+  RESHARD_STEP_PACK = 1,
+  RESHARD_STEP_FORWARD = 2,
+  RESHARD_STEP_UNPACK = 3
+} reshard_step_t;
+
+/* One message of one GPU: in chunk `chunk`, stage `stage` (0 or 1), this GPU
+ * sends (dir 0) bytes [offset, offset + bytes) of its send buffer to GPU `peer`,
+ * or receives (dir 1) them into [offset, offset + bytes) of its receive buffer
+ * from `peer`.  Both ends of a message list the same byte count. */
+typedef struct {
+  int32_t chunk;
+  int32_t stage;
+  int32_t peer;
+  int32_t dir;
+  int64_t offset;
+  int64_t bytes;
+} reshard_xfer_t;
+
+/* One GPU's share: the sizes of the send and receive buffers it must provide,
+ * bytes it copies from local source shards (each region once), and payload
+ * bytes (without padding) it sends and receives across domains (inter) and
+ * inside its domain (intra). */
+typedef struct {
+  int64_t send_bytes;
+  int64_t recv_bytes;
+  int64_t local_bytes;
+  int64_t sent_inter_bytes;
+  int64_t sent_intra_bytes;
+  int64_t recv_inter_bytes;
+  int64_t recv_intra_bytes;
+  int64_t n_xfers;
+} reshard_partition_gpu_t;
+
+/* The whole partition: destination bytes filled from a source shard on the same
+ * GPU (each replica counted), payload bytes sent across domains (every piece at
+ * most once per receiving domain) and inside domains, the largest per-GPU sent
+ * and received payloads, pieces, messages and planning time. */
+typedef struct {
+  int32_t ngpus;
+  int32_t ndomains;
+  int32_t nchunks;
+  int32_t nslots;
+  int64_t local_bytes;
+  int64_t inter_domain_bytes;
+  int64_t intra_domain_bytes;
+  int64_t max_gpu_send_bytes;
+  int64_t max_gpu_recv_bytes;
+  int64_t n_pieces;
+  int64_t n_messages;
+  int64_t planner_ns;
+} reshard_partition_stats_t;
+
+reshard_status_t reshard_partition_create(reshard_plan_t plan, const int32_t* src_gpu,
+                                          const int32_t* dst_gpu, int32_t ngpus,
+                                          const int32_t* gpu_domain, int32_t nchunks,
+                                          reshard_partition_t* out_partition);
+
+/* Whole-partition figures.  Errors: BAD_HANDLE, INVALID_ARG. */
+reshard_status_t reshard_partition_stats(reshard_partition_t part, reshard_partition_stats_t* out);
+
+/* One GPU's share.  Errors: BAD_HANDLE, INVALID_ARG. */
+reshard_status_t reshard_partition_gpu(reshard_partition_t part, int32_t gpu,
+                                       reshard_partition_gpu_t* out);
+
+/* Read-only view of one GPU's messages, valid until the partition is destroyed,
+ * sorted by (chunk, stage, dir, peer).  Errors: BAD_HANDLE, INVALID_ARG. */
+reshard_status_t reshard_partition_transfers(reshard_partition_t part, int32_t gpu,
+                                             const reshard_xfer_t** xfers, int64_t* n);
+
+/* Read-only view of the copy program of one step (reshard_step_t; chunk is
+ * ignored for LOCAL) of one GPU, as reshard_plan_program gives it.  Buffer
+ * indices: source rank r = r, destination rank r = M + r, the receive buffer
+ * M + N, the send buffer M + N + 1.  Errors: BAD_HANDLE, INVALID_ARG. */
+reshard_status_t reshard_partition_program(reshard_partition_t part, int32_t gpu, int32_t step,
+                                           int32_t chunk, const reshard_tile_t** tiles,
+                                           int64_t* ntiles, const int64_t** unit_prefix,
+                                           const uint32_t** group_offsets,
+                                           const uint16_t** group_buffers, int64_t* ngroups);
+
+/*
+ * Launch one step of one GPU on `stream` (the current device).  src_ptrs[M] and
+ * dst_ptrs[N] are indexed by rank; only the ranks on this GPU are read (a NULL
+ * is accepted for ranks the step's GPU does not read or write; entries of ranks
+ * on other GPUs are ignored).  recv_buf / send_buf: this GPU's buffers of at
+ * least reshard_partition_gpu's recv_bytes / send_bytes (may be NULL when that
+ * is 0).  The first launch of a step uploads its tables (one cudaMalloc and one
+ * synchronous copy), binding that step to the current device.  Errors:
+ * BAD_HANDLE, INVALID_ARG, CUDA.
+ */
+reshard_status_t reshard_partition_execute(reshard_partition_t part, int32_t gpu, int32_t step,
+                                           int32_t chunk, const void* const* src_ptrs,
+                                           void* const* dst_ptrs, void* recv_buf, void* send_buf,
+                                           void* stream);
+
+/* Release the partition and its device tables (the plan stays).  Errors: BAD_HANDLE. */
+reshard_status_t reshard_partition_destroy(reshard_partition_t part);
+
+/*
  * Local box of one rank (news.bpdata.com, section "A megkozelites": the DTensor
  * description fixes each rank's shard).  side 0 = source, 1 = destination.
  * shape[tensor_ndim], offset[tensor_ndim] receive the local shape and the

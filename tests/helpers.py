@@ -142,3 +142,42 @@ def pick_aliases(o, spec, rng=None):
         else:
             out.append(cands[0] if rng is None else rng.choice(cands))
     return out
+
+
+# ------------------------------------------------------------------ partition on the CPU
+def run_tile_list_cpu(tiles, goff, gbuf, bufs, writes):
+    """Execute a list of tiles (as the program views give them) on host buffers."""
+    for t in tiles:
+        src = bufs[t["src_buf"]]
+        for g in range(goff[t["dst_group"]], goff[t["dst_group"] + 1]):
+            di = gbuf[g]
+            dst = bufs[di]
+            for p in range(t["nplanes"]):
+                for r in range(t["nrows"]):
+                    so = t["src_off"] + p * t["src_plane_stride"] + r * t["src_row_stride"]
+                    do = t["dst_off"] + p * t["dst_plane_stride"] + r * t["dst_row_stride"]
+                    n = t["row_bytes"]
+                    assert src is not None and dst is not None, ("buffer not on this gpu", t)
+                    assert 0 <= so and so + n <= src.size, ("source out of bounds", t)
+                    assert 0 <= do and do + n <= dst.size, ("destination out of bounds", t)
+                    dst[do:do + n] = src[so:so + n]
+                    writes[di][do:do + n] += 1
+
+
+def partition_gpu_buffers(part, gpu, src_bytes, dst_sizes, src_gpu, dst_gpu):
+    """Host buffer table [sources..., destinations..., receive, send] of one GPU: only the
+    ranks on that GPU get buffers (others None)."""
+    info = rs.reshard_partition_gpu(part, gpu)
+    srcs = [src_bytes[r].copy() if src_gpu[r] == gpu else None for r in range(len(src_bytes))]
+    dsts = [np.full(n, 0xA5, dtype=np.uint8) if dst_gpu[r] == gpu else None
+            for r, n in enumerate(dst_sizes)]
+    recv = np.zeros(info["recv_bytes"], dtype=np.uint8)
+    send = np.zeros(info["send_bytes"], dtype=np.uint8)
+    bufs = srcs + dsts + [recv, send]
+    writes = [np.zeros(b.size, dtype=np.int32) if b is not None else None for b in bufs]
+    return bufs, writes
+
+
+def run_partition_step_cpu(part, gpu, step, chunk, bufs, writes):
+    tiles, _, goff, gbuf = rs.reshard_partition_program(part, gpu, step, chunk)
+    run_tile_list_cpu(tiles, goff, gbuf, bufs, writes)
