@@ -130,13 +130,18 @@ def test_partition_reduced_workloads_on_the_gpu(oracle, cfg):
 
 def test_partition_full_ffn_up(oracle):
     """The dense FFN up projection [14336, 4096] bf16, (DP2, TP4) -> (DP4, TP2), over 8
-    emulated GPUs in 2 domains, training and generation ranks colocated, 2 chunks."""
+    emulated GPUs, training and generation ranks colocated, 2 chunks.  The domains take
+    alternate GPUs, so each holds only half of the source's tensor-parallel shards and
+    the rest must cross (domains of consecutive GPUs would each hold a whole replica)."""
     spec = workload(2).tensors[0]
     plan = helpers.spec_plan(spec)
     src_gpu, dst_gpu = _maps("colocated", plan.n_src, plan.n_dst, 8)
-    part, glob, got = _emulate(oracle, spec, src_gpu, dst_gpu, [g // 4 for g in range(8)], 2)
+    dom = [g % 2 for g in range(8)]
+    part, glob, got = _emulate(oracle, spec, src_gpu, dst_gpu, dom, 2)
     st = rs.reshard_partition_stats(part)
     assert st["inter_domain_bytes"] > 0 and st["intra_domain_bytes"] > 0
+    whole = rs.reshard_partition_create(plan, src_gpu, dst_gpu, [g // 4 for g in range(8)], 2)
+    assert rs.reshard_partition_stats(whole)["inter_domain_bytes"] == 0
     for r, (off, shp) in enumerate(oracle.boxes(spec.global_shape, spec.dst_mesh,
                                                 spec.dst_placements)):
         want = helpers.to_bytes(helpers.slice_box(glob, off, shp))
