@@ -76,6 +76,7 @@ void append_plan(Program& C, const Program& F, int64_t base) {
   C.tscatter = C.tscatter || F.tscatter;
   C.long_row_bytes += F.long_row_bytes;
   C.wide_row_bytes += F.wide_row_bytes;
+  C.narrow_row_bytes += F.narrow_row_bytes;
 }
 
 void finish_class(BatchClass& c) {

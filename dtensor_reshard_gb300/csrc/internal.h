@@ -53,6 +53,10 @@ constexpr int kNumPrograms = 5;
 // 138 MB fp32 gather of 56 pieces of 628 bytes into 15 replicas: 0.553 -> 0.386 ms.
 constexpr int64_t kAssembleFanout = 8;
 
+// Rows shorter than this count as narrow (the element kernel keeps fewer
+// loads in flight for programs made mostly of them).
+constexpr int64_t kNarrowRow = 32;
+
 // Fixed work of one row (offsets, partial first and last words, a row-table
 // entry), counted in bytes of streaming when rows are grouped into units.
 constexpr int64_t kRowCostBytes = 256;
@@ -131,6 +135,7 @@ struct Program {
   int64_t write_bytes = 0;  // bytes written: each tile's bytes times its replicas
   int64_t long_row_bytes = 0;  // ... of those in rows of at least 512 bytes (runs included)
   int64_t wide_row_bytes = 0;  // ... of those in rows of at least 8 KiB (runs included)
+  int64_t narrow_row_bytes = 0;  // ... of those in rows under kNarrowRow bytes
   int64_t total_units() const { return prefix.empty() ? 0 : prefix.back(); }
   // transpose blocks (narrow innermost pieces grouped by shared rows)
   std::vector<reshard_tblock_t> tblocks;
@@ -246,6 +251,7 @@ struct Dispatch {
   int path = RESHARD_PATH_NONE;  // reshard_path_t
   int w_log2 = 0;                // widest common access, log2 bytes
   int kidx = 0;                  // copy-kernel table index (kernels.cu)
+  int narrow = 0;                // 1: the variant for mostly narrow rows
   uint32_t flags = 0;            // kFlag* bits for the kernel
 };
 Dispatch decide(const Program& prog, unsigned char* const* bufs, int nbufs, bool allow_tma_fanout);

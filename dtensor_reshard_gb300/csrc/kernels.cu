@@ -12,7 +12,8 @@
 //
 // Within a tile a CTA streams 16-byte vectors (narrower when the runtime
 // addresses, strides or row length are not 16-byte aligned): every thread
-// issues kUnroll independent loads before it stores, and each loaded vector is
+// issues several independent loads before it stores (about 64 bytes in flight
+// per thread whatever the vector width), and each loaded vector is
 // stored to every destination buffer of the tile's group (the fan-out: the
 // source region is read from HBM once, written R times).  Loads and stores use
 // the evict-first (streaming) cache policy because no byte is touched twice.
@@ -34,7 +35,13 @@ namespace rs {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+// Independent loads each thread keeps in flight: about kInflightBytes per
+// thread whatever the access width (at most 16 loads), so that narrow accesses
+// still keep enough bytes in flight to cover the memory latency.
+constexpr int kInflightBytes = 64;
+template <int W> __host__ __device__ constexpr int unroll_of() {
+  return kInflightBytes / W < 4 ? 4 : (kInflightBytes / W > 16 ? 16 : kInflightBytes / W);
+}
 
 // Unsigned 32-bit division by a runtime-invariant divisor through a multiply
 // and a shift (Granlund and Montgomery, "Division by Invariant Integers using
@@ -71,7 +78,7 @@ __device__ __forceinline__ void store_stream(unsigned char* p, const T& v) {
 
 // Bytes [0, nbytes) of a contiguous run: from src to dst + dofs for each of
 // the R destination buffers dst in sdst.
-template <int W>
+template <int W, int kUnroll>
 __device__ __forceinline__ void copy_run(const unsigned char* __restrict__ src,
                                          unsigned char* const* sdst, int R, int64_t dofs,
                                          uint32_t nbytes) {
@@ -104,7 +111,7 @@ __device__ __forceinline__ void copy_run(const unsigned char* __restrict__ src,
 // streamed as one flat range of vectors by the whole CTA; shorter rows are packed
 // kThreads / vpr to a pass, one thread per vector, and every thread carries
 // kUnroll rows at once.
-template <int W, bool PLANES>
+template <int W, bool PLANES, int kUnroll>
 __device__ __forceinline__ void copy_rows(const reshard_tile_t& t, const unsigned char* src,
                                           unsigned char* const* sdst, int R, uint32_t r_begin,
                                           uint32_t r_end) {
@@ -124,9 +131,9 @@ __device__ __forceinline__ void copy_rows(const reshard_tile_t& t, const unsigne
   };
   if (vpr >= uint32_t(kThreads)) {
     // long rows: the block walks (row, vector) pairs flat, kThreads vectors apart,
-    // so every thread keeps kUnroll loads in flight whatever the row length.  As
+    // so every thread keeps its loads in flight whatever the row length.  As
     // vpr >= kThreads a step crosses at most one row boundary.  The store cursor
-    // repeats the load cursor's walk instead of holding kUnroll offsets.
+    // repeats the load cursor's walk instead of holding one offset per load.
     uint32_t lrow = r_begin, lcol = threadIdx.x;
     int64_t lbase = src_row(lrow);
     uint32_t srow = r_begin, scol = threadIdx.x;
@@ -185,9 +192,14 @@ __device__ __forceinline__ void copy_rows(const reshard_tile_t& t, const unsigne
   }
 }
 
-template <int W, bool PLANES>
+// NARROW: programs whose bytes are mostly in rows under kNarrowRow bytes keep 4
+// loads in flight per thread: each load there already pulls a whole sector of
+// the source, and more of them in flight were measured slower (4-byte rows at
+// a 32-byte source stride: 0.15 -> 0.21 ms with 16).
+template <int W, bool PLANES, bool NARROW>
 __global__ void __launch_bounds__(kThreads, PLANES ? 2 : 4)
     reshard_copy_kernel(const __grid_constant__ KernelParams p) {
+  constexpr int kUnroll = NARROW ? 4 : unroll_of<W>();
   __shared__ unsigned char* s_dst[kMaxGroup];
 
   const int64_t total = p.total_units;
@@ -221,14 +233,14 @@ __global__ void __launch_bounds__(kThreads, PLANES ? 2 : 4)
     if (t.nrows == 1 && t.nplanes == 1) {
       const int64_t b0 = a * kUnitBytes;
       const int64_t b1 = min(b * kUnitBytes, int64_t(t.row_bytes));
-      copy_run<W>(src + t.src_off + b0, s_dst, R, t.dst_off + b0, uint32_t(b1 - b0));
+      copy_run<W, kUnroll>(src + t.src_off + b0, s_dst, R, t.dst_off + b0, uint32_t(b1 - b0));
     } else {
       const uint32_t upr = rows_per_unit(t.row_bytes);
       const uint64_t rows = uint64_t(t.nrows) * t.nplanes;
       const uint32_t r_begin = uint32_t(a * upr);
       const uint32_t r_end = uint32_t(min(uint64_t(b) * upr, rows));
-      if (PLANES && t.nplanes > 1) copy_rows<W, true>(t, src, s_dst, R, r_begin, r_end);
-      else copy_rows<W, false>(t, src, s_dst, R, r_begin, r_end);
+      if (PLANES && t.nplanes > 1) copy_rows<W, true, kUnroll>(t, src, s_dst, R, r_begin, r_end);
+      else copy_rows<W, false, kUnroll>(t, src, s_dst, R, r_begin, r_end);
     }
     u0 = tb + b;
     ++ti;
@@ -424,17 +436,22 @@ bool bulk_stores(const Program& prog) {
   return prog.max_fanout >= kBulkStoreFanout && 2 * prog.wide_row_bytes >= prog.tile_bytes;
 }
 
-// Instantiations indexed by [log2 W][planes].
+// Instantiations indexed by [narrow rows][log2 W][planes].
 // [0]: realigning kernel (any alignment); [k], k = 1..4: 2^k-byte vector kernel;
 // [5]: byte kernel.
-const KernelFn kKernels[6][2] = {
-    {reshard_realign_kernel<false>, reshard_realign_kernel<true>},
-    {reshard_copy_kernel<2, false>, reshard_copy_kernel<2, true>},
-    {reshard_copy_kernel<4, false>, reshard_copy_kernel<4, true>},
-    {reshard_copy_kernel<8, false>, reshard_copy_kernel<8, true>},
-    {reshard_copy_kernel<16, false>, reshard_copy_kernel<16, true>},
-    {reshard_copy_kernel<1, false>, reshard_copy_kernel<1, true>},
-};
+const KernelFn kKernels[2][6][2] = {
+    {{reshard_realign_kernel<false>, reshard_realign_kernel<true>},
+     {reshard_copy_kernel<2, false, false>, reshard_copy_kernel<2, true, false>},
+     {reshard_copy_kernel<4, false, false>, reshard_copy_kernel<4, true, false>},
+     {reshard_copy_kernel<8, false, false>, reshard_copy_kernel<8, true, false>},
+     {reshard_copy_kernel<16, false, false>, reshard_copy_kernel<16, true, false>},
+     {reshard_copy_kernel<1, false, false>, reshard_copy_kernel<1, true, false>}},
+    {{reshard_realign_kernel<false>, reshard_realign_kernel<true>},
+     {reshard_copy_kernel<2, false, true>, reshard_copy_kernel<2, true, true>},
+     {reshard_copy_kernel<4, false, true>, reshard_copy_kernel<4, true, true>},
+     {reshard_copy_kernel<8, false, true>, reshard_copy_kernel<8, true, true>},
+     {reshard_copy_kernel<16, false, true>, reshard_copy_kernel<16, true, true>},
+     {reshard_copy_kernel<1, false, true>, reshard_copy_kernel<1, true, true>}}};
 
 // Kernel for a program whose widest common access is 2^w_log2 bytes (rule
 // fitted to per-tensor timings of the uneven-stress tensors):
@@ -475,8 +492,8 @@ bool destinations_congruent(const Program& prog, unsigned char* const* bufs) {
 std::mutex g_occ_mu;
 std::map<std::pair<int, int>, int> g_occ;  // (device, kernel index) -> blocks per SM
 
-reshard_status_t occupancy(int device, int w_log2, int planes, int* blocks) {
-  const std::pair<int, int> key(device, w_log2 * 2 + planes);
+reshard_status_t occupancy(int device, int w_log2, int planes, int narrow, int* blocks) {
+  const std::pair<int, int> key(device, (narrow * 6 + w_log2) * 2 + planes);
   std::lock_guard<std::mutex> lk(g_occ_mu);
   auto it = g_occ.find(key);
   if (it != g_occ.end()) {
@@ -485,7 +502,7 @@ reshard_status_t occupancy(int device, int w_log2, int planes, int* blocks) {
   }
   int n = 0;
   cudaError_t ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &n, reinterpret_cast<const void*>(kKernels[w_log2][planes]), kThreads, 0);
+      &n, reinterpret_cast<const void*>(kKernels[narrow][w_log2][planes]), kThreads, 0);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("occupancy query: ") + cudaGetErrorString(ce));
   n = n > 0 ? n : 1;
@@ -510,6 +527,7 @@ Dispatch decide(const Program& prog, unsigned char* const* bufs, int nbufs, bool
     return d;
   }
   d.kidx = choose_kernel(prog, d.w_log2);
+  d.narrow = 2 * prog.narrow_row_bytes >= prog.tile_bytes ? 1 : 0;
   if (d.kidx == kStagedRealign) {
     if (bulk_stores(prog)) d.flags |= kFlagBulkStores;
     d.path = (d.flags & kFlagDstCongruent) && (d.flags & kFlagBulkStores)
@@ -528,7 +546,7 @@ reshard_status_t copy_kernel_occupancy(int* blocks_per_sm) {
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ce));
-  return occupancy(dev, 4, 0, blocks_per_sm);
+  return occupancy(dev, 4, 0, 0, blocks_per_sm);
 }
 
 static reshard_status_t launch_tiles(const reshard_plan_s* plan, const Program& prog,
@@ -562,12 +580,12 @@ static reshard_status_t launch_tiles(const reshard_plan_s* plan, const Program& 
   const int planes = prog.has_planes ? 1 : 0;
   const int kidx = d.kidx;
   int bps = 1;
-  reshard_status_t st = occupancy(dev, kidx, planes, &bps);
+  reshard_status_t st = occupancy(dev, kidx, planes, d.narrow, &bps);
   if (st != RESHARD_OK) return st;
   const int64_t max_grid = int64_t(plan->num_sms) * bps;
   const unsigned grid = unsigned(total < max_grid ? total : max_grid);
   void* args[] = {&kp};
-  cudaError_t ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[kidx][planes]),
+  cudaError_t ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[d.narrow][kidx][planes]),
                                     dim3(grid), dim3(kThreads), args, 0,
                                     static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess)
@@ -617,7 +635,7 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
   const int kidx = d.kidx;
   int bps = 1;
   if (kidx >= 0) {
-    reshard_status_t st = occupancy(dev, kidx, planes, &bps);
+    reshard_status_t st = occupancy(dev, kidx, planes, d.narrow, &bps);
     if (st != RESHARD_OK) return st;
   }
 
@@ -638,7 +656,7 @@ reshard_status_t launch_program_tables(const Program& prog, const reshard_tile_t
   const int64_t max_grid = int64_t(num_sms) * bps;
   const unsigned grid = unsigned(total < max_grid ? total : max_grid);
   void* args[] = {&kp};
-  ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[kidx][planes]), dim3(grid),
+  ce = cudaLaunchKernel(reinterpret_cast<const void*>(kKernels[d.narrow][kidx][planes]), dim3(grid),
                         dim3(kThreads), args, 0, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess)
     return fail(RESHARD_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(ce));

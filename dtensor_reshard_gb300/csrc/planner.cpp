@@ -267,6 +267,7 @@ void finish_program(Program& P) {
     P.write_bytes += bytes * int64_t(P.goff[t.dst_group + 1] - P.goff[t.dst_group]);
     if (t.row_bytes >= 512) P.long_row_bytes += bytes;
     if (t.row_bytes >= 8192) P.wide_row_bytes += bytes;
+    if (t.row_bytes < kNarrowRow) P.narrow_row_bytes += bytes;
   }
   for (size_t g = 0; g + 1 < P.goff.size(); ++g)
     P.max_fanout = std::max<int>(P.max_fanout, int(P.goff[g + 1] - P.goff[g]));
