@@ -103,7 +103,7 @@ class reshard_tblock_t(ctypes.Structure):
     _fields_ = [("wide_off", ctypes.c_int64), ("row_bytes", ctypes.c_uint32),
                 ("nrows", ctypes.c_uint32), ("seg_begin", ctypes.c_uint32),
                 ("seg_count", ctypes.c_uint32), ("wide", ctypes.c_uint16),
-                ("direction", ctypes.c_uint16), ("pad", ctypes.c_uint32)]
+                ("direction", ctypes.c_uint16), ("flags", ctypes.c_uint32)]
 
 
 class reshard_tseg_t(ctypes.Structure):

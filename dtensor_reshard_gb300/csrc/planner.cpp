@@ -521,14 +521,36 @@ reshard_status_t build_plan(reshard_plan_s* P) {
         else narrow_ids[i] = fan_groups(dc[g.d].ranks);
       }
       // rows per block: enough blocks to occupy the GPU, at most one shared-memory image
-      const int64_t nb = std::min<int64_t>(
+      int64_t nb = std::min<int64_t>(
           rows, std::max<int64_t>(1, std::min<int64_t>(kTransposeBlockBytes / L,
                                                        (planes * rows + kTransposeMinBlocks - 1) /
                                                            kTransposeMinBlocks)));
+      // a multiple of the rows after which every narrow range is back at the same
+      // address mod 16 (then the kernel keeps its granule plans from block to
+      // block), unless the cut costs more than a quarter of the block (a gather of
+      // 42 pieces of 68 bytes: 0.125 -> 0.092 ms with its plans kept)
+      {
+        int64_t m = 1;
+        for (const Piece& pc : ps) {
+          int64_t w = pc.narrow.width, g = 16;
+          while (w % 2 == 0 && g > 1) {
+            w /= 2;
+            g /= 2;
+          }
+          m = std::max(m, g);  // 16 / gcd(16, width); powers of two, so the max is the lcm
+        }
+        if (nb >= m && 4 * (nb % m) <= nb) nb -= nb % m;
+      }
       for (uint16_t wid : wide_ids) {
         for (int64_t pl = 0; pl < planes; ++pl) {
           for (int64_t r0 = 0; r0 < rows; r0 += nb) {
             reshard_tblock_t blk = {};
+            // same shape as the block before it (same wide side, rows and segments;
+            // only the offsets move): the kernel keeps what it worked out for it
+            if (r0 > 0 || pl > 0) {
+              const int64_t prev_rows = r0 > 0 ? nb : std::min(nb, rows - (rows - 1) / nb * nb);
+              if (std::min(nb, rows - r0) == prev_rows) blk.flags = RESHARD_TBLOCK_SAME_SHAPE;
+            }
             blk.wide_off = wide_base + pl * wide_pstride + r0 * L;
             blk.row_bytes = uint32_t(L);
             blk.nrows = uint32_t(std::min(nb, rows - r0));

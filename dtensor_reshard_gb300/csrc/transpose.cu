@@ -76,9 +76,10 @@ struct SegInfo {
   uint32_t col;              // byte column inside a wide row
   uint32_t m, l;             // fast division by units
   uint32_t rbeg, rcnt;       // scatter: replica pointers [rbeg, rbeg + rcnt) of ptrs[]
-  uint32_t gstart;           // first staging granule of the segment
+  uint32_t gstart;           // first granule of the segment
   uint32_t gmis;             // narrow global address mod 16 (replica 0 for scatter)
   uint32_t nbytes;           // width * nrows
+  uint32_t moved;            // gmis differs from the block the granule plans were made for
 };
 
 template <int U> struct UType;
@@ -87,7 +88,7 @@ template <> struct UType<2> { using T = uint16_t; };
 template <> struct UType<4> { using T = uint32_t; };
 template <> struct UType<8> { using T = uint2; };
 
-// segment owning staging granule g (largest k with gstart[k] <= g)
+// segment owning granule g (largest k with gstart[k] <= g)
 __device__ __forceinline__ int find_granule(const SegInfo* si, int K, uint32_t g) {
   int lo = 0, hi = K - 1;
   while (lo < hi) {
@@ -126,117 +127,189 @@ __device__ __forceinline__ void granule_put(uint32_t (&w)[4], int i, typename UT
   }
 }
 
-// Where granule g (flattened over the segments' dense ranges) starts: its
-// segment, the bytes [lo, hi) of the granule that belong to it, and the
-// image address of its first element; the elements of a segment follow one
-// another along a row of `units` elements, then wrap to the next row.
-struct GranuleWalk {
-  const SegInfo* s;
-  uint32_t j, lo, hi, c;
-  uint32_t img_off;  // image byte of the first element (before the image shift)
-};
-template <int U>
-__device__ __forceinline__ GranuleWalk granule_walk(const SegInfo* si, int K, uint32_t g,
-                                                    uint32_t L) {
-  GranuleWalk w;
-  w.s = &si[find_granule(si, K, g)];
-  const SegInfo& s = *w.s;
-  w.j = g - s.gstart;
-  w.lo = w.j == 0 ? s.gmis : 0u;
-  w.hi = min(16u, s.gmis + s.nbytes - 16u * w.j);
-  const uint32_t e0 = (16u * w.j + w.lo - s.gmis) / U;
-  const uint32_t row = fastdiv(e0, s.m, s.l);
-  w.c = e0 - row * s.units;
-  w.img_off = s.col + row * L + w.c * U;
-  return w;
+// The plan of one granule: which segment it belongs to, which of its bytes
+// [lo, hi) are the segment's, the image byte of its first element (counted
+// from the image's shifted origin) and, for the general walk, that element's
+// column in its row.  Granules come in three kinds:
+//   ROWS  a whole granule of 16 / width whole rows (width divides 16 and the
+//         narrow start's offset mod 16): element i is at row i / units,
+//         column i % units, a pattern the compiler unrolls;
+//   INROW a whole granule of 16 bytes inside one row (16 divides the width,
+//         the narrow range 16-byte aligned): one unaligned 16-byte stretch of
+//         the image;
+//   WALK  anything else: elements in order, wrapping to the next row.
+// A plan depends on the block's shape and on the narrow ranges' addresses mod
+// 16 only, so a CTA keeps its threads' plans over blocks of the same shape and
+// redoes only those of segments whose narrow address mod 16 moved.
+constexpr uint32_t kKindNone = 0, kKindWalk = 1, kKindRows = 2, kKindInrow = 3;
+constexpr int kSlots = 6;  // planned granules per thread (more are walked each block)
+
+// One 32-bit word per planned granule: image byte of the first element (before
+// the image shift, below 2^15), segment, kind, and the first element's column.
+// The granule's bytes [lo, hi) follow from its segment and index.
+__device__ __forceinline__ uint32_t plan_off(uint32_t m) { return m & 0x7fffu; }
+__device__ __forceinline__ uint32_t plan_k(uint32_t m) { return (m >> 15) & 0x7fu; }
+__device__ __forceinline__ uint32_t plan_kind(uint32_t m) { return (m >> 22) & 0x3u; }
+__device__ __forceinline__ uint32_t plan_c(uint32_t m) { return m >> 24; }
+static_assert(kTransposeBlockBytes < (1 << 15) && kTransposeMaxSegs <= 128 &&
+                  kTransposeMaxWidth <= 129, "granule plan fields");
+
+// Bytes [lo, hi) of granule j that belong to its segment (hi <= lo: none).
+__device__ __forceinline__ void granule_span(const SegInfo& s, uint32_t j, uint32_t* lo,
+                                             uint32_t* hi) {
+  *lo = j == 0 ? s.gmis : 0u;
+  const int32_t h = int32_t(s.gmis + s.nbytes) - int32_t(16u * j);
+  *hi = h >= 16 ? 16u : (h > 0 ? uint32_t(h) : 0u);
 }
 
-// gather: each thread loads whole aligned 16-byte granules of the segments'
-// dense source ranges (kTVecUnroll in flight) and puts their elements into
-// the image columns they belong to.
+// Does the segment's whole granules take a fast kind (ROWS or INROW)?
 template <int U>
-__device__ __forceinline__ void gather_direct(const SegInfo* si, int K, uint32_t ngran,
-                                              unsigned char* img, uint32_t mis, uint32_t L) {
+__device__ __forceinline__ bool fast_segment(const SegInfo& s) {
+  const uint32_t width = s.units * U;
+  return (16u % width == 0 && s.gmis % width == 0) || (width % 16u == 0 && s.gmis == 0);
+}
+
+// Partial granule e of a block (e < 2 K): the first (e even) or the last (e odd)
+// granule of segment e / 2, when that granule is not whole and the segment's
+// whole granules take a fast kind; false otherwise.
+template <int U>
+__device__ __forceinline__ bool edge_granule(const SegInfo* si, uint32_t e, uint32_t* k,
+                                             uint32_t* j) {
+  const SegInfo& s = si[e >> 1];
+  if (!fast_segment<U>(s)) return false;
+  const uint32_t n = (s.gmis + s.nbytes + 15u) >> 4;  // granules of the segment
+  if (n == 0) return false;
+  *k = e >> 1;
+  if ((e & 1u) == 0) {
+    *j = 0;
+    return s.gmis != 0 || s.nbytes < 16;  // the first granule, when not whole
+  }
+  *j = n - 1;
+  return n > 1 && ((s.gmis + s.nbytes) & 15u) != 0;  // the last one, when not whole
+}
+
+// Plan of granule j of segment k.  With EDGE false, a granule that is not
+// whole (the first or last of a segment whose narrow range is not 16-byte
+// aligned at that end) of a segment whose whole granules take a fast kind is
+// left out (kind none): the edge pass takes those, so that warps of whole
+// granules do not also run the partial-granule path.
+template <int U, bool EDGE = false>
+__device__ __forceinline__ uint32_t plan_of(const SegInfo& s, uint32_t k, uint32_t j, uint32_t L) {
+  uint32_t lo, hi;
+  granule_span(s, j, &lo, &hi);
+  if (hi <= lo || (!EDGE && (lo != 0 || hi != 16) && fast_segment<U>(s)))
+    return k << 15;  // kind none
+  const uint32_t e0 = (16u * j + lo - s.gmis) / U;
+  const uint32_t row = fastdiv(e0, s.m, s.l);
+  const uint32_t c = e0 - row * s.units;
+  const uint32_t off = s.col + row * L + c * U;
+  uint32_t kind = kKindWalk;
+  const uint32_t width = s.units * U;
+  if (lo == 0 && hi == 16) {
+    // a whole granule starts at a row boundary when the width divides 16 and the
+    // narrow start's offset mod 16; it lies inside one row when 16 divides the
+    // width and the narrow start is aligned
+    if (16u % width == 0 && s.gmis % width == 0) kind = kKindRows;
+    else if (width % 16u == 0 && s.gmis == 0) kind = kKindInrow;
+  }
+  return off | (k << 15) | (kind << 22) | (c << 24);
+}
+
+// A whole granule of rows: element i at row i / UNITS, column i % UNITS.
+template <int U, int UNITS, bool GATHER>
+__device__ __forceinline__ void rows_move(unsigned char* img_at, uint32_t L, uint32_t (&words)[4],
+                                          const uint4& v) {
   using T = typename UType<U>::T;
   constexpr int E = 16 / U;
-#pragma unroll 1
-  for (uint32_t g0 = threadIdx.x; g0 < ngran; g0 += kTThreads * kTVecUnroll) {
-    uint4 v[kTVecUnroll];
 #pragma unroll
-    for (int q = 0; q < kTVecUnroll; ++q) {
-      const uint32_t g = g0 + q * kTThreads;
-      if (g < ngran) {
-        const SegInfo& s = si[find_granule(si, K, g)];
-        v[q] = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(g - s.gstart)));
-      }
-    }
+  for (int i = 0; i < E; ++i) {
+    unsigned char* a = img_at + (i / UNITS) * L + (i % UNITS) * U;
+    if constexpr (GATHER) *reinterpret_cast<T*>(a) = granule_elem<U>(v, i);
+    else granule_put<U>(words, i, *reinterpret_cast<const T*>(a));
+  }
+}
+template <int U, bool GATHER>
+__device__ __forceinline__ void rows_dispatch(uint32_t units, unsigned char* img_at, uint32_t L,
+                                              uint32_t (&words)[4], const uint4& v) {
+  constexpr int E = 16 / U;
+  switch (units) {
+    case 1: rows_move<U, 1, GATHER>(img_at, L, words, v); break;
+    case 2: if constexpr (E >= 2) rows_move<U, 2, GATHER>(img_at, L, words, v); break;
+    case 4: if constexpr (E >= 4) rows_move<U, 4, GATHER>(img_at, L, words, v); break;
+    case 8: if constexpr (E >= 8) rows_move<U, 8, GATHER>(img_at, L, words, v); break;
+    default: if constexpr (E >= 16) rows_move<U, 16, GATHER>(img_at, L, words, v); break;
+  }
+}
+
+// The elements [lo, hi) of a granule in order, wrapping from the end of a row to
+// the start of the next one (c: column of the first element in its row).
+template <int U, bool GATHER>
+__device__ __forceinline__ void walk_move(unsigned char* to, uint32_t units, uint32_t wrap,
+                                          uint32_t c, uint32_t lo, uint32_t hi,
+                                          uint32_t (&words)[4], const uint4& v) {
+  using T = typename UType<U>::T;
+  constexpr int E = 16 / U;
+  const int ilo = int(lo / U), ihi = int(hi / U);
 #pragma unroll
-    for (int q = 0; q < kTVecUnroll; ++q) {
-      const uint32_t g = g0 + q * kTThreads;
-      if (g < ngran) {
-        GranuleWalk w = granule_walk<U>(si, K, g, L);
-        const uint32_t units = w.s->units, wrap = L - units * U;
-        unsigned char* to = img + mis + w.img_off;
-        const int ilo = int(w.lo / U), ihi = int(w.hi / U);
-        uint32_t c = w.c;
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-          if (i >= ilo && i < ihi) {
-            *reinterpret_cast<T*>(to) = granule_elem<U>(v[q], i);
-            to += U;
-            if (++c == units) {
-              c = 0;
-              to += wrap;
-            }
-          }
-        }
+  for (int i = 0; i < E; ++i) {
+    if (i >= ilo && i < ihi) {
+      if constexpr (GATHER) *reinterpret_cast<T*>(to) = granule_elem<U>(v, i);
+      else granule_put<U>(words, i, *reinterpret_cast<const T*>(to));
+      to += U;
+      if (++c == units) {
+        c = 0;
+        to += wrap;
       }
     }
   }
 }
 
-// scatter: each thread builds whole 16-byte granules of the segments' dense
-// destination ranges (aligned like replica 0) from the image columns and
-// writes them to every replica of the segment.
-template <int U>
-__device__ __forceinline__ void scatter_direct(const SegInfo* si, int K, uint32_t ngran,
-                                               const unsigned char* img, uint32_t mis, uint32_t L,
-                                               unsigned char* const* ptrs) {
-  using T = typename UType<U>::T;
-  constexpr int E = 16 / U;
-#pragma unroll 1
-  for (uint32_t g = threadIdx.x; g < ngran; g += kTThreads) {
-    GranuleWalk w = granule_walk<U>(si, K, g, L);
-    const SegInfo& s = *w.s;
-    const uint32_t units = s.units, wrap = L - units * U;
-    const unsigned char* from = img + mis + w.img_off;
-    const int ilo = int(w.lo / U), ihi = int(w.hi / U);
-    uint32_t c = w.c;
-    uint32_t words[4] = {0u, 0u, 0u, 0u};
+// The image bytes of one granule (scatter: into words; gather: from v).
+template <int U, bool GATHER>
+__device__ __forceinline__ void granule_move(const SegInfo& s, uint32_t meta, uint32_t lo,
+                                             uint32_t hi, unsigned char* img_at, uint32_t L,
+                                             uint32_t (&words)[4], const uint4& v) {
+  const uint32_t kind = plan_kind(meta);
+  if (kind == kKindRows) {
+    rows_dispatch<U, GATHER>(s.units, img_at, L, words, v);
+  } else if (kind == kKindInrow) {
+    if constexpr (GATHER) {
+      using T = typename UType<U>::T;
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
-      if (i >= ilo && i < ihi) {
-        granule_put<U>(words, i, *reinterpret_cast<const T*>(from));
-        from += U;
-        if (++c == units) {
-          c = 0;
-          from += wrap;
-        }
-      }
+      for (int i = 0; i < 16 / U; ++i) *reinterpret_cast<T*>(img_at + i * U) = granule_elem<U>(v, i);
+    } else {
+      // 16 bytes at any alignment: two aligned 16-byte loads and a funnel
+      const uint32_t a = uint32_t(reinterpret_cast<uintptr_t>(img_at) & 15u);
+      const unsigned char* base = img_at - a;
+      const uint4 A = *reinterpret_cast<const uint4*>(base);
+      const uint4 B = a ? *reinterpret_cast<const uint4*>(base + 16) : A;
+      const uint4 out = staging::funnel16(A, B, a >> 2, 0x3210u + 0x1111u * (a & 3u));
+      words[0] = out.x;
+      words[1] = out.y;
+      words[2] = out.z;
+      words[3] = out.w;
     }
-    const uint4 v = make_uint4(words[0], words[1], words[2], words[3]);
-    for (uint32_t r = 0; r < s.rcnt; ++r) {
-      unsigned char* base = ptrs[s.rbeg + r] + s.off;  // segment byte 0 of this replica
-      if ((reinterpret_cast<uintptr_t>(base) & 15u) == s.gmis) {
-        // aligned like replica 0: a whole granule in one store, a partial one in the
-        // widest aligned stores that fit
-        unsigned char* gp = base - s.gmis + 16 * size_t(w.j);
-        if (w.lo == 0 && w.hi == 16) __stcs(reinterpret_cast<uint4*>(gp), v);
-        else staging::store_partial16(gp, v, w.lo, w.hi);
-      } else {
-        for (uint32_t b = w.lo; b < w.hi; ++b)
-          base[16 * w.j + b - s.gmis] = uint8_t(staging::word_at(v, b >> 2) >> (8u * (b & 3u)));
-      }
+  } else {
+    walk_move<U, GATHER>(img_at, s.units, L - s.units * U, plan_c(meta), lo, hi, words, v);
+  }
+}
+
+// scatter: a granule built from the image goes to every replica of its segment.
+__device__ __forceinline__ void scatter_store(const SegInfo& s, uint32_t j, uint32_t lo,
+                                              uint32_t hi, const uint32_t (&words)[4],
+                                              unsigned char* const* ptrs) {
+  const uint4 v = make_uint4(words[0], words[1], words[2], words[3]);
+  for (uint32_t r = 0; r < s.rcnt; ++r) {
+    unsigned char* base = ptrs[s.rbeg + r] + s.off;  // segment byte 0 of this replica
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) == s.gmis) {
+      // aligned like replica 0: a whole granule in one store, a partial one in the
+      // widest aligned stores that fit
+      unsigned char* gp = base - s.gmis + 16 * size_t(j);
+      if (lo == 0 && hi == 16) __stcs(reinterpret_cast<uint4*>(gp), v);
+      else staging::store_partial16(gp, v, lo, hi);
+    } else {
+      for (uint32_t b = lo; b < hi; ++b)
+        base[16 * j + b - s.gmis] = uint8_t(staging::word_at(v, b >> 2) >> (8u * (b & 3u)));
     }
   }
 }
@@ -275,13 +348,19 @@ __global__ void __launch_bounds__(kTThreads, 4)
     staging::mbar_arrive_expect(&s_bar[buf], bytes);
     staging::bulk_load(dyn + buf * kImageBytes, src - m, bytes, &s_bar[buf]);
   };
+  // this thread's granules tid + s * kTThreads, planned for the current shape
+  uint32_t plan[kSlots];
   // uniform over the CTA: scatter blocks seen, loads issued per image, wait parities
   uint32_t nscatter = 0, pending = 0, parity = 0;
+  bool have_plan = false;
   for (int64_t bi = b0; bi < b1; ++bi) {
     const reshard_tblock_t blk = p.blocks[bi];
     const uint32_t L = blk.row_bytes, nr = blk.nrows, K = blk.seg_count;
     const uint32_t n = L * nr;
     const bool gather = blk.direction == 0;
+    // the shape of the previous block of this CTA: plans, segment layout and
+    // replica pointers stay, only the offsets move
+    const bool same = have_plan && (blk.flags & RESHARD_TBLOCK_SAME_SHAPE) != 0;
     __syncthreads();  // the previous block is completely done with its image, si and ptrs
     const uint32_t buf = (DB && !gather) ? (nscatter & 1u) : 0u;
     unsigned char* img = dyn + buf * kImageBytes;
@@ -303,35 +382,41 @@ __global__ void __launch_bounds__(kTThreads, 4)
     if (gather) {
       const uint32_t g0 = p.goff[blk.wide];
       R = int(p.goff[blk.wide + 1] - g0);
-      for (int i = threadIdx.x; i < R; i += kTThreads) ptrs[i] = p.bufs[p.gbuf[g0 + i]];
+      if (!same)
+        for (int i = threadIdx.x; i < R; i += kTThreads) ptrs[i] = p.bufs[p.gbuf[g0 + i]];
     } else {
       wsrc = p.bufs[blk.wide] + blk.wide_off;
     }
+    if (threadIdx.x == 0) s_align = L;
     __syncthreads();
     const uint32_t mis = gather ? uint32_t(reinterpret_cast<uintptr_t>(ptrs[0] + blk.wide_off) & 15u)
                                 : uint32_t(reinterpret_cast<uintptr_t>(wsrc) & 15u);
-    if (threadIdx.x == 0) s_align = L;
-    __syncthreads();
     // per-segment set-up (one thread per segment), alignment of every narrow access
     for (uint32_t k = threadIdx.x; k < K; k += kTThreads) {
       const reshard_tseg_t sg = p.segs[blk.seg_begin + k];
       unsigned int a = sg.width | (mis + sg.col);
+      uint32_t gm;
       if (gather) {
         si[k].src = p.bufs[sg.narrow] + sg.narrow_off;
-        si[k].gmis = unsigned(reinterpret_cast<uintptr_t>(si[k].src) & 15u);
+        gm = unsigned(reinterpret_cast<uintptr_t>(si[k].src) & 15u);
         a |= unsigned(reinterpret_cast<uintptr_t>(si[k].src));
       } else {
         si[k].off = sg.narrow_off;
         const uint32_t g0 = p.goff[sg.narrow];
-        const uint32_t rc = p.goff[sg.narrow + 1] - g0;
-        si[k].rcnt = rc;
-        si[k].gmis =
-            unsigned(reinterpret_cast<uintptr_t>(p.bufs[p.gbuf[g0]] + sg.narrow_off) & 15u);
-        a |= si[k].gmis;
+        if (!same) si[k].rcnt = p.goff[sg.narrow + 1] - g0;
+        gm = unsigned(reinterpret_cast<uintptr_t>(p.bufs[p.gbuf[g0]] + sg.narrow_off) & 15u);
+        a |= gm;
       }
-      si[k].nbytes = sg.width * nr;
-      si[k].col = sg.col;
-      si[k].units = sg.width;  // bytes for now
+      if (same) {
+        // a segment whose narrow start moved mod 16 has its granules replanned
+        si[k].moved = si[k].moved | (gm != si[k].gmis ? 1u : 0u);
+      } else {
+        si[k].nbytes = sg.width * nr;
+        si[k].col = sg.col;
+        si[k].units = sg.width;  // bytes for now
+        si[k].moved = 0;
+      }
+      si[k].gmis = gm;
       atomicOr(&s_align, a);
     }
     __syncthreads();
@@ -352,59 +437,137 @@ __global__ void __launch_bounds__(kTThreads, 4)
     }
     if ((s_align & uint32_t(U - 1)) != 0) {
       if (threadIdx.x == 0) atomicExch(p.status, staging::kStatusTransposeAlign);
+      have_plan = false;
       continue;  // uniform: every thread read the same s_align
     }
-    if (threadIdx.x < 32) {
-      // staging granules and replica pointer slots, exclusive prefix in segment order:
-      // each lane owns segments [4 lane, 4 lane + 4) (K <= 128), then a warp scan
-      const int lane = int(threadIdx.x);
-      uint32_t rc[4], gc[4], rsum = 0, gsum = 0;
+    const bool replan = !same;
+    if (replan) {
+      if (threadIdx.x < 32) {
+        // granules and replica pointer slots, exclusive prefix in segment order:
+        // each lane owns segments [4 lane, 4 lane + 4) (K <= 128), then a warp scan.
+        // A segment gets as many granules as its narrow range can touch at any
+        // start mod 16, so the numbering holds for every block of the same shape
+        // (the granules a start does not touch are empty).
+        const int lane = int(threadIdx.x);
+        uint32_t rc[4], gc[4], rsum = 0, gsum = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t k = uint32_t(4 * lane + q);
-        rc[q] = (k < K && !gather) ? si[k].rcnt : 0u;
-        gc[q] = k < K ? (si[k].gmis + si[k].nbytes + 15u) >> 4 : 0u;
-        rsum += rc[q];
-        gsum += gc[q];
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t k = uint32_t(4 * lane + q);
+          rc[q] = (k < K && !gather) ? si[k].rcnt : 0u;
+          gc[q] = k < K ? (si[k].nbytes + 30u) >> 4 : 0u;
+          rsum += rc[q];
+          gsum += gc[q];
+        }
+        uint32_t rinc = rsum, ginc = gsum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t b = __shfl_up_sync(0xffffffffu, rinc, d);
+          const uint32_t c = __shfl_up_sync(0xffffffffu, ginc, d);
+          if (lane >= d) {
+            rinc += b;
+            ginc += c;
+          }
+        }
+        uint32_t rb = rinc - rsum, gs = ginc - gsum;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t k = uint32_t(4 * lane + q);
+          if (k < K) {
+            if (!same) si[k].units /= U;
+            si[k].rbeg = rb;
+            si[k].gstart = gs;
+            si[k].moved = 0;
+          }
+          rb += rc[q];
+          gs += gc[q];
+        }
+        if (lane == 31) s_ngran = ginc;
       }
-      uint32_t rinc = rsum, ginc = gsum;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t b = __shfl_up_sync(0xffffffffu, rinc, d);
-        const uint32_t c = __shfl_up_sync(0xffffffffu, ginc, d);
-        if (lane >= d) {
-          rinc += b;
-          ginc += c;
+      __syncthreads();
+      for (uint32_t k = threadIdx.x; k < K; k += kTThreads) {
+        if (!same) fastdiv_init(si[k].units, &si[k].m, &si[k].l);
+        if (!gather) {
+          const uint32_t g0 = p.goff[p.segs[blk.seg_begin + k].narrow];
+          for (uint32_t r = 0; r < si[k].rcnt; ++r) ptrs[si[k].rbeg + r] = p.bufs[p.gbuf[g0 + r]];
         }
       }
-      uint32_t rb = rinc - rsum, gs = ginc - gsum;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t k = uint32_t(4 * lane + q);
-        if (k < K) {
-          si[k].units /= U;
-          si[k].rbeg = rb;
-          si[k].gstart = gs;
-        }
-        rb += rc[q];
-        gs += gc[q];
-      }
-      if (lane == 31) s_ngran = ginc;
+      __syncthreads();
     }
-    __syncthreads();
-    for (uint32_t k = threadIdx.x; k < K; k += kTThreads) {
-      fastdiv_init(si[k].units, &si[k].m, &si[k].l);
-      if (!gather) {
-        const reshard_tseg_t sg = p.segs[blk.seg_begin + k];
-        const uint32_t g0 = p.goff[sg.narrow];
-        for (uint32_t r = 0; r < si[k].rcnt; ++r) ptrs[si[k].rbeg + r] = p.bufs[p.gbuf[g0 + r]];
-      }
-    }
-    __syncthreads();
     const uint32_t ngran = s_ngran;
+    // this thread's plans: made for a new shape, redone for segments that moved
+#pragma unroll
+    for (int sl = 0; sl < kSlots; ++sl) {
+      const uint32_t g = threadIdx.x + uint32_t(sl) * kTThreads;
+      if (g >= ngran) {
+        plan[sl] = 0u;  // kind none
+      } else if (replan) {
+        const uint32_t k = uint32_t(find_granule(si, int(K), g));
+        plan[sl] = plan_of<U>(si[k], k, g - si[k].gstart, L);
+      } else {
+        const uint32_t k = plan_k(plan[sl]);
+        if (si[k].moved) plan[sl] = plan_of<U>(si[k], k, g - si[k].gstart, L);
+      }
+    }
+    have_plan = true;
+    // granules beyond the planned slots (blocks of unusually many granules)
+    const uint32_t g_extra = uint32_t(kSlots) * kTThreads;
 
     if (gather) {
-      gather_direct<U>(si, int(K), ngran, img, mis, L);
+      // each thread loads whole aligned 16-byte granules of the segments' dense
+      // source ranges (all its slots in flight) and puts their elements into the
+      // image columns they belong to
+      uint32_t unused[4] = {0u, 0u, 0u, 0u};
+      constexpr int kHalf = kSlots / 2;
+#pragma unroll
+      for (int h0 = 0; h0 < kSlots; h0 += kHalf) {
+        uint4 v[kHalf];
+#pragma unroll
+        for (int q = 0; q < kHalf; ++q) {
+          const uint32_t meta = plan[h0 + q];
+          if (plan_kind(meta) != kKindNone) {
+            const SegInfo& s = si[plan_k(meta)];
+            const uint32_t g = threadIdx.x + uint32_t(h0 + q) * kTThreads;
+            v[q] = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(g - s.gstart)));
+          }
+        }
+        if (h0 == 0) {
+          // this thread's partial granule (threads < 2 K), while its loads are in flight
+          uint32_t k, j;
+          if (threadIdx.x < 2 * K && edge_granule<U>(si, threadIdx.x, &k, &j)) {
+            const SegInfo& s = si[k];
+            const uint32_t meta = plan_of<U, true>(s, k, j, L);
+            if (plan_kind(meta) != kKindNone) {
+              uint32_t lo, hi;
+              granule_span(s, j, &lo, &hi);
+              const uint4 w = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(j)));
+              granule_move<U, true>(s, meta, lo, hi, img + mis + plan_off(meta), L, unused, w);
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kHalf; ++q) {
+          const uint32_t meta = plan[h0 + q];
+          if (plan_kind(meta) == kKindNone) continue;
+          const SegInfo& s = si[plan_k(meta)];
+          uint32_t lo = 0u, hi = 16u;
+          if (plan_kind(meta) == kKindWalk) {
+            const uint32_t g = threadIdx.x + uint32_t(h0 + q) * kTThreads;
+            granule_span(s, g - s.gstart, &lo, &hi);
+          }
+          granule_move<U, true>(s, meta, lo, hi, img + mis + plan_off(meta), L, unused, v[q]);
+        }
+      }
+      // whole granules beyond the planned slots, then the partial ones
+      for (uint32_t g = g_extra + threadIdx.x; g < ngran; g += kTThreads) {
+        const uint32_t k = uint32_t(find_granule(si, int(K), g));
+        const SegInfo& s = si[k];
+        const uint32_t meta = plan_of<U>(s, k, g - s.gstart, L);
+        if (plan_kind(meta) == kKindNone) continue;
+        uint32_t lo, hi;
+        granule_span(s, g - s.gstart, &lo, &hi);
+        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(g - s.gstart)));
+        granule_move<U, true>(s, meta, lo, hi, img + mis + plan_off(meta), L, unused, w);
+      }
       __syncthreads();
       // image [mis, mis + n) -> each replica's [wide_off, wide_off + n)
       const uint32_t h = min((16u - mis) & 15u, n);
@@ -422,29 +585,82 @@ __global__ void __launch_bounds__(kTThreads, 4)
                  *reinterpret_cast<const uint4*>(img + mis + h + 16 * k));
         for (uint32_t i = h + 16 * m16 + threadIdx.x; i < n; i += kTThreads) d[i] = img[mis + i];
       }
-    } else if constexpr (DB) {
-      // the wide rows arrived by the bulk copy waited for above
-      scatter_direct<U>(si, int(K), ngran, img, mis, L, ptrs);
     } else {
-      // wide rows -> image, 16-byte loads from the aligned granules holding them
-      const unsigned char* base = wsrc - mis;
-      const uint32_t nv = (mis + n + 15u) >> 4;
+      if constexpr (!DB) {
+        // wide rows -> image, 16-byte loads from the aligned granules holding them
+        const unsigned char* base = wsrc - mis;
+        const uint32_t nv = (mis + n + 15u) >> 4;
 #pragma unroll 1
-      for (uint32_t k0 = threadIdx.x; k0 < nv; k0 += kTThreads * kTVecUnroll) {
-        uint4 v[kTVecUnroll];
+        for (uint32_t k0 = threadIdx.x; k0 < nv; k0 += kTThreads * kTVecUnroll) {
+          uint4 v[kTVecUnroll];
 #pragma unroll
-        for (int j = 0; j < kTVecUnroll; ++j) {
-          const uint32_t k = k0 + j * kTThreads;
-          if (k < nv) v[j] = __ldcs(reinterpret_cast<const uint4*>(base + 16 * k));
+          for (int j = 0; j < kTVecUnroll; ++j) {
+            const uint32_t k = k0 + j * kTThreads;
+            if (k < nv) v[j] = __ldcs(reinterpret_cast<const uint4*>(base + 16 * k));
+          }
+#pragma unroll
+          for (int j = 0; j < kTVecUnroll; ++j) {
+            const uint32_t k = k0 + j * kTThreads;
+            if (k < nv) *reinterpret_cast<uint4*>(img + 16 * k) = v[j];
+          }
         }
+        __syncthreads();
+      }
+      // (DB: the wide rows arrived by the bulk copy waited for above)
+      // each thread builds whole 16-byte granules of the segments' dense destination
+      // ranges (aligned like replica 0) from the image and writes them to every
+      // replica of the segment
+      const uint4 none = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int j = 0; j < kTVecUnroll; ++j) {
-          const uint32_t k = k0 + j * kTThreads;
-          if (k < nv) *reinterpret_cast<uint4*>(img + 16 * k) = v[j];
+      for (int sl = 0; sl < kSlots; ++sl) {
+        if (sl == 1) {
+          // this thread's partial granule (threads < 2 K), between its planned ones so
+          // that it overlaps the other warps' work
+          uint32_t k, j;
+          if (threadIdx.x < 2 * K && edge_granule<U>(si, threadIdx.x, &k, &j)) {
+            const SegInfo& s = si[k];
+            const uint32_t meta = plan_of<U, true>(s, k, j, L);
+            if (plan_kind(meta) != kKindNone) {
+              uint32_t lo, hi;
+              granule_span(s, j, &lo, &hi);
+              uint32_t words[4] = {0u, 0u, 0u, 0u};
+              granule_move<U, false>(s, meta, lo, hi, img + mis + plan_off(meta), L, words, none);
+              scatter_store(s, j, lo, hi, words, ptrs);
+            }
+          }
+        }
+        const uint32_t meta = plan[sl];
+        if (plan_kind(meta) == kKindNone) continue;
+        const SegInfo& s = si[plan_k(meta)];
+        const uint32_t j = threadIdx.x + uint32_t(sl) * kTThreads - s.gstart;
+        uint32_t words[4] = {0u, 0u, 0u, 0u};
+        if (plan_kind(meta) != kKindWalk) {
+          // a whole granule: with one replica, one aligned store
+          granule_move<U, false>(s, meta, 0u, 16u, img + mis + plan_off(meta), L, words, none);
+          if (s.rcnt == 1)
+            __stcs(reinterpret_cast<uint4*>(ptrs[s.rbeg] + s.off - s.gmis + 16 * size_t(j)),
+                   make_uint4(words[0], words[1], words[2], words[3]));
+          else
+            scatter_store(s, j, 0u, 16u, words, ptrs);
+        } else {
+          uint32_t lo, hi;
+          granule_span(s, j, &lo, &hi);
+          granule_move<U, false>(s, meta, lo, hi, img + mis + plan_off(meta), L, words, none);
+          scatter_store(s, j, lo, hi, words, ptrs);
         }
       }
-      __syncthreads();
-      scatter_direct<U>(si, int(K), ngran, img, mis, L, ptrs);
+      // whole granules beyond the planned slots, then the partial ones
+      for (uint32_t g = g_extra + threadIdx.x; g < ngran; g += kTThreads) {
+        const uint32_t k = uint32_t(find_granule(si, int(K), g));
+        const SegInfo& s = si[k];
+        const uint32_t meta = plan_of<U>(s, k, g - s.gstart, L);
+        if (plan_kind(meta) == kKindNone) continue;
+        uint32_t lo, hi;
+        granule_span(s, g - s.gstart, &lo, &hi);
+        uint32_t words[4] = {0u, 0u, 0u, 0u};
+        granule_move<U, false>(s, meta, lo, hi, img + mis + plan_off(meta), L, words, none);
+        scatter_store(s, g - s.gstart, lo, hi, words, ptrs);
+      }
     }
   }
 }

@@ -192,7 +192,12 @@ typedef struct reshard_tile {
  * or splits the rows in shared memory, so both sides move contiguous bytes.
  *   direction 0 (gather):  narrow sources -> wide destination group;
  *   direction 1 (scatter): wide source -> narrow destination groups.
+ * flags: RESHARD_TBLOCK_SAME_SHAPE when the block has the shape of the block
+ * before it in the program (same wide side, direction, row length, rows, and
+ * segments of the same widths, columns and narrow sides in the same order; only
+ * the offsets differ), so a kernel may keep what it derived from that shape.
  */
+#define RESHARD_TBLOCK_SAME_SHAPE 1u
 typedef struct reshard_tblock {
   int64_t wide_off;    /* bytes: row 0 of the block in the wide buffer(s) */
   uint32_t row_bytes;  /* wide row length */
@@ -200,7 +205,7 @@ typedef struct reshard_tblock {
   uint32_t seg_begin, seg_count;
   uint16_t wide;       /* gather: destination group; scatter: source buffer index */
   uint16_t direction;  /* 0 gather, 1 scatter */
-  uint32_t pad;
+  uint32_t flags;      /* RESHARD_TBLOCK_* bits */
 } reshard_tblock_t;
 
 typedef struct reshard_tseg {

@@ -95,6 +95,23 @@ def test_transpose_rule_for_narrow_pieces(oracle, case, transposed):
     plan = _check_spec(oracle, spec)
     blocks, _ = rs.reshard_plan_transposes(plan, rs.PROGRAM_FANOUT)
     assert bool(blocks) == transposed
+    # a block flagged as having the previous block's shape has it: same wide side,
+    # direction, rows and segments (widths, columns, narrow sides), other offsets
+    blocks, segs = rs.reshard_plan_transposes(plan, rs.PROGRAM_FANOUT)
+    flagged = 0
+    for i, b in enumerate(blocks):
+        if not b["flags"] & 1:
+            continue
+        flagged += 1
+        assert i > 0
+        a = blocks[i - 1]
+        for f in ("wide", "direction", "row_bytes", "nrows", "seg_count"):
+            assert a[f] == b[f], (i, f)
+        for k in range(b["seg_count"]):
+            x, y = segs[a["seg_begin"] + k], segs[b["seg_begin"] + k]
+            assert (x["width"], x["col"], x["narrow"]) == (y["width"], y["col"], y["narrow"])
+    if blocks:
+        assert flagged >= len(blocks) // 2 or len(blocks) < 4
     # transpose blocks are a fan-out device only: the box-copy, gather, slice and
     # replicate programs (which the allocation-free entry point runs from tables at
     # explicit addresses) stay tiles alone
