@@ -549,7 +549,11 @@ reshard_status_t build_plan(reshard_plan_s* P) {
             // only the offsets move): the kernel keeps what it worked out for it
             if (r0 > 0 || pl > 0) {
               const int64_t prev_rows = r0 > 0 ? nb : std::min(nb, rows - (rows - 1) / nb * nb);
-              if (std::min(nb, rows - r0) == prev_rows) blk.flags = RESHARD_TBLOCK_SAME_SHAPE;
+              if (std::min(nb, rows - r0) == prev_rows) {
+                blk.flags = RESHARD_TBLOCK_SAME_SHAPE;
+                // inside a plane its rows and narrow ranges also follow the previous ones
+                if (r0 > 0) blk.flags |= RESHARD_TBLOCK_FOLLOWS;
+              }
             }
             blk.wide_off = wide_base + pl * wide_pstride + r0 * L;
             blk.row_bytes = uint32_t(L);

@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
   // uniform over the CTA: scatter blocks seen, loads issued per image, wait parities
   uint32_t nscatter = 0, pending = 0, parity = 0;
   bool have_plan = false;
+  int R = 0;  // gather: replicas of the wide destination group (in ptrs[0..R))
   for (int64_t bi = b0; bi < b1; ++bi) {
     const reshard_tblock_t blk = p.blocks[bi];
     const uint32_t L = blk.row_bytes, nr = blk.nrows, K = blk.seg_count;
@@ -361,6 +362,10 @@ __global__ void __launch_bounds__(kTThreads, 4)
     // the shape of the previous block of this CTA: plans, segment layout and
     // replica pointers stay, only the offsets move
     const bool same = have_plan && (blk.flags & RESHARD_TBLOCK_SAME_SHAPE) != 0;
+    // ... and its rows and narrow ranges follow the previous block's: every offset
+    // advances by rows x width, with no segment record to read and no alignment to
+    // check again (the advances are multiples of the element width)
+    const bool follows = same && (blk.flags & RESHARD_TBLOCK_FOLLOWS) != 0;
     __syncthreads();  // the previous block is completely done with its image, si and ptrs
     const uint32_t buf = (DB && !gather) ? (nscatter & 1u) : 0u;
     unsigned char* img = dyn + buf * kImageBytes;
@@ -377,22 +382,33 @@ __global__ void __launch_bounds__(kTThreads, 4)
       }
     }
     // wide-side pointers: gather -> the destination group in ptrs[0..R); scatter -> source
-    int R = 0;
     const unsigned char* wsrc = nullptr;
     if (gather) {
-      const uint32_t g0 = p.goff[blk.wide];
-      R = int(p.goff[blk.wide + 1] - g0);
-      if (!same)
+      if (!same) {  // (a block of the same shape has the same destination group)
+        const uint32_t g0 = p.goff[blk.wide];
+        R = int(p.goff[blk.wide + 1] - g0);
         for (int i = threadIdx.x; i < R; i += kTThreads) ptrs[i] = p.bufs[p.gbuf[g0 + i]];
+      }
     } else {
       wsrc = p.bufs[blk.wide] + blk.wide_off;
     }
-    if (threadIdx.x == 0) s_align = L;
+    if (follows) {
+      for (uint32_t k = threadIdx.x; k < K; k += kTThreads) {
+        const uint32_t adv = si[k].nbytes;  // rows x width
+        if (gather) si[k].src += adv;
+        else si[k].off += adv;
+        const uint32_t gm = (si[k].gmis + adv) & 15u;
+        si[k].moved = si[k].moved | (gm != si[k].gmis ? 1u : 0u);
+        si[k].gmis = gm;
+      }
+    } else {
+      if (threadIdx.x == 0) s_align = L;
+    }
     __syncthreads();
     const uint32_t mis = gather ? uint32_t(reinterpret_cast<uintptr_t>(ptrs[0] + blk.wide_off) & 15u)
                                 : uint32_t(reinterpret_cast<uintptr_t>(wsrc) & 15u);
     // per-segment set-up (one thread per segment), alignment of every narrow access
-    for (uint32_t k = threadIdx.x; k < K; k += kTThreads) {
+    for (uint32_t k = threadIdx.x; k < K && !follows; k += kTThreads) {
       const reshard_tseg_t sg = p.segs[blk.seg_begin + k];
       unsigned int a = sg.width | (mis + sg.col);
       uint32_t gm;
@@ -419,7 +435,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
       si[k].gmis = gm;
       atomicOr(&s_align, a);
     }
-    __syncthreads();
+    if (!follows) __syncthreads();  // uniform
     if (DB && !gather) {
       // this block's image (every thread polls; the outcome is made uniform)
       const bool landed = staging::mbar_wait(&s_bar[buf], (parity >> buf) & 1u,
@@ -435,7 +451,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
         return;
       }
     }
-    if ((s_align & uint32_t(U - 1)) != 0) {
+    if (!follows && (s_align & uint32_t(U - 1)) != 0) {
       if (threadIdx.x == 0) atomicExch(p.status, staging::kStatusTransposeAlign);
       have_plan = false;
       continue;  // uniform: every thread read the same s_align

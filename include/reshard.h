@@ -195,9 +195,13 @@ typedef struct reshard_tile {
  * flags: RESHARD_TBLOCK_SAME_SHAPE when the block has the shape of the block
  * before it in the program (same wide side, direction, row length, rows, and
  * segments of the same widths, columns and narrow sides in the same order; only
- * the offsets differ), so a kernel may keep what it derived from that shape.
+ * the offsets differ), so a kernel may keep what it derived from that shape;
+ * RESHARD_TBLOCK_FOLLOWS (with SAME_SHAPE) when moreover its wide rows and every
+ * narrow range start right where the previous block's end (offsets advanced by
+ * nrows x row_bytes and nrows x width).
  */
 #define RESHARD_TBLOCK_SAME_SHAPE 1u
+#define RESHARD_TBLOCK_FOLLOWS 2u
 typedef struct reshard_tblock {
   int64_t wide_off;    /* bytes: row 0 of the block in the wide buffer(s) */
   uint32_t row_bytes;  /* wide row length */

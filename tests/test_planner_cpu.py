@@ -110,6 +110,10 @@ def test_transpose_rule_for_narrow_pieces(oracle, case, transposed):
         for k in range(b["seg_count"]):
             x, y = segs[a["seg_begin"] + k], segs[b["seg_begin"] + k]
             assert (x["width"], x["col"], x["narrow"]) == (y["width"], y["col"], y["narrow"])
+            if b["flags"] & 2:   # follows: offsets advanced by the previous block's rows
+                assert y["narrow_off"] == x["narrow_off"] + a["nrows"] * x["width"]
+        if b["flags"] & 2:
+            assert b["wide_off"] == a["wide_off"] + a["nrows"] * a["row_bytes"]
     if blocks:
         assert flagged >= len(blocks) // 2 or len(blocks) < 4
     # transpose blocks are a fan-out device only: the box-copy, gather, slice and
