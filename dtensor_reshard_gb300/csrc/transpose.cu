@@ -294,6 +294,15 @@ __device__ __forceinline__ void granule_move(const SegInfo& s, uint32_t meta, ui
   }
 }
 
+// gather: an aligned 16-byte granule of a narrow source range, with the normal
+// cache policy.  A block's range shares its first and last 32-byte sectors with
+// the neighbouring blocks' ranges; evict-first loads dropped those sectors before
+// the neighbour read its half, and the narrow side was read from DRAM 1.5 times
+// (a gather of 58-byte pieces into 12 replicas).
+__device__ __forceinline__ uint4 narrow_load(const unsigned char* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
 // scatter: a granule built from the image goes to every replica of its segment.
 __device__ __forceinline__ void scatter_store(const SegInfo& s, uint32_t j, uint32_t lo,
                                               uint32_t hi, const uint32_t (&words)[4],
@@ -543,7 +552,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
           if (plan_kind(meta) != kKindNone) {
             const SegInfo& s = si[plan_k(meta)];
             const uint32_t g = threadIdx.x + uint32_t(h0 + q) * kTThreads;
-            v[q] = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(g - s.gstart)));
+            v[q] = narrow_load(s.src - s.gmis + 16 * size_t(g - s.gstart));
           }
         }
         if (h0 == 0) {
@@ -555,7 +564,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
             if (plan_kind(meta) != kKindNone) {
               uint32_t lo, hi;
               granule_span(s, j, &lo, &hi);
-              const uint4 w = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(j)));
+              const uint4 w = narrow_load(s.src - s.gmis + 16 * size_t(j));
               granule_move<U, true>(s, meta, lo, hi, img + mis + plan_off(meta), L, unused, w);
             }
           }
@@ -581,7 +590,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
         if (plan_kind(meta) == kKindNone) continue;
         uint32_t lo, hi;
         granule_span(s, g - s.gstart, &lo, &hi);
-        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(s.src - s.gmis + 16 * size_t(g - s.gstart)));
+        const uint4 w = narrow_load(s.src - s.gmis + 16 * size_t(g - s.gstart));
         granule_move<U, true>(s, meta, lo, hi, img + mis + plan_off(meta), L, unused, w);
       }
       __syncthreads();
