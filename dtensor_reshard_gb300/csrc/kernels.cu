@@ -16,7 +16,7 @@
 // per thread whatever the vector width), and each loaded vector is
 // stored to every destination buffer of the tile's group (the fan-out: the
 // source region is read from HBM once, written R times).  Loads and stores use
-// the evict-first (streaming) cache policy because no byte is touched twice.
+// the normal cache policy (see load_stream).
 //
 // There is no tensor-core work here: a reshard is a pure byte copy, bounded by
 // HBM bandwidth.
@@ -67,13 +67,23 @@ template <> struct Vec<4> { using T = unsigned int; };
 template <> struct Vec<2> { using T = unsigned short; };
 template <> struct Vec<1> { using T = unsigned char; };
 
+// Loads and stores of the element kernel keep the normal cache policy: rows that
+// do not start or end on a 32-byte sector share those sectors with other tiles,
+// which evict-first accesses dropped from L2 before the other tile's access
+// (measured per tensor: 12-20% on short-row scatters and gathers, no change on
+// long runs).
 template <typename T>
 __device__ __forceinline__ T load_stream(const unsigned char* p) {
-  return __ldcs(reinterpret_cast<const T*>(p));
+  return *reinterpret_cast<const T*>(p);
 }
 template <typename T>
 __device__ __forceinline__ void store_stream(unsigned char* p, const T& v) {
-  __stcs(reinterpret_cast<T*>(p), v);
+  *reinterpret_cast<T*>(p) = v;
+}
+// The register realigning kernel's stores stay evict-first (measured 3% faster
+// there on a 6-replica fan-out of 13 KB rows).
+__device__ __forceinline__ void store_evict_first(unsigned char* p, const uint4& v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
 // Bytes [0, nbytes) of a contiguous run: from src to dst + dofs for each of
@@ -291,7 +301,7 @@ __device__ __forceinline__ void realigned_body(const unsigned char* base, uint32
 #pragma unroll
       for (int j = 0; j < kRealignUnroll; ++j) {
         const uint32_t k = k0 + j * nthr;
-        if (k < m) store_stream<uint4>(d + size_t(k) * 16, out[j]);
+        if (k < m) store_evict_first(d + size_t(k) * 16, out[j]);
       }
     }
   }
