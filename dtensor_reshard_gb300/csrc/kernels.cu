@@ -471,8 +471,10 @@ const KernelFn kKernels[2][6][2] = {
 //     large enough to fill its pipelines, else the register realigning kernel
 //     when most bytes are in rows of at least 512 bytes;
 //   one replica, rows of at least 512 bytes: the staged kernel when the
-//     element width would be 1 or 2 bytes, or 4 bytes in a large program (its
-//     loads stay wide whatever the alignment);
+//     element width would be 1 or 2 bytes, or 4 bytes in a large program made
+//     mostly of rows of at least 8 KiB (long runs: its loads stay wide whatever
+//     the alignment; on 0.6-1.4 KB rows the element kernel, with 64 bytes in
+//     flight per thread, was measured 11-29% faster);
 //   otherwise the element-width kernel.
 int choose_kernel(const Program& prog, int w_log2) {
   if (w_log2 == 4) return 4;
@@ -481,7 +483,8 @@ int choose_kernel(const Program& prog, int w_log2) {
   if (prog.max_fanout >= 2) {
     if (wide_rows && prog.tile_bytes >= kStagedFanoutMinBytes) return kStagedRealign;
     if (long_rows) return 0;
-  } else if (long_rows && (w_log2 <= 1 || (w_log2 == 2 && prog.tile_bytes >= kStagedW4MinBytes))) {
+  } else if (long_rows && (w_log2 <= 1 || (w_log2 == 2 && wide_rows &&
+                                            prog.tile_bytes >= kStagedW4MinBytes))) {
     return kStagedRealign;
   }
   return w_log2 == 0 ? 5 : w_log2;

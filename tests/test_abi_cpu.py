@@ -208,6 +208,10 @@ def _fake_ptrs(plan, side, n, mis):
     ((2000, 1301), "bf16", (3,), ("S0",), (2,), ("S0",), 3, 3, 0, ("staged", 1)),
     # one replica, 8-byte alignment: element kernel
     ((6971, 7418), "fp32", (49,), ("S1",), (10,), ("S1",), 0, 0, 0, ("vector", 8)),
+    # one replica at 4-byte alignment: the staged kernel for long runs of a large
+    # program, the element kernel for rows of 1372 bytes
+    ((880, 3593, 34), "fp16", (1,), ("R",), (15,), ("S0",), 0, 0, 0, ("staged", 4)),
+    ((6401, 8213), "fp32", (7,), ("S0",), (24,), ("S1",), 0, 0, 0, ("vector", 4)),
     # short rows (< 512 bytes): element kernel
     ((1000, 37), "bf16", (3,), ("S1",), (7,), ("S0",), 0, 0, 0, ("vector", 2)),
     # fan-out, small or not in wide rows: register realigning kernel
