@@ -74,15 +74,17 @@ struct Config {
 // into its granule and whose first source byte is staged at stage + spos.
 // Byte j of the granule is row byte 16k + j - dmis, staged at
 // stage + spos - dmis + 16k + j (spos >= kHead, so the start is in the stage).
+// The granule is five aligned 4-byte stage words funnel-shifted by the byte
+// offset (no run-time word selection; the reads stay inside the 32 bytes from
+// the aligned 16 bytes that hold its first byte).
 __device__ __forceinline__ uint4 granule(const unsigned char* stage, uint32_t spos, uint32_t dmis,
                                          uint32_t k) {
   const uint32_t at = spos - dmis + 16u * k;
-  const uint32_t o = at & 15u;
-  const unsigned char* a = stage + (at - o);
-  const uint4 A = *reinterpret_cast<const uint4*>(a);
-  if (o == 0) return A;
-  const uint4 B = *reinterpret_cast<const uint4*>(a + 16);
-  return funnel16(A, B, o >> 2, 0x3210u + 0x1111u * (o & 3u));
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(stage + (at & ~3u));
+  const uint32_t sh = 8u * (at & 3u);
+  const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = sh ? w[4] : 0u;
+  return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                    __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
 }
 
 // Granule k (bytes v) of a row to one replica: dst + doff is the row's first
