@@ -184,7 +184,7 @@ int64_t tile_bytes(const reshard_tile_t& t);
 constexpr int64_t kTransposeMaxWidth = 129;
 constexpr int64_t kTransposeBlockBytes = 20 * 1024;
 // Blocks a transpose group aims for (smaller blocks when the group is small).
-constexpr int64_t kTransposeMinBlocks = 512;
+constexpr int64_t kTransposeMinBlocks = 128;
 // Most segments one transpose group may have (the kernel stages them in shared memory).
 constexpr int64_t kTransposeMaxSegs = 128;
 // Most narrow replica pointers one scatter block may address.
