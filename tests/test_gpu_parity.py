@@ -827,6 +827,38 @@ def test_staged_realign_fanout(oracle, dst_mis, want):
     run_and_compare(oracle, BULK_SPEC, misalign=0, dst_misalign=dst_mis, expect_path=want)
 
 
+# Short rows (32..481 bytes) off the 16-byte grid, one replica or replicas at one
+# address mod 16: the element kernel at the rows' common width.
+SHORT_ROW_CASES = [
+    # a column re-split of 2-byte elements: pieces of up to 160 bytes from 1-2 sources
+    ("resplit", _spec((731, 397), "fp16", (5,), ("S1",), (6,), ("S1",), seed=21)),
+    # 3-D tiles with planes (an innermost split into a middle-dim split)
+    ("planes", _spec((40, 60, 301), "fp16", (3,), ("S2",), (4,), ("S1",), seed=22)),
+    # rows of 474-480 bytes and 2-byte pieces beside them
+    ("long_short", _spec((300, 957), "bf16", (4,), ("S1",), (2,), ("S1",), seed=23)),
+    # 4-byte elements in rows of up to 448 bytes
+    ("fp32", _spec((500, 1003), "fp32", (7,), ("S1",), (9,), ("S1",), seed=24)),
+    # three replicas of every destination piece
+    ("fanout", _spec((900, 397), "fp16", (5,), ("S1",), (3, 2), ("R", "S1"), seed=25)),
+    # 410-byte rows from 818-byte source rows: every pair of source and destination
+    # offsets mod 16
+    ("all_offsets", _spec((1433, 409), "bf16", (4,), ("S0",), (2,), ("S1",), seed=26)),
+]
+
+
+@pytest.mark.parametrize("misalign", [0, 3])
+@pytest.mark.parametrize("i", range(len(SHORT_ROW_CASES)))
+def test_short_unaligned_rows(oracle, i, misalign):
+    name, spec = SHORT_ROW_CASES[i]
+    run_and_compare(oracle, spec, misalign=misalign, expect_path="vector")
+
+
+def test_short_rows_with_incongruent_replicas(oracle):
+    _, spec = SHORT_ROW_CASES[4]
+    run_and_compare(oracle, spec, misalign=0, dst_misalign=lambda r: (r * 6) % 16,
+                    expect_path="vector")
+
+
 def test_small_misaligned_fanout_uses_register_realign(oracle):
     spec = _spec((2000, 1301), "bf16", (3,), ("S0",), (2,), ("R",), seed=18)
     run_and_compare(oracle, spec, misalign=3, expect_path="realign")
