@@ -15,7 +15,7 @@
 //     position in the stage's row table;
 //   kConsumerWarps consumer warps cover every destination granule (16 aligned
 //     destination bytes) of every row with one thread, cutting the granule's
-//     bytes out of two 16-byte shared-memory words with byte permutes;
+//     bytes out of five aligned 4-byte stage words with funnel shifts;
 //   by default each consumer writes its granules to every replica itself
 //     with aligned 16-byte stores (one realignment when every destination
 //     buffer has the same address mod 16, one per replica otherwise; the
@@ -285,20 +285,15 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
       const uint32_t len = c.kind == 1 ? t.row_bytes : c.bytes;
       const uint32_t gmax = (len + 30u) >> 4;  // granules a row of len bytes can touch
       const uint32_t ost = Walker::out_stride(len);
-      const FastDiv32 by_g(gmax);
       const unsigned char* stage = in_mem + size_t(s) * kStageBytes;
       unsigned char* out = out_mem + size_t(o) * kStageBytes;
       unsigned char* const* dptr = dst_ptr[s];
-      const uint32_t items = nr * gmax;
-      for (uint32_t i = ct; i < items; i += kConsumerThreads) {
-        const uint32_t r = by_g.div(i);
-        const uint32_t k = i - r * gmax;
-        const int64_t doff = row_doff[s][r];
-        const uint32_t spos = row_spos[s][r];
+      // granule k of staged row r; dmis and G are the first replica's (every
+      // replica's on the bulk and congruent paths)
+      auto item = [&](uint32_t r, uint32_t k, int64_t doff, uint32_t spos, uint32_t dmis,
+                      uint32_t G) {
         if (bulk) {
-          const uint32_t dmis = uint32_t(reinterpret_cast<uintptr_t>(dptr[0] + doff) & 15u);
-          const uint32_t G = (dmis + len + 15u) >> 4;
-          if (k >= G) continue;
+          if (k >= G) return;
           const uint4 v = granule(stage, spos, dmis, k);
           uint32_t lo, hi;
           granule_span(dmis, len, G, k, &lo, &hi);
@@ -309,9 +304,7 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
               store_partial16(dptr[j] + doff - int64_t(dmis) + 16 * int64_t(k), v, lo, hi);
           }
         } else if (congruent) {
-          const uint32_t dmis = uint32_t(reinterpret_cast<uintptr_t>(dptr[0] + doff) & 15u);
-          const uint32_t G = (dmis + len + 15u) >> 4;
-          if (k >= G) continue;
+          if (k >= G) return;
           const uint4 v = granule(stage, spos, dmis, k);
           uint32_t lo, hi;
           granule_span(dmis, len, G, k, &lo, &hi);
@@ -323,10 +316,29 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
           }
         } else {
           for (int j = 0; j < R; ++j) {
-            const uint32_t dmis = uint32_t(reinterpret_cast<uintptr_t>(dptr[j] + doff) & 15u);
-            const uint32_t G = (dmis + len + 15u) >> 4;
-            if (k < G) put_granule(dptr[j], doff, dmis, len, G, k, granule(stage, spos, dmis, k));
+            const uint32_t dm = uint32_t(reinterpret_cast<uintptr_t>(dptr[j] + doff) & 15u);
+            const uint32_t Gj = (dm + len + 15u) >> 4;
+            if (k < Gj) put_granule(dptr[j], doff, dm, len, Gj, k, granule(stage, spos, dm, k));
           }
+        }
+      };
+      if (nr == 1) {
+        // one row (a piece of a run or of a long row): its offsets once per stage
+        const int64_t doff = row_doff[s][0];
+        const uint32_t spos = row_spos[s][0];
+        const uint32_t dmis = uint32_t(reinterpret_cast<uintptr_t>(dptr[0] + doff) & 15u);
+        const uint32_t G = (dmis + len + 15u) >> 4;
+        const uint32_t kend = bulk || congruent ? G : gmax;
+        for (uint32_t k = ct; k < kend; k += kConsumerThreads) item(0, k, doff, spos, dmis, G);
+      } else {
+        const FastDiv32 by_g(gmax);
+        const uint32_t items = nr * gmax;
+        for (uint32_t i = ct; i < items; i += kConsumerThreads) {
+          const uint32_t r = by_g.div(i);
+          const uint32_t k = i - r * gmax;
+          const int64_t doff = row_doff[s][r];
+          const uint32_t dmis = uint32_t(reinterpret_cast<uintptr_t>(dptr[0] + doff) & 15u);
+          item(r, k, doff, row_spos[s][r], dmis, (dmis + len + 15u) >> 4);
         }
       }
       if (bulk) {

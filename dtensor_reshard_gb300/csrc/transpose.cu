@@ -294,6 +294,25 @@ __device__ __forceinline__ void granule_move(const SegInfo& s, uint32_t meta, ui
   }
 }
 
+// a[i] for a run-time i (< N) by a chain of selects, so that a rolled loop over
+// the slots keeps them in registers.  The scatter's slot loop is rolled: its body
+// (every granule kind, inlined) is then emitted once instead of once per slot,
+// and its warps, at different slots, no longer stall on instruction fetch.  The
+// gather's stays unrolled (its granule loads of several slots are in flight at
+// once, and it was measured faster so).
+template <int N>
+__device__ __forceinline__ uint32_t pick(const uint32_t (&a)[N], int i) {
+  uint32_t r = a[0];
+#pragma unroll
+  for (int q = 1; q < N; ++q) r = i == q ? a[q] : r;
+  return r;
+}
+
+// every bulk copy this thread committed has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // gather: an aligned 16-byte granule of a narrow source range, with the normal
 // cache policy.  A block's range shares its first and last 32-byte sectors with
 // the neighbouring blocks' ranges; evict-first loads dropped those sectors before
@@ -375,6 +394,8 @@ __global__ void __launch_bounds__(kTThreads, 4)
     // advances by rows x width, with no segment record to read and no alignment to
     // check again (the advances are multiples of the element width)
     const bool follows = same && (blk.flags & RESHARD_TBLOCK_FOLLOWS) != 0;
+    // the previous gather block's bulk stores have read its image (thread 0 issued them)
+    if (threadIdx.x == 0) bulk_wait_read_all();
     __syncthreads();  // the previous block is completely done with its image, si and ptrs
     const uint32_t buf = (DB && !gather) ? (nscatter & 1u) : 0u;
     unsigned char* img = dyn + buf * kImageBytes;
@@ -456,7 +477,10 @@ __global__ void __launch_bounds__(kTThreads, 4)
         // give the other image's load, if one is on its way, its own bounded wait
         if ((pending >> (buf ^ 1u)) & 1u)
           staging::mbar_wait(&s_bar[buf ^ 1u], (parity >> (buf ^ 1u)) & 1u, staging::kWaitPolls);
-        if (threadIdx.x == 0) atomicExch(p.status, staging::kStatusConsumerWait);
+        if (threadIdx.x == 0) {
+          atomicExch(p.status, staging::kStatusConsumerWait);
+          staging::bulk_wait_all();
+        }
         return;
       }
     }
@@ -593,8 +617,13 @@ __global__ void __launch_bounds__(kTThreads, 4)
         const uint4 w = narrow_load(s.src - s.gmis + 16 * size_t(g - s.gstart));
         granule_move<U, true>(s, meta, lo, hi, img + mis + plan_off(meta), L, unused, w);
       }
+      // the image's bytes become visible to the bulk copies' (async) proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncthreads();
-      // image [mis, mis + n) -> each replica's [wide_off, wide_off + n)
+      // image [mis, mis + n) -> each replica's [wide_off, wide_off + n): the aligned
+      // middle by one bulk copy per replica (thread 0; the image is not written
+      // again before thread 0 has seen the copies read it), the partial head and
+      // tail granules by the threads
       const uint32_t h = min((16u - mis) & 15u, n);
       const uint32_t m16 = (n - h) >> 4;
       for (int r = 0; r < R; ++r) {
@@ -605,11 +634,10 @@ __global__ void __launch_bounds__(kTThreads, 4)
           continue;
         }
         for (uint32_t i = threadIdx.x; i < h; i += kTThreads) d[i] = img[mis + i];
-        for (uint32_t k = threadIdx.x; k < m16; k += kTThreads)
-          __stcs(reinterpret_cast<uint4*>(d + h + 16 * k),
-                 *reinterpret_cast<const uint4*>(img + mis + h + 16 * k));
+        if (m16 != 0 && threadIdx.x == 0) staging::bulk_store(d + h, img + mis + h, 16u * m16);
         for (uint32_t i = h + 16 * m16 + threadIdx.x; i < n; i += kTThreads) d[i] = img[mis + i];
       }
+      if (threadIdx.x == 0) staging::bulk_commit();
     } else {
       if constexpr (!DB) {
         // wide rows -> image, 16-byte loads from the aligned granules holding them
@@ -636,7 +664,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
       // ranges (aligned like replica 0) from the image and writes them to every
       // replica of the segment
       const uint4 none = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
+#pragma unroll 1
       for (int sl = 0; sl < kSlots; ++sl) {
         if (sl == 1) {
           // this thread's partial granule (threads < 2 K), between its planned ones so
@@ -654,7 +682,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
             }
           }
         }
-        const uint32_t meta = plan[sl];
+        const uint32_t meta = pick(plan, sl);
         if (plan_kind(meta) == kKindNone) continue;
         const SegInfo& s = si[plan_k(meta)];
         const uint32_t j = threadIdx.x + uint32_t(sl) * kTThreads - s.gstart;
@@ -688,6 +716,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
       }
     }
   }
+  if (threadIdx.x == 0) staging::bulk_wait_all();  // the last gather block's bulk stores
 }
 
 std::mutex g_t_mu;
