@@ -308,6 +308,21 @@ __device__ __forceinline__ uint32_t pick(const uint32_t (&a)[N], int i) {
   return r;
 }
 
+// A bulk copy shared -> global whose lines L2 evicts first: a gather's image goes
+// out once to each replica and is not read again, while the narrow source's
+// boundary granules are read again by the next block (with the normal policy the
+// image stores displaced them: reads of the 12-replica gather rose from 1.07 to
+// 1.39 times its source bytes).
+__device__ __forceinline__ void bulk_store_evict_first(void* gdst, const void* ssrc,
+                                                       uint32_t bytes) {
+  asm volatile(
+      "{ .reg .b64 pol; createpolicy.fractional.L2::evict_first.b64 pol, 1.0; "
+      "cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, pol; }" ::"l"(
+          gdst),
+      "r"(staging::smem_addr(ssrc)), "r"(bytes)
+      : "memory");
+}
+
 // every bulk copy this thread committed has finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -634,7 +649,7 @@ __global__ void __launch_bounds__(kTThreads, 4)
           continue;
         }
         for (uint32_t i = threadIdx.x; i < h; i += kTThreads) d[i] = img[mis + i];
-        if (m16 != 0 && threadIdx.x == 0) staging::bulk_store(d + h, img + mis + h, 16u * m16);
+        if (m16 != 0 && threadIdx.x == 0) bulk_store_evict_first(d + h, img + mis + h, 16u * m16);
         for (uint32_t i = h + 16 * m16 + threadIdx.x; i < n; i += kTThreads) d[i] = img[mis + i];
       }
       if (threadIdx.x == 0) staging::bulk_commit();

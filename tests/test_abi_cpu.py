@@ -212,8 +212,14 @@ def _fake_ptrs(plan, side, n, mis):
     # program, the element kernel for rows of 1372 bytes
     ((880, 3593, 34), "fp16", (1,), ("R",), (15,), ("S0",), 0, 0, 0, ("staged", 4)),
     ((6401, 8213), "fp32", (7,), ("S0",), (24,), ("S1",), 0, 0, 0, ("vector", 4)),
-    # short rows (< 512 bytes): element kernel
+    # narrow rows (< 32 bytes): element kernel
     ((1000, 37), "bf16", (3,), ("S1",), (7,), ("S0",), 0, 0, 0, ("vector", 2)),
+    # short rows (32..511 bytes) off the 16-byte grid: element kernel (a thread per
+    # element column, stepping down the rows, was measured faster than 16-byte
+    # granules realigned per row)
+    ((731, 397), "fp16", (5,), ("S1",), (6,), ("S1",), 0, 0, 0, ("vector", 2)),
+    ((731, 397), "fp16", (5,), ("S1",), (6,), ("S1",), 3, 3, 0, ("vector", 1)),
+    ((900, 397), "fp16", (5,), ("S1",), (3, 2), ("R", "S1"), 0, 5, 0, ("vector", 1)),
     # fan-out, small or not in wide rows: register realigning kernel
     ((2000, 1301), "bf16", (3,), ("S0",), (2,), ("R",), 3, 3, 0, ("realign", 1)),
     # fan-out of 52.8 MB in 16 MB runs: bulk stores, unless the replicas differ mod 16

@@ -827,7 +827,7 @@ def test_staged_realign_fanout(oracle, dst_mis, want):
     run_and_compare(oracle, BULK_SPEC, misalign=0, dst_misalign=dst_mis, expect_path=want)
 
 
-# Short rows (32..481 bytes) off the 16-byte grid, one replica or replicas at one
+# Short rows (32..511 bytes) off the 16-byte grid, one replica or replicas at one
 # address mod 16: the element kernel at the rows' common width.
 SHORT_ROW_CASES = [
     # a column re-split of 2-byte elements: pieces of up to 160 bytes from 1-2 sources
@@ -851,6 +851,15 @@ SHORT_ROW_CASES = [
 def test_short_unaligned_rows(oracle, i, misalign):
     name, spec = SHORT_ROW_CASES[i]
     run_and_compare(oracle, spec, misalign=misalign, expect_path="vector")
+
+
+@pytest.mark.parametrize("i", [0, 1, 5])
+def test_short_unaligned_rows_every_destination_offset(oracle, i):
+    """Destination rank r starts r bytes past its alignment: every destination
+    offset mod 16 against every source offset."""
+    _, spec = SHORT_ROW_CASES[i]
+    run_and_compare(oracle, spec, misalign=0, dst_misalign=lambda r: r % 16,
+                    expect_path="vector")
 
 
 def test_short_rows_with_incongruent_replicas(oracle):
