@@ -374,10 +374,9 @@ reshard_status_t reshard_selftest_wait_timeout(uint32_t polls, void* stream);
  * result is the same.  The plan need not be uploaded.
  *
  * The first call on a device looks up the arrays' device addresses
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Each call copies the plan's tables from host memory into
- * the static array with cudaMemcpyAsync on `stream` and then launches the
- * gather and slice kernels on `stream`.  No part of the arrays needs to start at
+ * (cudaGetSymbolAddress) with that device current.  Each call copies the plan's
+ * tables from host memory into the static array with cudaMemcpyAsync on
+ * `stream` and then launches the gather and slice kernels on `stream`.  No part of the arrays needs to start at
  * zero: the gather writes every byte of the global tensor before the slice reads
  * it, and the tables are rewritten by every call.
  *
