@@ -278,16 +278,16 @@ __device__ __forceinline__ void granule_move(const SegInfo& s, uint32_t meta, ui
 #pragma unroll
       for (int i = 0; i < 16 / U; ++i) *reinterpret_cast<T*>(img_at + i * U) = granule_elem<U>(v, i);
     } else {
-      // 16 bytes at any alignment: two aligned 16-byte loads and a funnel
-      const uint32_t a = uint32_t(reinterpret_cast<uintptr_t>(img_at) & 15u);
-      const unsigned char* base = img_at - a;
-      const uint4 A = *reinterpret_cast<const uint4*>(base);
-      const uint4 B = a ? *reinterpret_cast<const uint4*>(base + 16) : A;
-      const uint4 out = staging::funnel16(A, B, a >> 2, 0x3210u + 0x1111u * (a & 3u));
-      words[0] = out.x;
-      words[1] = out.y;
-      words[2] = out.z;
-      words[3] = out.w;
+      // 16 bytes at any alignment: five aligned 4-byte words funnel-shifted by the
+      // byte offset (the reads stay inside the image and its slack)
+      const uint32_t a = uint32_t(reinterpret_cast<uintptr_t>(img_at) & 3u);
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(img_at - a);
+      const uint32_t sh = 8u * a;
+      const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = sh ? w[4] : 0u;
+      words[0] = __funnelshift_r(w0, w1, sh);
+      words[1] = __funnelshift_r(w1, w2, sh);
+      words[2] = __funnelshift_r(w2, w3, sh);
+      words[3] = __funnelshift_r(w3, w4, sh);
     }
   } else {
     walk_move<U, GATHER>(img_at, s.units, L - s.units * U, plan_c(meta), lo, hi, words, v);

@@ -750,6 +750,10 @@ TRANSPOSE_CASES = [
     _spec((3, 400, 1416), "bf16", (42,), ("S2",), (5,), ("S1",), seed=11),      # gather, 68 B
     _spec((520, 583, 3), "fp16", (1,), ("S1",), (45,), ("S2",), seed=12),       # de-interleave
     _spec((700, 3), "fp16", (1,), ("R",), (2,), ("S1",), seed=13),              # 4 + 2 bytes
+    # gathers whose whole image is under one or two 16-byte granules: no bulk copy
+    # of an aligned middle, or one of a single granule, beside the threads' bytes
+    _spec((2, 6), "u8", (6,), ("S1",), (2,), ("R",), seed=14),
+    _spec((5, 6), "u8", (6,), ("S1",), (3,), ("R",), seed=15),
 ]
 
 
