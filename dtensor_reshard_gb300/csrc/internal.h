@@ -50,8 +50,9 @@ constexpr int kNumPrograms = 5;
 // through the register realigning kernel (tiles off the 16-byte grid, mostly in
 // rows of 512 bytes to 8 KiB) is assembled in one replica and then copied to the
 // others as one aligned run (RESHARD_PROGRAM_REPLICATE).  Measured on GB300, a
-// 138 MB fp32 gather of 56 pieces of 628 bytes into 15 replicas: 0.553 -> 0.386 ms.
-constexpr int64_t kAssembleFanout = 8;
+// 138 MB fp32 gather of 56 pieces of 628 bytes into 15 replicas: 0.553 -> 0.386 ms;
+// a 62 MB bf16 gather of 17 pieces of 770 bytes into 6 replicas: 0.119 -> 0.108 ms.
+constexpr int64_t kAssembleFanout = 6;
 
 // Rows shorter than this count as narrow (the element kernel keeps fewer
 // loads in flight for programs made mostly of them).

@@ -129,8 +129,9 @@ def test_transpose_rule_for_narrow_pieces(oracle, case, transposed):
     (((60, 2200), "fp32", (14,), ("S1",), (9,), ("R",)), 1),
     # two destination classes of 12 replicas each, bands of 632 bytes in 3-D: assembled
     (((2, 30, 4424), "bf16", (2, 14), ("R", "S2"), (2, 12), ("S0", "R")), 2),
-    # 7 replicas: too few
-    (((60, 2200), "fp32", (14,), ("S1",), (7,), ("R",)), 0),
+    # 6 replicas: assembled; 5: too few
+    (((60, 2200), "fp32", (14,), ("S1",), (6,), ("R",)), 1),
+    (((60, 2200), "fp32", (14,), ("S1",), (5,), ("R",)), 0),
     # bands of 640 bytes, on the 16-byte grid: the TMA fan-out takes them directly
     (((60, 2240), "fp32", (14,), ("S1",), (9,), ("R",)), 0),
     # one source region per shard (a replicated tensor): nothing to assemble
