@@ -122,6 +122,9 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
   __shared__ uint16_t row_spos[kStages][kMaxRows];
   __shared__ unsigned char* dst_ptr[kStages][kMaxGroup];
   __shared__ StageDesc desc[kStages];
+  // the chunk's row length and replica count, from the producer: the consumers and
+  // the store warp read no tile record or group table from global memory
+  __shared__ uint32_t desc_len[kStages], desc_R[kStages];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // bulk: the store warp writes whole granules from the output stages and
   // releases the input stages; otherwise the consumers write everything and
@@ -150,6 +153,8 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
     Chunk c;
     int stage_tile[kStages];
     for (int s = 0; s < kStages; ++s) stage_tile[s] = -1;
+    int cur_tile = -1;
+    uint32_t g0 = 0, R = 0;  // the current tile's destination group
     bool ok = true;
     const int64_t npieces = sched.count();
     uint32_t piece = grab_piece(queue, lane);
@@ -166,18 +171,25 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
         break;
       }
       const reshard_tile_t& t = w.t;
-      if (lane == 0) desc[s] = StageDesc{c.ti, c.kind, c.bytes, c.a, c.b};
+      if (c.ti != cur_tile) {
+        g0 = p.goff[t.dst_group];
+        R = p.goff[t.dst_group + 1] - g0;
+        cur_tile = c.ti;
+      }
+      const uint32_t nr = c.kind == 1 ? uint32_t(c.b - c.a) : 1u;
+      const uint32_t len = c.kind == 1 ? t.row_bytes : c.bytes;
+      if (lane == 0) {
+        desc[s] = StageDesc{c.ti, c.kind, c.bytes, c.a, c.b};
+        desc_len[s] = len;
+        desc_R[s] = R;
+      }
       if (stage_tile[s] != c.ti) {
         // the stage's destination pointers (the stage's last readers are done)
-        const uint32_t g0 = p.goff[t.dst_group];
-        const int R = int(p.goff[t.dst_group + 1] - g0);
-        for (int i = lane; i < R; i += 32) dst_ptr[s][i] = p.bufs[p.gbuf[g0 + i]];
+        for (uint32_t i = lane; i < R; i += 32) dst_ptr[s][i] = p.bufs[p.gbuf[g0 + i]];
         stage_tile[s] = c.ti;
       }
       const unsigned char* src = p.bufs[t.src_buf];
       unsigned char* stage = in_mem + size_t(s) * kStageBytes;
-      const uint32_t nr = c.kind == 1 ? uint32_t(c.b - c.a) : 1u;
-      const uint32_t len = c.kind == 1 ? t.row_bytes : c.bytes;
       if (c.kind != 1 || Walker::source_contiguous(t)) {
         // one copy: the chunk's bytes are contiguous in the source
         const unsigned char* sa = c.kind == 0   ? src + t.src_off + c.a
@@ -260,8 +272,6 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
   } else if (warp < kStoreWarp) {
     // ------------------------------------------------------------ consumers
     const uint32_t ct = threadIdx.x - 32;
-    int cur_tile = -1;
-    reshard_tile_t t = {};
     while (true) {
       const int s = int(n % kStages), o = int(n % kOutStages);
       if (!warp_wait(&full[s], (n / kStages) & 1u) ||
@@ -276,13 +286,9 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
         if (bulk && lane == 0) mbar_arrive(&out_full[o]);
         break;
       }
-      if (c.ti != cur_tile) {
-        t = p.tiles[c.ti];
-        cur_tile = c.ti;
-      }
-      const int R = int(p.goff[t.dst_group + 1] - p.goff[t.dst_group]);
+      const int R = int(desc_R[s]);
       const uint32_t nr = c.kind == 1 ? uint32_t(c.b - c.a) : 1u;
-      const uint32_t len = c.kind == 1 ? t.row_bytes : c.bytes;
+      const uint32_t len = desc_len[s];
       const uint32_t gmax = (len + 30u) >> 4;  // granules a row of len bytes can touch
       const uint32_t ost = Walker::out_stride(len);
       const unsigned char* stage = in_mem + size_t(s) * kStageBytes;
@@ -354,8 +360,6 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
     }
   } else if (bulk) {
     // ------------------------------------------------------------ store warp
-    int cur_tile = -1;
-    reshard_tile_t t = {};
     while (true) {
       const int s = int(n % kStages), o = int(n % kOutStages);
       if (!warp_wait(&out_full[o], (n / kOutStages) & 1u)) {
@@ -364,13 +368,9 @@ __global__ void __launch_bounds__(Config<BULK>::kThreads)
       }
       const StageDesc c = desc[s];
       if (c.ti < 0) break;
-      if (c.ti != cur_tile) {
-        t = p.tiles[c.ti];
-        cur_tile = c.ti;
-      }
-      const uint32_t R = p.goff[t.dst_group + 1] - p.goff[t.dst_group];
+      const uint32_t R = desc_R[s];
       const uint32_t nr = c.kind == 1 ? uint32_t(c.b - c.a) : 1u;
-      const uint32_t len = c.kind == 1 ? t.row_bytes : c.bytes;
+      const uint32_t len = desc_len[s];
       const uint32_t ost = Walker::out_stride(len);
       const unsigned char* out = out_mem + size_t(o) * kStageBytes;
       unsigned char* const* dptr = dst_ptr[s];
