@@ -775,6 +775,8 @@ ASSEMBLE_CASES = [
     _spec((600, 2200), "fp32", (14,), ("S1",), (9,), ("R",), seed=21),
     _spec((393, 8780), "fp32", (56,), ("S1",), (15,), ("R",), seed=22),
     _spec((2, 300, 4424), "bf16", (2, 14), ("R", "S2"), (3, 12), ("S0", "R"), seed=23),
+    # 6 replicas (the smallest fan-out that is assembled) of 770-byte column bands
+    _spec((300, 6538), "bf16", (17,), ("S1",), (6,), ("R",), seed=24),
 ]
 
 
