@@ -294,20 +294,6 @@ __device__ __forceinline__ void granule_move(const SegInfo& s, uint32_t meta, ui
   }
 }
 
-// a[i] for a run-time i (< N) by a chain of selects, so that a rolled loop over
-// the slots keeps them in registers.  The scatter's slot loop is rolled: its body
-// (every granule kind, inlined) is then emitted once instead of once per slot,
-// and its warps, at different slots, no longer stall on instruction fetch.  The
-// gather's stays unrolled (its granule loads of several slots are in flight at
-// once, and it was measured faster so).
-template <int N>
-__device__ __forceinline__ uint32_t pick(const uint32_t (&a)[N], int i) {
-  uint32_t r = a[0];
-#pragma unroll
-  for (int q = 1; q < N; ++q) r = i == q ? a[q] : r;
-  return r;
-}
-
 // A bulk copy shared -> global whose lines L2 evicts first: a gather's image goes
 // out once to each replica and is not read again, while the narrow source's
 // boundary granules are read again by the next block (with the normal policy the
@@ -681,6 +667,16 @@ __global__ void __launch_bounds__(kTThreads, 4)
       const uint4 none = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
       for (int sl = 0; sl < kSlots; ++sl) {
+        // The loop is rolled: its body, with every granule kind inlined, exists once
+        // instead of once per slot (unrolled, the warps stalled on instruction
+        // fetch; the gather's loop stays unrolled, its loads of several slots in
+        // flight together).  This slot's plan is plan[0]: rotating the plans left
+        // each slot (kSlots rotations restore their order for the next block) keeps
+        // them in registers at one move each.
+        const uint32_t meta = plan[0];
+#pragma unroll
+        for (int q = 0; q + 1 < kSlots; ++q) plan[q] = plan[q + 1];
+        plan[kSlots - 1] = meta;
         if (sl == 1) {
           // this thread's partial granule (threads < 2 K), between its planned ones so
           // that it overlaps the other warps' work
@@ -697,7 +693,6 @@ __global__ void __launch_bounds__(kTThreads, 4)
             }
           }
         }
-        const uint32_t meta = pick(plan, sl);
         if (plan_kind(meta) == kKindNone) continue;
         const SegInfo& s = si[plan_k(meta)];
         const uint32_t j = threadIdx.x + uint32_t(sl) * kTThreads - s.gstart;
